@@ -1,0 +1,376 @@
+"""Benchmark of the batch-invariant decode step on GB300.
+
+One "step" is one batched decode step of one dense decoder layer shaped like a
+~27B model (hidden 5120, 40 query / 8 KV heads, head_dim 128, SwiGLU 17408,
+every projection q8_0) for 4 sequences at 2,051 keys each: RMSNorm ->
+quantize -> QKV matvec -> RoPE + KV append -> split-K attention -> quantize ->
+O matvec -> RMSNorm -> quantize -> gate||up matvec -> SwiGLU -> quantize ->
+down matvec.  Inputs are seeded synthetic data resident in HBM; the L2 is
+flushed (a 256 MiB write) between steps, outside the timed events.
+
+Prints ONE JSON line.  `value` = aggregate decode tok/s (rows per second) at
+n_seq = 4; the q8_0 matvec's HBM GB/s (the other half of the metric) is in
+`roofline` (dominant kernel) and `detail`.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle on the same workload (host cores).
+Under torchrun each rank runs an independent replica (no collective).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "q8_0 narrow-batch matvec HBM GB/s; aggregate decode tok/s at n_seq=1..4"
+FALLBACK_HBM_GBS = 6800.0
+KV_TOKENS = 2051
+LAYER_FIELDS = ["attn_norm", "wqkv_q", "wqkv_d", "wo_q", "wo_d", "ffn_norm", "wgu_q", "wgu_d", "wdown_q", "wdown_d"]
+
+
+def workload_config(n_seq: int) -> dict:
+    from invariant_sequence_decode_gb300 import workloads as wl
+    d = wl.LAYER27B
+    return {"workload": "one dense decoder layer decode step (~27B shape), q8_0 projections, "
+                        f"{n_seq} sequences x 1 row at {KV_TOKENS} keys of f16 KV",
+            "hidden": d.hidden, "n_q_heads": d.n_q_heads, "n_kv_heads": d.n_kv_heads, "head_dim": d.head_dim,
+            "ffn": d.ffn, "n_seq": n_seq, "rows": n_seq, "kv_tokens": KV_TOKENS, "seed": 1,
+            "l2": "flushed between steps (256 MiB write, outside the timed events)"}
+
+
+def layer_bytes(d) -> int:
+    """Algorithmic weight bytes of one layer: N*K*(34/32) per q8_0 projection."""
+    H, Hq, Hkv, D, F = d.hidden, d.n_q_heads, d.n_kv_heads, d.head_dim, d.ffn
+    nk = (Hq + 2 * Hkv) * D * H + H * Hq * D + 2 * F * H + H * F
+    return nk * 34 // 32
+
+
+def peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            j = json.load(open(p))
+            for k in ("hbm_gbs", "hbm_GBps", "hbm"):
+                if k in j:
+                    return {"hbm_gbs": float(j[k]), "source": "of measured"}
+        except Exception:
+            pass
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "of fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi sampling (200 ms) while the GPU is under load."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.p = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.p is not None:
+            self.p.terminate()
+            try:
+                self.out, _ = self.p.communicate(timeout=5)
+            except Exception:
+                self.p.kill()
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "out", "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ our arm
+
+class Layer27B:
+    """Device-resident weights, caches and buffers of the one-layer workload."""
+
+    def __init__(self, torch, luce, wl, n_seq_max=4, seed=1):
+        self.torch, self.luce = torch, luce
+        d = wl.LAYER27B
+        self.d = d
+        self.host = wl.layer_host(seed, 0, d)
+        cu = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+        self.layer = luce.LayerTensors(*[cu(getattr(self.host, f)) for f in LAYER_FIELDS])
+        self.model = luce.Model([self.layer], d.hidden, d.n_q_heads, d.n_kv_heads, d.ffn)
+        self.cap = KV_TOKENS
+        self.len = KV_TOKENS - 1
+        self.slots = []
+        self.caches_host = []
+        for s in range(n_seq_max):
+            k, v = wl.cache_host(seed, s, 0, d, self.cap, self.len)
+            self.caches_host.append((k, v))
+            self.slots.append(luce.Slot(cu(k[None]), cu(v[None]), self.len))
+        self.x_host = wl.acts(seed, n_seq_max, d.hidden, sub=9)
+        self.x = cu(self.x_host)
+        self.ws = self.model.workspace(n_seq_max, self.cap)
+        self.flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+
+    def step(self, n_seq: int, x=None):
+        self.luce.luce_decode_step(self.model, self.slots[:n_seq], [1] * n_seq,
+                                   self.x[:n_seq] if x is None else x, self.ws)
+
+    def flush_l2(self):
+        self.flush.fill_(1)
+
+
+def time_steps(torch, fn, flush, k: int) -> list:
+    """Per-step device milliseconds (CUDA events on the launching stream)."""
+    st = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(k)]
+    for a, b in ev:
+        flush()
+        a.record(st)
+        fn()
+        b.record(st)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def matvec_roofline(torch, luce, wl, L: Layer27B, T: int, reps: int) -> dict:
+    """Standalone timing of the four projections of the layer at T rows."""
+    d = L.d
+    H, Hq, Hkv, D, F = d.hidden, d.n_q_heads, d.n_kv_heads, d.head_dim, d.ffn
+    shapes = [("qkv", L.layer.wqkv_q, L.layer.wqkv_d, (Hq + 2 * Hkv) * D, H),
+              ("o", L.layer.wo_q, L.layer.wo_d, H, Hq * D),
+              ("gate_up", L.layer.wgu_q, L.layer.wgu_d, 2 * F, H),
+              ("down", L.layer.wdown_q, L.layer.wdown_d, H, F)]
+    out = {}
+    tot_b, tot_ms = 0, 0.0
+    for name, wq, wdd, N, K in shapes:
+        x = torch.from_numpy(wl.acts(3, T, K, sub=5)).cuda()
+        aq, ad = luce.luce_q8_quantize_act(x)
+        y = torch.empty((T, N), dtype=torch.float32, device="cuda")
+        fn = lambda: luce.luce_q8_matvec_batch(wq, wdd, aq, ad, y)
+        for _ in range(3):
+            fn()
+        ms = statistics.mean(time_steps(torch, fn, L.flush_l2, reps))
+        b = N * K * 34 // 32 + T * K + T * (K // 32) * 4 + T * N * 4
+        out[name] = {"N": N, "K": K, "ms": ms, "gbps": b / ms / 1e6}
+        tot_b += b
+        tot_ms += ms
+    out["all"] = {"bytes": tot_b, "ms": tot_ms, "gbps": tot_b / tot_ms / 1e6}
+    return out
+
+
+def cpu_baseline_oracle(wl, L_host, caches_host, x_host, n_seq: int) -> dict:
+    import oracle
+    d = wl.LAYER27B
+    lw = oracle.LayerWeights(*[getattr(L_host, f) for f in LAYER_FIELDS])
+    dims = oracle.Dims(d.hidden, d.n_q_heads, d.n_kv_heads, d.head_dim, d.ffn)
+    slots = [oracle.Slot(k.view(np.uint16).copy(), v.view(np.uint16).copy(), KV_TOKENS - 1)
+             for k, v in caches_host[:n_seq]]
+    t0 = time.perf_counter()
+    oracle.decode_layer(x_host[:n_seq], lw, dims, slots, [1] * n_seq)
+    dt = time.perf_counter() - t0
+    return {"value": n_seq / dt, "unit": "tok/s", "cores": 1, "kind": "oracle",
+            "sample": f"one full decode step of the layer ({n_seq} rows) by the single-threaded C oracle "
+                      f"({dt:.2f} s)"}
+
+
+def run_ours(args, rank: int, world: int, local_rank: int):
+    import torch
+    import invariant_sequence_decode_gb300 as luce
+    from invariant_sequence_decode_gb300 import build, workloads as wl
+    build.build()
+    luce.load_library()
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    L = Layer27B(torch, luce, wl)
+    n_seq = 4
+    for _ in range(args.warmup):
+        L.flush_l2()
+        L.step(n_seq)
+    torch.cuda.synchronize()
+
+    with ClockSampler(local_rank) as clk:
+        # untimed load so the sampler sees the clocks under this workload
+        t_end = time.perf_counter() + 1.0
+        while time.perf_counter() < t_end:
+            for _ in range(20):
+                L.step(n_seq)
+            torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        c0 = luce.launch_count()
+        w0 = time.perf_counter()
+        step_ms = time_steps(torch, lambda: L.step(n_seq), L.flush_l2, args.steps)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - w0
+        launches = luce.launch_count() - c0
+        if dist:
+            dist.barrier()
+    total_ms = sum(step_ms)
+    ms_per_step = total_ms / args.steps
+    if dist:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+        ms_per_step = total_ms / args.steps
+    rows_total = n_seq * args.steps * world
+    value = rows_total / (total_ms / 1e3)
+
+    # aggregate tok/s at n_seq = 1..3 and the k-solo-launch arm (untimed in the contract, reported)
+    detail = {"tok_s_by_n_seq": {}, "solo_launches_tok_s": {}, "step_ms_by_n_seq": {}}
+    for k in (1, 2, 3, 4):
+        ms = statistics.median(time_steps(torch, lambda: L.step(k), L.flush_l2, max(5, args.steps)))
+        detail["tok_s_by_n_seq"][str(k)] = k / (ms / 1e3)
+        detail["step_ms_by_n_seq"][str(k)] = ms
+
+        def solo():
+            for s in range(k):
+                L.luce.luce_decode_step(L.model, [L.slots[s]], [1], L.x[s:s + 1], L.ws)
+        ms_s = statistics.median(time_steps(torch, solo, L.flush_l2, max(5, args.steps)))
+        detail["solo_launches_tok_s"][str(k)] = k / (ms_s / 1e3)
+
+    mv = {}
+    for T in (1, 2, 3, 4, 8, 12, 16):
+        mv[str(T)] = matvec_roofline(torch, luce, wl, L, T, reps=10)
+    detail["matvec_gbps_by_ntok"] = {T: round(v["all"]["gbps"], 1) for T, v in mv.items()}
+    detail["matvec_by_proj_ntok4"] = {k: {"gbps": round(v["gbps"], 1), "us": round(v["ms"] * 1e3, 2)}
+                                      for k, v in mv["4"].items() if k != "all"}
+    detail["layer_weight_bytes"] = layer_bytes(L.d)
+    detail["step_bytes_algorithmic"] = layer_bytes(L.d) + n_seq * 2 * L.d.n_kv_heads * KV_TOKENS * 128 * 2
+    detail["step_gbps"] = detail["step_bytes_algorithmic"] / (ms_per_step / 1e3) / 1e9
+
+    pk = peaks()
+    a = mv["4"]["all"]["gbps"]
+    roofline = {"bound": "hbm", "kernel": "q8_matvec_kernel (the four projections of the layer, n_tok=4)",
+                "achieved": round(a, 1), "peak": pk["hbm_gbs"], "peak_source": pk["source"], "unit": "GB/s",
+                "frac": round(a / pk["hbm_gbs"], 4), "frac_of_8tbs_nominal": round(a / 8000.0, 4),
+                "traffic": None}
+
+    # end to end through the public API with host buffers: pinned H2D of the
+    # step's rows, the step, D2H of its output rows
+    xh = torch.from_numpy(L.x_host[:n_seq].copy()).pin_memory()
+    outh = torch.empty_like(xh).pin_memory()
+    xd = torch.empty((n_seq, L.d.hidden), dtype=torch.float32, device="cuda")
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        L.flush_l2()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        xd.copy_(xh, non_blocking=True)
+        L.step(n_seq, xd)
+        outh.copy_(xd, non_blocking=True)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append((time.perf_counter() - t0) * 1e3)
+    e2e_total = sum(e2e_ms)
+    if dist:
+        t = torch.tensor([e2e_total], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_total = float(t.item())
+    e2e = {"value": n_seq * args.steps * world / (e2e_total / 1e3), "unit": "tok/s",
+           "h2d_bytes_per_step": int(xh.numel() * 4), "d2h_bytes_per_step": int(outh.numel() * 4)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_oracle(wl, L.host, L.caches_host, L.x_host, n_seq)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 2), "unit": "tok/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "int8xint8->int32, fp32", "data": "synthetic (seeded SplitMix64; q8_0 weights, f16 KV)",
+                "config": {**workload_config(n_seq), "parallelism": f"replicas x{world}"},
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
+                "clocks": clk.summary(), "wall_s_timed_region": round(wall, 4), "detail": detail}
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args, rank: int, world: int):
+    if rank != 0:
+        return
+    from invariant_sequence_decode_gb300 import workloads as wl
+    import oracle
+    oracle.build()
+    n_seq = 4
+    d = wl.LAYER27B
+    L_host = wl.layer_host(1, 0, d)
+    caches = [wl.cache_host(1, s, 0, d, KV_TOKENS, KV_TOKENS - 1) for s in range(n_seq)]
+    x = wl.acts(1, n_seq, d.hidden, sub=9)
+    for _ in range(args.warmup):
+        cpu_baseline_oracle(wl, L_host, caches, x, n_seq)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        r = cpu_baseline_oracle(wl, L_host, caches, x, n_seq)
+    dt = time.perf_counter() - t0
+    value = n_seq * args.steps / dt
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tok/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8xint8->int64, f64",
+            "data": "synthetic (seeded SplitMix64; q8_0 weights, f16 KV)",
+            "config": {**workload_config(n_seq), "parallelism": "host cores, oracle"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "tok/s", "cores": 1, "kind": "oracle",
+                             "sample": r["sample"]},
+            "e2e": {"value": round(value, 4), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,240 @@
+/*
+ * luce.h - C ABI of the batch-invariant concurrent decode step for GB300 (sm_103a).
+ *
+ * One decode step serves 1..4 sequences ("slots"); each slot contributes 1..4
+ * rows (1 for plain decode, up to 4 when it verifies draft tokens), at most 16
+ * rows in all.  Every projection reads the q8_0 weights once for all rows,
+ * and every row comes out bit-identical to the same slot run alone: no
+ * reduction order anywhere depends on the number of rows, on the other rows,
+ * on their order or on the launch grid.
+ *
+ * Sources, cited by page title and section:
+ *   [exact-4-slot]  "feat(qwen4exp): exact 4-slot concurrent serving",
+ *                   sections "What" and "How it stays exact".
+ *   [qfuse]         "#1209 Speed up concurrent generation, fix QFUSE, and
+ *                   improve prefill monitoring", "What changed and why".
+ *   [ds4-604]       antirez/ds4 pull 604, section 2 ("Single-GPU decode
+ *                   batches don't scale") and "Commit walkthrough".
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked (device) are CUDA device pointers; (host) are host
+ *     pointers read during the call only.  The caller allocates and owns
+ *     every buffer; the library allocates nothing and never synchronises the
+ *     host.  Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream) and is complete when that stream is.
+ *   - Return value: LUCE_OK (0) or a negative luce_status.  On error nothing
+ *     has been enqueued, except LUCE_ECUDA from a failed launch.
+ *     luce_last_error() gives a message for the calling thread's last error.
+ *   - binary16 data (fp16 weight scales, the K/V cache) is passed as uint16_t
+ *     payloads.  q8_0 weights are stored as int8 wq[N][K] (row-major) plus
+ *     binary16 wd[N][K/32]: 32 weights per block share one scale, 34 bytes
+ *     per block in all.
+ *   - Alignment: int8 rows and K/V rows start on 16-byte boundaries.
+ */
+#ifndef LUCE_H
+#define LUCE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum luce_status {
+    LUCE_OK = 0,
+    LUCE_EINVAL = -1,       /* a null/misaligned pointer or an out-of-range size */
+    LUCE_EUNSUPPORTED = -2, /* a shape the kernels do not serve (e.g. head_dim != 128) */
+    LUCE_ECUDA = -3,        /* a CUDA launch failed */
+    LUCE_ENOSPACE = -4      /* the workspace is smaller than required */
+} luce_status;
+
+#define LUCE_QK 32               /* q8_0 block length [ds4-604, Commit walkthrough] */
+#define LUCE_MAX_SEQ 4           /* slots per step; more are refused [exact-4-slot, What] */
+#define LUCE_MAX_ROWS_PER_SEQ 4  /* rows per slot (1 decode + up to 3 drafts) */
+#define LUCE_MAX_ROWS 16         /* 8/12/16-row verify capacities [qfuse, item 1] */
+#define LUCE_HEAD_DIM 128
+#define LUCE_ATTN_CHUNK 256      /* keys per split-K chunk of decode attention */
+
+/* Message of the calling thread's last non-OK status ("" if none). */
+const char* luce_last_error(void);
+
+/* ABI version (major * 10000 + minor * 100 + patch). */
+int luce_version(void);
+
+/* Number of kernel launches this library has enqueued since it was loaded
+ * (all threads).  A diagnostic for counting the work a call submits. */
+uint64_t luce_launch_count(void);
+
+/*
+ * Activation quantization to q8_0 blocks [qfuse, item 2: the consumer's
+ * division and rounding convention; ds4-604, Commit walkthrough].
+ * For each row t and block b of 32 values: amax = max|x| (NaN skipped),
+ * d = amax / 127 (fp32, IEEE division), q = round(x / d) with an IEEE fp32
+ * division and rounding half away from zero, clamped to [-127, 127]; a block
+ * with d == 0 gives all-zero codes and a NaN quotient gives 0.
+ *   x  (device) fp32 [T][ldx], first K columns used (ldx >= K)
+ *   q  (device) int8 [T][K], 16-byte aligned
+ *   d  (device) fp32 [T][K/32]
+ * 1 <= T <= LUCE_MAX_ROWS (any T >= 1 is accepted), K % 32 == 0.
+ */
+int luce_q8_quantize_act(const float* x, int T, int K, int64_t ldx, int8_t* q, float* d, void* stream);
+
+/*
+ * Narrow-batch q8_0 matvec [ds4-604, Commit walkthrough: each 32-weight
+ * block read once and dotted against all tokens; exact-4-slot, How it stays
+ * exact: the same arithmetic for 1 row as for 4]:
+ *   y[t][n] = sum_b (wd[n][b] * ad[t][b]) * sum_i wq[n][32b+i] * aq[t][32b+i]
+ * The per-block sum is an exact int32.  The fp32 combine of a row uses a fixed
+ * order that depends on K only: block b feeds partial sum (b mod 32), each
+ * partial adds its blocks in ascending order with fused multiply-adds, and the
+ * 32 partials are summed pairwise by an xor butterfly over offsets
+ * 16, 8, 4, 2, 1.  Hence y[t][.] is bitwise independent of T, of the other
+ * rows and of the launch shape.
+ *   wq (device) int8 [N][K], 16-byte aligned;  wd (device) binary16 [N][K/32]
+ *   aq (device) int8 [T][K], 16-byte aligned;  ad (device) fp32 [T][K/32]
+ *   y  (device) fp32 [T][ldy] (ldy >= N)
+ * 1 <= T <= LUCE_MAX_ROWS, K % 32 == 0, N >= 1.
+ */
+int luce_q8_matvec_batch(const int8_t* wq, const uint16_t* wd, int N, int K,
+                         const int8_t* aq, const float* ad, int T, float* y, int64_t ldy, void* stream);
+
+/*
+ * Per-block integer dots out[t][n][b] = sum_i wq[n][32b+i] * aq[t][32b+i],
+ * computed by the matvec kernel's own dot routine (exposed so the exactness
+ * of the integer stage can be checked).  out (device) int32 [T][N][K/32].
+ */
+int luce_q8_block_dots(const int8_t* wq, int N, int K, const int8_t* aq, int T, int32_t* out, void* stream);
+
+/*
+ * Pos-vector RoPE [ds4-604, Commit walkthrough: decode tokens of different
+ * sequences sit at arbitrary positions; a row equals a single-row launch at
+ * its own position].  Dims (i, i + D/2) of every head of row t rotate by
+ * pos[t] * theta^(-2i/D).  The cosine and sine are evaluated in double
+ * precision and rounded to fp32; the rotation itself is fp32.
+ *   x   (device) fp32, element (t, h, d) at t*ldx + h*D + d, rotated in place
+ *   pos (device) int32 [T]
+ * D == 128, 1 <= T <= LUCE_MAX_ROWS (any T >= 1 is accepted), n_heads >= 1,
+ * ldx >= n_heads * D.
+ */
+int luce_rope_posvec(float* x, int T, int n_heads, int D, int64_t ldx, const int32_t* pos,
+                     double theta, void* stream);
+
+/*
+ * A sequence's view of its K/V cache for one layer [ds4-604, Commit
+ * walkthrough: per-sequence view passed by value, max 4].  Element (g, j, d)
+ * of K (and V) is at k[g*head_stride + j*tok_stride + d], binary16.
+ * `len` counts the keys including this step's n_q rows: row j (0..n_q-1) of
+ * the sequence is at position len - n_q + j and attends to keys
+ * [0, len - n_q + j].  Its query/output row is row0 + j.
+ */
+typedef struct luce_seqview {
+    uint16_t* k;          /* (device) */
+    uint16_t* v;          /* (device) */
+    int32_t len;
+    int32_t n_q;          /* 1..LUCE_MAX_ROWS_PER_SEQ */
+    int32_t row0;
+    int32_t cap;          /* positions the view holds (len <= cap) */
+    int64_t head_stride;  /* elements, multiple of 8 */
+    int64_t tok_stride;   /* elements, multiple of 8, >= D */
+} luce_seqview;
+
+/*
+ * Per-sequence KV append [ds4-604, section 2: KV append runs per sequence
+ * with the single-token helpers].  Row row0 + j of k and v (fp32, element
+ * (t, g, d) at t*ldkv + g*D + d) is rounded to binary16 (nearest even) and
+ * written at position len - n_q + j of that view's cache.
+ *   views (host) [n_seq], 1 <= n_seq <= LUCE_MAX_SEQ.
+ */
+int luce_kv_append(const float* k, const float* v, int64_t ldkv, int Hkv, int D,
+                   const luce_seqview* views, int n_seq, void* stream);
+
+/*
+ * Multi-sequence decode attention [ds4-604, Commit walkthrough: one query
+ * token per sequence against its own cache; here up to 4 causal rows per
+ * sequence].  For row r of view s and query head h (KV head g = h / (Hq/Hkv)):
+ *   out[r][h] = sum_j softmax_j(scale * q[r][h] . K[g][j]) V[g][j]
+ * over the row's keys.  The keys are split into fixed chunks of
+ * LUCE_ATTN_CHUNK (a function of the row's own key count only); each chunk
+ * yields (max, sum, unnormalised output) and the chunks are merged in order
+ * by the exact log-sum-exp rule.  No output depends on the other rows.
+ *   q   (device) fp32 [T][Hq][D] with T = max(row0 + n_q)
+ *   out (device) fp32 [T][Hq][D]
+ *   ws  (device) scratch of at least luce_decode_attn_workspace_size(...) bytes
+ * D == 128, Hq % Hkv == 0, Hq / Hkv <= 8, 1 <= n_seq <= LUCE_MAX_SEQ,
+ * 1 <= len - n_q + 1, len <= cap.
+ */
+int luce_decode_attn_multiseq(const float* q, const luce_seqview* views, int n_seq,
+                              int Hq, int Hkv, int D, float scale, float* out,
+                              void* ws, size_t ws_bytes, void* stream);
+
+/* Bytes of scratch luce_decode_attn_multiseq needs for n_rows rows whose key
+ * counts are at most max_len. */
+size_t luce_decode_attn_workspace_size(int n_rows, int Hq, int D, int max_len);
+
+/* ---------------------------------------------------------------- decode step */
+
+/* One pre-norm decoder layer, all projections q8_0 (device pointers). */
+typedef struct luce_layer {
+    const float* attn_norm;                          /* [hidden] */
+    const int8_t* wqkv_q; const uint16_t* wqkv_d;    /* [(Hq + 2 Hkv) D][hidden]: q rows, k rows, v rows */
+    const int8_t* wo_q;   const uint16_t* wo_d;      /* [hidden][Hq D] */
+    const float* ffn_norm;                           /* [hidden] */
+    const int8_t* wgu_q;  const uint16_t* wgu_d;     /* [2 ffn][hidden]: gate rows first, then up */
+    const int8_t* wdown_q; const uint16_t* wdown_d;  /* [hidden][ffn] */
+} luce_layer;
+
+typedef struct luce_model {
+    int32_t n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab; /* vocab 0: no head */
+    float rms_eps;
+    double rope_theta;
+    const luce_layer* layers;                        /* (host) [n_layers] */
+    const float* final_norm;                         /* (device) [hidden], when vocab > 0 */
+    const int8_t* head_q; const uint16_t* head_d;    /* (device) [vocab][hidden], when vocab > 0 */
+} luce_model;
+
+/* A slot's K/V cache for all layers: binary16 [n_layers][n_kv_heads][cap][head_dim]. */
+typedef struct luce_slot {
+    uint16_t* k;    /* (device) */
+    uint16_t* v;    /* (device) */
+    int32_t len;    /* tokens already cached before this step */
+    int32_t cap;
+} luce_slot;
+
+/* Byte offsets of the step's intermediates inside its workspace (the last
+ * layer's values remain there after the call; useful for inspection). */
+typedef struct luce_step_layout {
+    size_t rope_cs, xn, xn_q, xn_d, qkv, q_rot, part, attn, attn_q, attn_d, x1,
+           xn2, xn2_q, xn2_d, gu, h, h_q, h_d, xf, xf_q, xf_d, total;
+} luce_step_layout;
+
+/* Workspace layout for n_rows rows and caches of at most max_ctx positions. */
+int luce_decode_step_layout(const luce_model* m, int n_rows, int max_ctx, luce_step_layout* out);
+
+/*
+ * One batched decode step through every layer [ds4-604, section 2: the dense
+ * projections run once on the shared batch workspace with n_tokens = count,
+ * KV append per sequence, one multi-sequence attention launch; logits land
+ * one row per sequence].  slots (host) [n_seq] and rows_per_slot (host)
+ * [n_seq]: slot s owns rows_per_slot[s] consecutive rows of x, in call order,
+ * its row j at position slots[s].len + j.  For each layer:
+ *   x1 = x + Wo . attn(rope(Wq . q8(norm(x))), cache)     (K/V rows appended)
+ *   x  = x1 + Wdown . q8(silu(Wgate . q8(norm(x1))) * (Wup . q8(norm(x1))))
+ * then, when vocab > 0 and logits/argmax are given, logits = Whead .
+ * q8(norm(x)) and argmax (lowest index on ties).
+ *   x      (device) fp32 [T][hidden], in: this step's hidden rows; out: the
+ *          hidden state after the last layer
+ *   logits (device) fp32 [T][vocab] or NULL;  argmax (device) int32 [T] or NULL
+ * The cache rows [len, len + rows) of every listed slot are written; slots
+ * are not otherwise touched and `len` is not updated (the caller commits the
+ * accepted prefix).  1 <= n_seq <= LUCE_MAX_SEQ (5 or more is refused),
+ * rows per slot 1..LUCE_MAX_ROWS_PER_SEQ, len + rows <= cap <= max_ctx of ws.
+ */
+int luce_decode_step(const luce_model* m, const luce_slot* slots, const int32_t* rows_per_slot,
+                     int n_seq, float* x, float* logits, int32_t* argmax,
+                     void* ws, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LUCE_H */

@@ -1,0 +1,307 @@
+"""Batch-invariant concurrent decode step for GB300 (sm_103a).
+
+Thin Python binding over ``libluce.so`` (the C ABI declared in
+``include/luce.h``).  Functions take torch CUDA tensors, check dtypes and
+layouts, and pass raw pointers and the current CUDA stream to the library:
+argument marshalling only, every step of the path runs in the library's CUDA
+kernels.  There is no fallback: a missing library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import List, Optional, Sequence
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libluce.so")
+
+QK = 32
+MAX_SEQ = 4
+MAX_ROWS_PER_SEQ = 4
+MAX_ROWS = 16
+HEAD_DIM = 128
+ATTN_CHUNK = 256
+
+LUCE_OK, LUCE_EINVAL, LUCE_EUNSUPPORTED, LUCE_ECUDA, LUCE_ENOSPACE = 0, -1, -2, -3, -4
+
+
+class LuceError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"luce status {status}: {msg}")
+        self.status = status
+
+
+# ------------------------------------------------------------ ctypes mirror of luce.h
+
+class SeqViewC(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("len", ctypes.c_int32),
+                ("n_q", ctypes.c_int32), ("row0", ctypes.c_int32), ("cap", ctypes.c_int32),
+                ("head_stride", ctypes.c_int64), ("tok_stride", ctypes.c_int64)]
+
+
+class LayerC(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "attn_norm", "wqkv_q", "wqkv_d", "wo_q", "wo_d", "ffn_norm", "wgu_q", "wgu_d", "wdown_q", "wdown_d")]
+
+
+class ModelC(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int32), ("hidden", ctypes.c_int32), ("n_q_heads", ctypes.c_int32),
+                ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("ffn", ctypes.c_int32),
+                ("vocab", ctypes.c_int32), ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_double),
+                ("layers", ctypes.POINTER(LayerC)), ("final_norm", ctypes.c_void_p),
+                ("head_q", ctypes.c_void_p), ("head_d", ctypes.c_void_p)]
+
+
+class SlotC(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("len", ctypes.c_int32), ("cap", ctypes.c_int32)]
+
+
+_LAYOUT_FIELDS = ("rope_cs", "xn", "xn_q", "xn_d", "qkv", "q_rot", "part", "attn", "attn_q", "attn_d", "x1",
+                  "xn2", "xn2_q", "xn2_d", "gu", "h", "h_q", "h_d", "xf", "xf_q", "xf_d", "total")
+
+
+class StepLayoutC(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in _LAYOUT_FIELDS]
+
+
+EXPORTS = ("luce_last_error", "luce_version", "luce_launch_count", "luce_q8_quantize_act", "luce_q8_matvec_batch",
+           "luce_q8_block_dots", "luce_rope_posvec", "luce_kv_append", "luce_decode_attn_multiseq",
+           "luce_decode_attn_workspace_size", "luce_decode_step_layout", "luce_decode_step")
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libluce.so (built by ``invariant_sequence_decode_gb300.build``).  Raises if missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is not built; run `python -m invariant_sequence_decode_gb300.build`")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, sz, f32, f64 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t,
+                                  ctypes.c_float, ctypes.c_double)
+    lib.luce_last_error.restype = ctypes.c_char_p
+    lib.luce_last_error.argtypes = []
+    lib.luce_version.restype = i32
+    lib.luce_launch_count.restype = ctypes.c_uint64
+    lib.luce_launch_count.argtypes = []
+    lib.luce_q8_quantize_act.argtypes = [vp, i32, i32, i64, vp, vp, vp]
+    lib.luce_q8_matvec_batch.argtypes = [vp, vp, i32, i32, vp, vp, i32, vp, i64, vp]
+    lib.luce_q8_block_dots.argtypes = [vp, i32, i32, vp, i32, vp, vp]
+    lib.luce_rope_posvec.argtypes = [vp, i32, i32, i32, i64, vp, f64, vp]
+    lib.luce_kv_append.argtypes = [vp, vp, i64, i32, i32, ctypes.POINTER(SeqViewC), i32, vp]
+    lib.luce_decode_attn_multiseq.argtypes = [vp, ctypes.POINTER(SeqViewC), i32, i32, i32, i32, f32, vp, vp, sz, vp]
+    lib.luce_decode_attn_workspace_size.argtypes = [i32, i32, i32, i32]
+    lib.luce_decode_attn_workspace_size.restype = sz
+    lib.luce_decode_step_layout.argtypes = [ctypes.POINTER(ModelC), i32, i32, ctypes.POINTER(StepLayoutC)]
+    lib.luce_decode_step.argtypes = [ctypes.POINTER(ModelC), ctypes.POINTER(SlotC), ctypes.POINTER(ctypes.c_int32),
+                                     i32, vp, vp, vp, vp, sz, vp]
+    for name in EXPORTS:
+        if name not in ("luce_last_error", "luce_version", "luce_launch_count", "luce_decode_attn_workspace_size"):
+            getattr(lib, name).restype = i32
+    _lib = lib
+    return lib
+
+
+def launch_count() -> int:
+    """Kernel launches the library has enqueued so far (all threads)."""
+    return int(load_library().luce_launch_count())
+
+
+def _check(rc: int):
+    if rc != LUCE_OK:
+        raise LuceError(rc, load_library().luce_last_error().decode())
+
+
+def _stream(stream=None) -> int:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _need(t, dtype, name):
+    import torch
+    if not isinstance(t, torch.Tensor) or t.dtype != dtype or not t.is_cuda:
+        raise TypeError(f"{name}: expected a CUDA {dtype} tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+
+
+# ------------------------------------------------------------ kernels
+
+def luce_q8_quantize_act(x, q=None, d=None, stream=None):
+    """fp32 [T][K] -> (int8 [T][K], fp32 [T][K/32]) q8_0 activation blocks."""
+    import torch
+    _need(x, torch.float32, "x")
+    T, K = x.shape
+    q = torch.empty((T, K), dtype=torch.int8, device=x.device) if q is None else q
+    d = torch.empty((T, K // QK), dtype=torch.float32, device=x.device) if d is None else d
+    _check(load_library().luce_q8_quantize_act(x.data_ptr(), T, K, K, q.data_ptr(), d.data_ptr(), _stream(stream)))
+    return q, d
+
+
+def luce_q8_matvec_batch(wq, wd, aq, ad, y=None, stream=None):
+    """q8_0 weights (int8 [N][K], fp16 [N][K/32]) x q8_0 activations -> fp32 [T][N]."""
+    import torch
+    _need(wq, torch.int8, "wq")
+    _need(aq, torch.int8, "aq")
+    _need(ad, torch.float32, "ad")
+    if wd.dtype not in (torch.float16, torch.int16, torch.uint16):
+        raise TypeError("wd: expected fp16 scales")
+    N, K = wq.shape
+    T = aq.shape[0]
+    y = torch.empty((T, N), dtype=torch.float32, device=wq.device) if y is None else y
+    _check(load_library().luce_q8_matvec_batch(wq.data_ptr(), wd.data_ptr(), N, K, aq.data_ptr(), ad.data_ptr(),
+                                               T, y.data_ptr(), y.stride(0), _stream(stream)))
+    return y
+
+
+def luce_q8_block_dots(wq, aq, stream=None):
+    import torch
+    N, K = wq.shape
+    T = aq.shape[0]
+    out = torch.empty((T, N, K // QK), dtype=torch.int32, device=wq.device)
+    _check(load_library().luce_q8_block_dots(wq.data_ptr(), N, K, aq.data_ptr(), T, out.data_ptr(), _stream(stream)))
+    return out
+
+
+def luce_rope_posvec(x, pos, theta: float, stream=None):
+    """In-place RoPE of fp32 x [T][n_heads][128] at per-row positions pos (int32 [T])."""
+    import torch
+    _need(x, torch.float32, "x")
+    _need(pos, torch.int32, "pos")
+    T, nh, D = x.shape
+    _check(load_library().luce_rope_posvec(x.data_ptr(), T, nh, D, nh * D, pos.data_ptr(), float(theta),
+                                           _stream(stream)))
+    return x
+
+
+@dataclass
+class SeqView:
+    """A sequence's cache for one layer (fp16 [Hkv][cap][128] K and V) with ``len``
+    keys including this step's ``n_q`` rows, which are rows row0.. of q/out."""
+    k: object
+    v: object
+    len: int
+    n_q: int = 1
+    row0: int = 0
+
+    def c(self) -> SeqViewC:
+        Hkv, cap, D = self.k.shape
+        return SeqViewC(self.k.data_ptr(), self.v.data_ptr(), self.len, self.n_q, self.row0, cap,
+                        self.k.stride(0), self.k.stride(1))
+
+
+def _views(views: Sequence[SeqView]):
+    arr = (SeqViewC * max(1, len(views)))()
+    for i, v in enumerate(views):
+        arr[i] = v.c()
+    return arr
+
+
+def luce_kv_append(k, v, views: Sequence[SeqView], stream=None):
+    """Append fp32 rows k, v ([T][Hkv][128]) as fp16 at each view's positions."""
+    import torch
+    _need(k, torch.float32, "k")
+    _need(v, torch.float32, "v")
+    T, Hkv, D = k.shape
+    _check(load_library().luce_kv_append(k.data_ptr(), v.data_ptr(), Hkv * D, Hkv, D, _views(views), len(views),
+                                         _stream(stream)))
+
+
+def luce_decode_attn_workspace_size(n_rows: int, Hq: int, D: int, max_len: int) -> int:
+    return int(load_library().luce_decode_attn_workspace_size(n_rows, Hq, D, max_len))
+
+
+def luce_decode_attn_multiseq(q, views: Sequence[SeqView], n_kv_heads: int, scale: float, out=None, ws=None,
+                              stream=None):
+    """Decode attention of fp32 q [T][Hq][128] against each row's own fp16 cache."""
+    import torch
+    _need(q, torch.float32, "q")
+    T, Hq, D = q.shape
+    out = torch.empty_like(q) if out is None else out
+    if ws is None:
+        max_len = max(v.len for v in views)
+        ws = torch.empty(luce_decode_attn_workspace_size(T, Hq, D, max_len), dtype=torch.uint8, device=q.device)
+    _check(load_library().luce_decode_attn_multiseq(q.data_ptr(), _views(views), len(views), Hq, n_kv_heads, D,
+                                                    float(scale), out.data_ptr(), ws.data_ptr(), ws.numel(),
+                                                    _stream(stream)))
+    return out
+
+
+# ------------------------------------------------------------ decode step
+
+@dataclass
+class LayerTensors:
+    attn_norm: object
+    wqkv_q: object
+    wqkv_d: object
+    wo_q: object
+    wo_d: object
+    ffn_norm: object
+    wgu_q: object
+    wgu_d: object
+    wdown_q: object
+    wdown_d: object
+
+
+class Model:
+    """Device weights of a decoder stack plus the C struct that points at them."""
+
+    def __init__(self, layers: List[LayerTensors], hidden: int, n_q_heads: int, n_kv_heads: int, ffn: int,
+                 head_dim: int = HEAD_DIM, rms_eps: float = 1e-6, rope_theta: float = 1e6,
+                 final_norm=None, head_q=None, head_d=None):
+        self.layers = layers
+        self.hidden, self.n_q_heads, self.n_kv_heads, self.ffn, self.head_dim = hidden, n_q_heads, n_kv_heads, ffn, head_dim
+        self.rms_eps, self.rope_theta = rms_eps, rope_theta
+        self.final_norm, self.head_q, self.head_d = final_norm, head_q, head_d
+        self.vocab = 0 if head_q is None else head_q.shape[0]
+        self._layers_c = (LayerC * max(1, len(layers)))()
+        for i, L in enumerate(layers):
+            self._layers_c[i] = LayerC(*[getattr(L, n).data_ptr() for n, _ in LayerC._fields_])
+        self.c = ModelC(len(layers), hidden, n_q_heads, n_kv_heads, head_dim, ffn, self.vocab, rms_eps, rope_theta,
+                        self._layers_c, _ptr(final_norm), _ptr(head_q), _ptr(head_d))
+
+    def layout(self, n_rows: int, max_ctx: int) -> dict:
+        out = StepLayoutC()
+        _check(load_library().luce_decode_step_layout(ctypes.byref(self.c), n_rows, max_ctx, ctypes.byref(out)))
+        return {n: getattr(out, n) for n in _LAYOUT_FIELDS}
+
+    def workspace(self, n_rows: int, max_ctx: int, device="cuda"):
+        import torch
+        return torch.empty(self.layout(n_rows, max_ctx)["total"], dtype=torch.uint8, device=device)
+
+
+@dataclass
+class Slot:
+    """A sequence's K/V cache for every layer: fp16 [n_layers][Hkv][cap][128] each,
+    with ``len`` tokens already cached."""
+    k: object
+    v: object
+    len: int
+
+    @property
+    def cap(self) -> int:
+        return self.k.shape[2]
+
+
+def luce_decode_step(model: Model, slots: Sequence[Slot], rows_per_slot: Sequence[int], x, ws,
+                     logits=None, argmax=None, stream=None):
+    """One batched decode step (all layers, optional head) over the given slots.
+    x: fp32 [T][hidden] in/out.  The slots' caches get this step's K/V rows."""
+    import torch
+    _need(x, torch.float32, "x")
+    n = len(slots)
+    sc = (SlotC * max(1, n))()
+    for i, s in enumerate(slots):
+        sc[i] = SlotC(s.k.data_ptr(), s.v.data_ptr(), s.len, s.cap)
+    rows = (ctypes.c_int32 * max(1, n))(*rows_per_slot)
+    _check(load_library().luce_decode_step(ctypes.byref(model.c), sc, rows, n, x.data_ptr(), _ptr(logits),
+                                           _ptr(argmax), ws.data_ptr(), ws.numel(), _stream(stream)))
+    return x

@@ -1,0 +1,440 @@
+// api.cu - the C ABI of libluce (see include/luce.h for the contract).
+//
+// Every entry point validates all of its arguments on the host before it
+// enqueues anything; a refused call returns a negative status and leaves the
+// stream untouched.  Nothing here allocates device memory or synchronises.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <algorithm>
+#include <atomic>
+#include <string>
+
+#include "../../include/luce.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace luce;
+
+static std::atomic<uint64_t> g_launches{0};
+void luce::count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char* fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
+int ok()
+{
+    g_err.clear();
+    return LUCE_OK;
+}
+
+int cuda_status(cudaError_t e, const char* what)
+{
+    if (e != cudaSuccess) return fail(LUCE_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+    return ok();
+}
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+#define REQUIRE(cond, code, ...) \
+    do {                         \
+        if (!(cond)) return fail(code, __VA_ARGS__); \
+    } while (0)
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int chunks_of(int len) { return (len + kAttnChunk - 1) / kAttnChunk; }
+
+}  // namespace
+
+extern "C" {
+
+const char* luce_last_error(void) { return g_err.c_str(); }
+
+int luce_version(void) { return 10000; }
+
+uint64_t luce_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int luce_q8_quantize_act(const float* x, int T, int K, int64_t ldx, int8_t* q, float* d, void* stream)
+{
+    REQUIRE(x && q && d, LUCE_EINVAL, "quantize_act: null pointer");
+    REQUIRE(T >= 1, LUCE_EINVAL, "quantize_act: T=%d must be >= 1", T);
+    REQUIRE(K >= 32 && K % 32 == 0, LUCE_EINVAL, "quantize_act: K=%d must be a positive multiple of 32", K);
+    REQUIRE(ldx >= K, LUCE_EINVAL, "quantize_act: ldx=%lld < K", (long long)ldx);
+    REQUIRE(aligned(x, 4) && aligned(d, 4), LUCE_EINVAL, "quantize_act: x and d must be 4-byte aligned");
+    return cuda_status(launch_quantize(x, T, K, ldx, q, d, (cudaStream_t)stream), "quantize_act");
+}
+
+static int check_matvec(const int8_t* wq, const uint16_t* wd, int N, int K, const int8_t* aq, const float* ad,
+                        int T, const void* y, int64_t ldy, const char* who)
+{
+    REQUIRE(wq && wd && aq && ad && y, LUCE_EINVAL, "%s: null pointer", who);
+    REQUIRE(N >= 1, LUCE_EINVAL, "%s: N=%d must be >= 1", who, N);
+    REQUIRE(K >= 32 && K % 32 == 0, LUCE_EINVAL, "%s: K=%d must be a positive multiple of 32", who, K);
+    REQUIRE(T >= 1 && T <= LUCE_MAX_ROWS, LUCE_EINVAL, "%s: T=%d outside 1..%d", who, T, LUCE_MAX_ROWS);
+    REQUIRE(ldy >= N, LUCE_EINVAL, "%s: ldy=%lld < N", who, (long long)ldy);
+    REQUIRE(aligned(wq, 16) && aligned(aq, 16), LUCE_EINVAL, "%s: wq and aq must be 16-byte aligned", who);
+    REQUIRE(aligned(wd, 2) && aligned(ad, 4) && aligned(y, 4), LUCE_EINVAL, "%s: misaligned wd/ad/y", who);
+    REQUIRE((int64_t)N * K < ((int64_t)1 << 40), LUCE_EINVAL, "%s: N*K too large", who);
+    return LUCE_OK;
+}
+
+int luce_q8_matvec_batch(const int8_t* wq, const uint16_t* wd, int N, int K, const int8_t* aq, const float* ad,
+                         int T, float* y, int64_t ldy, void* stream)
+{
+    int rc = check_matvec(wq, wd, N, K, aq, ad, T, y, ldy, "q8_matvec_batch");
+    if (rc) return rc;
+    return cuda_status(launch_matvec(wq, reinterpret_cast<const __half*>(wd), N, K, aq, ad, T, y, ldy, nullptr, 0,
+                                     (cudaStream_t)stream),
+                       "q8_matvec_batch");
+}
+
+int luce_q8_block_dots(const int8_t* wq, int N, int K, const int8_t* aq, int T, int32_t* out, void* stream)
+{
+    REQUIRE(wq && aq && out, LUCE_EINVAL, "q8_block_dots: null pointer");
+    REQUIRE(N >= 1 && T >= 1 && T <= LUCE_MAX_ROWS, LUCE_EINVAL, "q8_block_dots: bad N=%d or T=%d", N, T);
+    REQUIRE(K >= 32 && K % 32 == 0, LUCE_EINVAL, "q8_block_dots: K=%d must be a positive multiple of 32", K);
+    REQUIRE(aligned(wq, 16) && aligned(aq, 16) && aligned(out, 4), LUCE_EINVAL, "q8_block_dots: misaligned");
+    return cuda_status(launch_block_dots(wq, N, K, aq, T, out, (cudaStream_t)stream), "q8_block_dots");
+}
+
+int luce_rope_posvec(float* x, int T, int n_heads, int D, int64_t ldx, const int32_t* pos, double theta,
+                     void* stream)
+{
+    REQUIRE(x && pos, LUCE_EINVAL, "rope_posvec: null pointer");
+    REQUIRE(D == LUCE_HEAD_DIM, LUCE_EUNSUPPORTED, "rope_posvec: head_dim %d (only %d)", D, LUCE_HEAD_DIM);
+    REQUIRE(T >= 1 && n_heads >= 1, LUCE_EINVAL, "rope_posvec: T=%d n_heads=%d", T, n_heads);
+    REQUIRE(ldx >= (int64_t)n_heads * D, LUCE_EINVAL, "rope_posvec: ldx too small");
+    REQUIRE(theta > 0 && isfinite(theta), LUCE_EINVAL, "rope_posvec: theta must be positive");
+    REQUIRE(aligned(x, 4) && aligned(pos, 4), LUCE_EINVAL, "rope_posvec: misaligned");
+    return cuda_status(launch_rope_posvec(x, T, n_heads, ldx, pos, theta, (cudaStream_t)stream), "rope_posvec");
+}
+
+// Validates views and returns the number of rows they cover (rows 0..T-1,
+// each exactly once).
+static int check_views(const luce_seqview* views, int n_seq, int Hkv, int D, int* T_out, const char* who)
+{
+    REQUIRE(views, LUCE_EINVAL, "%s: null views", who);
+    REQUIRE(n_seq >= 1 && n_seq <= LUCE_MAX_SEQ, LUCE_EINVAL,
+            "%s: n_seq=%d outside 1..%d (more than %d sequences are refused)", who, n_seq, LUCE_MAX_SEQ,
+            LUCE_MAX_SEQ);
+    REQUIRE(D == LUCE_HEAD_DIM, LUCE_EUNSUPPORTED, "%s: head_dim %d (only %d)", who, D, LUCE_HEAD_DIM);
+    int covered[LUCE_MAX_ROWS] = {0};
+    int T = 0;
+    for (int s = 0; s < n_seq; ++s) {
+        const luce_seqview& v = views[s];
+        REQUIRE(v.k && v.v, LUCE_EINVAL, "%s: view %d has a null cache pointer", who, s);
+        REQUIRE(aligned(v.k, 16) && aligned(v.v, 16), LUCE_EINVAL, "%s: view %d cache not 16-byte aligned", who, s);
+        REQUIRE(v.n_q >= 1 && v.n_q <= LUCE_MAX_ROWS_PER_SEQ, LUCE_EINVAL, "%s: view %d n_q=%d outside 1..%d", who,
+                s, v.n_q, LUCE_MAX_ROWS_PER_SEQ);
+        REQUIRE(v.len >= v.n_q && v.len <= v.cap, LUCE_EINVAL, "%s: view %d len=%d outside [n_q, cap=%d]", who, s,
+                v.len, v.cap);
+        REQUIRE(v.tok_stride >= D && v.tok_stride % 8 == 0 && v.head_stride % 8 == 0, LUCE_EINVAL,
+                "%s: view %d strides must be multiples of 8 with tok_stride >= D", who, s);
+        REQUIRE(v.head_stride >= (int64_t)v.cap * v.tok_stride || Hkv == 1, LUCE_EINVAL,
+                "%s: view %d head_stride overlaps heads", who, s);
+        REQUIRE(v.row0 >= 0 && v.row0 + v.n_q <= LUCE_MAX_ROWS, LUCE_EINVAL, "%s: view %d rows out of range", who, s);
+        for (int j = 0; j < v.n_q; ++j) {
+            REQUIRE(!covered[v.row0 + j], LUCE_EINVAL, "%s: row %d claimed twice", who, v.row0 + j);
+            covered[v.row0 + j] = 1;
+        }
+        T = std::max(T, v.row0 + v.n_q);
+    }
+    for (int r = 0; r < T; ++r) REQUIRE(covered[r], LUCE_EINVAL, "%s: row %d belongs to no view", who, r);
+    *T_out = T;
+    return LUCE_OK;
+}
+
+int luce_kv_append(const float* k, const float* v, int64_t ldkv, int Hkv, int D, const luce_seqview* views,
+                   int n_seq, void* stream)
+{
+    REQUIRE(k && v, LUCE_EINVAL, "kv_append: null k/v");
+    REQUIRE(Hkv >= 1 && ldkv >= (int64_t)Hkv * D, LUCE_EINVAL, "kv_append: bad Hkv=%d or ldkv", Hkv);
+    int T = 0;
+    int rc = check_views(views, n_seq, Hkv, D, &T, "kv_append");
+    if (rc) return rc;
+    KvRows rows{};
+    rows.n_rows = T;
+    for (int s = 0; s < n_seq; ++s)
+        for (int j = 0; j < views[s].n_q; ++j) {
+            const int64_t p = views[s].len - views[s].n_q + j;
+            KvRow& r = rows.row[views[s].row0 + j];
+            r.k = reinterpret_cast<__half*>(views[s].k) + p * views[s].tok_stride;
+            r.v = reinterpret_cast<__half*>(views[s].v) + p * views[s].tok_stride;
+            r.head_stride = views[s].head_stride;
+        }
+    return cuda_status(launch_kv_append(k, v, ldkv, Hkv, rows, (cudaStream_t)stream), "kv_append");
+}
+
+size_t luce_decode_attn_workspace_size(int n_rows, int Hq, int D, int max_len)
+{
+    if (n_rows < 1 || Hq < 1 || D != LUCE_HEAD_DIM || max_len < 1) return 0;
+    return attn_part_floats(n_rows * chunks_of(max_len), Hq) * sizeof(float);
+}
+
+static void build_attn_rows(const luce_seqview* views, int n_seq, AttnRows& rows, int T)
+{
+    rows.n_rows = T;
+    for (int s = 0; s < n_seq; ++s)
+        for (int j = 0; j < views[s].n_q; ++j) {
+            AttnRow& r = rows.row[views[s].row0 + j];
+            r.k = reinterpret_cast<const __half*>(views[s].k);
+            r.v = reinterpret_cast<const __half*>(views[s].v);
+            r.head_stride = views[s].head_stride;
+            r.tok_stride = views[s].tok_stride;
+            r.len = views[s].len - views[s].n_q + 1 + j;
+        }
+    int c = 0;
+    for (int r = 0; r < T; ++r) {
+        rows.row[r].chunk0 = c;
+        c += chunks_of(rows.row[r].len);
+    }
+    rows.total_chunks = c;
+}
+
+int luce_decode_attn_multiseq(const float* q, const luce_seqview* views, int n_seq, int Hq, int Hkv, int D,
+                              float scale, float* out, void* ws, size_t ws_bytes, void* stream)
+{
+    REQUIRE(q && out && ws, LUCE_EINVAL, "decode_attn: null q/out/ws");
+    REQUIRE(Hkv >= 1 && Hq >= Hkv && Hq % Hkv == 0, LUCE_EINVAL, "decode_attn: Hq=%d must be a multiple of Hkv=%d",
+            Hq, Hkv);
+    REQUIRE(Hq / Hkv <= 8, LUCE_EUNSUPPORTED, "decode_attn: group size %d > 8", Hq / Hkv);
+    REQUIRE(isfinite(scale), LUCE_EINVAL, "decode_attn: scale must be finite");
+    REQUIRE(aligned(q, 16) && aligned(out, 4) && aligned(ws, 16), LUCE_EINVAL, "decode_attn: misaligned q/out/ws");
+    int T = 0;
+    int rc = check_views(views, n_seq, Hkv, D, &T, "decode_attn");
+    if (rc) return rc;
+    AttnRows rows{};
+    build_attn_rows(views, n_seq, rows, T);
+    const size_t need = attn_part_floats(rows.total_chunks, Hq) * sizeof(float);
+    REQUIRE(ws_bytes >= need, LUCE_ENOSPACE, "decode_attn: workspace %zu bytes < %zu needed", ws_bytes, need);
+    return cuda_status(launch_attention(q, (int64_t)Hq * D, rows, Hq, Hkv, scale, (float*)ws, out,
+                                        (int64_t)Hq * D, (cudaStream_t)stream),
+                       "decode_attn");
+}
+
+// ------------------------------------------------------------ decode step
+
+static int check_model(const luce_model* m, const char* who)
+{
+    REQUIRE(m, LUCE_EINVAL, "%s: null model", who);
+    REQUIRE(m->n_layers >= 0 && m->hidden >= 32 && m->hidden % 32 == 0, LUCE_EINVAL,
+            "%s: hidden=%d must be a positive multiple of 32", who, m->hidden);
+    REQUIRE(m->head_dim == LUCE_HEAD_DIM, LUCE_EUNSUPPORTED, "%s: head_dim %d (only %d)", who, m->head_dim,
+            LUCE_HEAD_DIM);
+    REQUIRE(m->n_kv_heads >= 1 && m->n_q_heads % m->n_kv_heads == 0 && m->n_q_heads / m->n_kv_heads <= 8,
+            LUCE_EUNSUPPORTED, "%s: heads %d/%d (need Hq %% Hkv == 0, group <= 8)", who, m->n_q_heads,
+            m->n_kv_heads);
+    REQUIRE(m->ffn >= 32 && m->ffn % 32 == 0, LUCE_EINVAL, "%s: ffn=%d must be a positive multiple of 32", who,
+            m->ffn);
+    REQUIRE(m->vocab >= 0, LUCE_EINVAL, "%s: vocab < 0", who);
+    REQUIRE(m->n_layers == 0 || m->layers, LUCE_EINVAL, "%s: null layer table", who);
+    REQUIRE(m->rope_theta > 0 && isfinite(m->rope_theta), LUCE_EINVAL, "%s: rope_theta must be positive", who);
+    REQUIRE(m->rms_eps >= 0 && isfinite(m->rms_eps), LUCE_EINVAL, "%s: rms_eps must be >= 0", who);
+    return LUCE_OK;
+}
+
+static void layout_of(const luce_model* m, int T, int max_ctx, luce_step_layout* L)
+{
+    const size_t H = m->hidden, Hq = m->n_q_heads, Hkv = m->n_kv_heads, D = m->head_dim, F = m->ffn;
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = o;
+        o = align_up(o + bytes, 256);
+        return at;
+    };
+    L->rope_cs = take(T * (D / 2) * sizeof(float2));
+    L->xn = take(T * H * 4);
+    L->xn_q = take(T * H);
+    L->xn_d = take(T * H / 32 * 4);
+    L->qkv = take(T * (Hq + 2 * Hkv) * D * 4);
+    L->q_rot = take(T * Hq * D * 4);
+    L->attn = take(T * Hq * D * 4);
+    L->attn_q = take(T * Hq * D);
+    L->attn_d = take(T * Hq * D / 32 * 4);
+    L->x1 = take(T * H * 4);
+    L->xn2 = take(T * H * 4);
+    L->xn2_q = take(T * H);
+    L->xn2_d = take(T * H / 32 * 4);
+    L->gu = take(T * 2 * F * 4);
+    L->h = take(T * F * 4);
+    L->h_q = take(T * F);
+    L->h_d = take(T * F / 32 * 4);
+    L->xf = take(T * H * 4);
+    L->xf_q = take(T * H);
+    L->xf_d = take(T * H / 32 * 4);
+    // The split-K scratch comes last so that the offsets above do not depend
+    // on the context bound.
+    L->part = take(attn_part_floats(T * chunks_of(std::max(max_ctx, 1)), (int)Hq) * 4);
+    L->total = o;
+}
+
+int luce_decode_step_layout(const luce_model* m, int n_rows, int max_ctx, luce_step_layout* out)
+{
+    int rc = check_model(m, "decode_step_layout");
+    if (rc) return rc;
+    REQUIRE(out, LUCE_EINVAL, "decode_step_layout: null out");
+    REQUIRE(n_rows >= 1 && n_rows <= LUCE_MAX_ROWS, LUCE_EINVAL, "decode_step_layout: n_rows=%d outside 1..%d",
+            n_rows, LUCE_MAX_ROWS);
+    REQUIRE(max_ctx >= 1, LUCE_EINVAL, "decode_step_layout: max_ctx=%d", max_ctx);
+    layout_of(m, n_rows, max_ctx, out);
+    return ok();
+}
+
+int luce_decode_step(const luce_model* m, const luce_slot* slots, const int32_t* rows_per_slot, int n_seq,
+                     float* x, float* logits, int32_t* argmax, void* ws, size_t ws_bytes, void* stream)
+{
+    const char* who = "decode_step";
+    int rc = check_model(m, who);
+    if (rc) return rc;
+    REQUIRE(slots && rows_per_slot && x && ws, LUCE_EINVAL, "%s: null slots/rows/x/ws", who);
+    REQUIRE(n_seq >= 1 && n_seq <= LUCE_MAX_SEQ, LUCE_EINVAL,
+            "%s: n_seq=%d outside 1..%d (more than %d slots are refused)", who, n_seq, LUCE_MAX_SEQ, LUCE_MAX_SEQ);
+    REQUIRE(aligned(x, 16) && aligned(ws, 256), LUCE_EINVAL, "%s: x must be 16-byte and ws 256-byte aligned", who);
+    REQUIRE(!(logits || argmax) || (m->vocab > 0 && m->final_norm && m->head_q && m->head_d), LUCE_EINVAL,
+            "%s: logits/argmax need vocab > 0 and the head weights", who);
+    REQUIRE(!argmax || logits, LUCE_EINVAL, "%s: argmax needs the logits buffer", who);
+    const int H = m->hidden, Hq = m->n_q_heads, Hkv = m->n_kv_heads, D = m->head_dim, F = m->ffn;
+    int T = 0, max_len = 1;
+    for (int s = 0; s < n_seq; ++s) {
+        const luce_slot& sl = slots[s];
+        const int n = rows_per_slot[s];
+        REQUIRE(n >= 1 && n <= LUCE_MAX_ROWS_PER_SEQ, LUCE_EINVAL, "%s: slot %d has %d rows (1..%d)", who, s, n,
+                LUCE_MAX_ROWS_PER_SEQ);
+        REQUIRE(sl.k && sl.v && aligned(sl.k, 16) && aligned(sl.v, 16), LUCE_EINVAL,
+                "%s: slot %d cache null or not 16-byte aligned", who, s);
+        REQUIRE(sl.len >= 0 && sl.cap >= 1 && (int64_t)sl.len + n <= sl.cap, LUCE_EINVAL,
+                "%s: slot %d len=%d + rows=%d exceeds cap=%d", who, s, sl.len, n, sl.cap);
+        for (int p = 0; p < s; ++p)
+            REQUIRE(slots[p].k != sl.k && slots[p].v != sl.v, LUCE_EINVAL, "%s: slots %d and %d share a cache", who,
+                    p, s);
+        T += n;
+        max_len = std::max(max_len, sl.len + n);
+    }
+    REQUIRE(T <= LUCE_MAX_ROWS, LUCE_EINVAL, "%s: %d rows > %d", who, T, LUCE_MAX_ROWS);
+    for (int l = 0; l < m->n_layers; ++l) {
+        const luce_layer& w = m->layers[l];
+        REQUIRE(w.attn_norm && w.wqkv_q && w.wqkv_d && w.wo_q && w.wo_d && w.ffn_norm && w.wgu_q && w.wgu_d &&
+                    w.wdown_q && w.wdown_d,
+                LUCE_EINVAL, "%s: layer %d has a null weight", who, l);
+        REQUIRE(aligned(w.wqkv_q, 16) && aligned(w.wo_q, 16) && aligned(w.wgu_q, 16) && aligned(w.wdown_q, 16),
+                LUCE_EINVAL, "%s: layer %d int8 weights must be 16-byte aligned", who, l);
+    }
+    REQUIRE(!logits || aligned(m->head_q, 16), LUCE_EINVAL, "%s: head weights must be 16-byte aligned", who);
+
+    luce_step_layout L;
+    layout_of(m, T, max_len, &L);
+    REQUIRE(ws_bytes >= L.total, LUCE_ENOSPACE, "%s: workspace %zu bytes < %zu needed", who, ws_bytes, L.total);
+
+    char* wsb = (char*)ws;
+    float2* rope_cs = (float2*)(wsb + L.rope_cs);
+    float* xn = (float*)(wsb + L.xn);
+    int8_t* xn_q = (int8_t*)(wsb + L.xn_q);
+    float* xn_d = (float*)(wsb + L.xn_d);
+    float* qkv = (float*)(wsb + L.qkv);
+    float* q_rot = (float*)(wsb + L.q_rot);
+    float* part = (float*)(wsb + L.part);
+    float* attn = (float*)(wsb + L.attn);
+    int8_t* attn_q = (int8_t*)(wsb + L.attn_q);
+    float* attn_d = (float*)(wsb + L.attn_d);
+    float* x1 = (float*)(wsb + L.x1);
+    float* xn2 = (float*)(wsb + L.xn2);
+    int8_t* xn2_q = (int8_t*)(wsb + L.xn2_q);
+    float* xn2_d = (float*)(wsb + L.xn2_d);
+    float* gu = (float*)(wsb + L.gu);
+    float* hh = (float*)(wsb + L.h);
+    int8_t* h_q = (int8_t*)(wsb + L.h_q);
+    float* h_d = (float*)(wsb + L.h_d);
+    cudaStream_t st = (cudaStream_t)stream;
+
+    // Row bookkeeping (host): positions, K/V destinations, attention rows.
+    RowPos pos{};
+    pos.n_rows = T;
+    int slot_of[LUCE_MAX_ROWS];
+    {
+        int r = 0;
+        for (int s = 0; s < n_seq; ++s)
+            for (int j = 0; j < rows_per_slot[s]; ++j, ++r) {
+                slot_of[r] = s;
+                pos.pos[r] = slots[s].len + j;
+            }
+    }
+    cudaError_t e = launch_rope_table(pos, m->rope_theta, rope_cs, st);
+    if (e != cudaSuccess) return cuda_status(e, who);
+
+    const float scale = (float)(1.0 / sqrt((double)D));
+    const int64_t qkv_rows = (int64_t)(Hq + 2 * Hkv) * D;
+    for (int l = 0; l < m->n_layers; ++l) {
+        const luce_layer& w = m->layers[l];
+        KvRows kv{};
+        AttnRows ar{};
+        kv.n_rows = ar.n_rows = T;
+        for (int r = 0; r < T; ++r) {
+            const luce_slot& sl = slots[slot_of[r]];
+            const int64_t head_stride = (int64_t)sl.cap * D;
+            const int64_t layer_off = (int64_t)l * Hkv * head_stride;
+            __half* kb = reinterpret_cast<__half*>(sl.k) + layer_off;
+            __half* vb = reinterpret_cast<__half*>(sl.v) + layer_off;
+            kv.row[r].k = kb + (int64_t)pos.pos[r] * D;
+            kv.row[r].v = vb + (int64_t)pos.pos[r] * D;
+            kv.row[r].head_stride = head_stride;
+            ar.row[r].k = kb;
+            ar.row[r].v = vb;
+            ar.row[r].head_stride = head_stride;
+            ar.row[r].tok_stride = D;
+            ar.row[r].len = pos.pos[r] + 1;
+        }
+        int c = 0;
+        for (int r = 0; r < T; ++r) {
+            ar.row[r].chunk0 = c;
+            c += chunks_of(ar.row[r].len);
+        }
+        ar.total_chunks = c;
+
+        if ((e = launch_rmsnorm_quant(x, T, H, w.attn_norm, m->rms_eps, xn, xn_q, xn_d, st))) break;
+        if ((e = launch_matvec(w.wqkv_q, (const __half*)w.wqkv_d, (int)qkv_rows, H, xn_q, xn_d, T, qkv, qkv_rows,
+                               nullptr, 0, st)))
+            break;
+        if ((e = launch_rope_kv(qkv, T, Hq, Hkv, rope_cs, q_rot, kv, st))) break;
+        if ((e = launch_attention(q_rot, (int64_t)Hq * D, ar, Hq, Hkv, scale, part, attn, (int64_t)Hq * D, st)))
+            break;
+        if ((e = launch_quantize(attn, T, Hq * D, (int64_t)Hq * D, attn_q, attn_d, st))) break;
+        if ((e = launch_matvec(w.wo_q, (const __half*)w.wo_d, H, Hq * D, attn_q, attn_d, T, x1, H, x, H, st)))
+            break;
+        if ((e = launch_rmsnorm_quant(x1, T, H, w.ffn_norm, m->rms_eps, xn2, xn2_q, xn2_d, st))) break;
+        if ((e = launch_matvec(w.wgu_q, (const __half*)w.wgu_d, 2 * F, H, xn2_q, xn2_d, T, gu, 2 * F, nullptr, 0,
+                               st)))
+            break;
+        if ((e = launch_swiglu_quant(gu, T, F, hh, h_q, h_d, st))) break;
+        if ((e = launch_matvec(w.wdown_q, (const __half*)w.wdown_d, H, F, h_q, h_d, T, x, H, x1, H, st))) break;
+    }
+    if (e != cudaSuccess) return cuda_status(e, who);
+
+    if (logits) {
+        float* xf = (float*)(wsb + L.xf);
+        int8_t* xf_q = (int8_t*)(wsb + L.xf_q);
+        float* xf_d = (float*)(wsb + L.xf_d);
+        if ((e = launch_rmsnorm_quant(x, T, H, m->final_norm, m->rms_eps, xf, xf_q, xf_d, st)))
+            return cuda_status(e, who);
+        if ((e = launch_matvec(m->head_q, (const __half*)m->head_d, m->vocab, H, xf_q, xf_d, T, logits, m->vocab,
+                               nullptr, 0, st)))
+            return cuda_status(e, who);
+        if (argmax && (e = launch_argmax(logits, T, m->vocab, argmax, st))) return cuda_status(e, who);
+    }
+    return ok();
+}
+
+}  // extern "C"

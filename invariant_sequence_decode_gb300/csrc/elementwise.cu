@@ -1,0 +1,167 @@
+// elementwise.cu - activation quantization and the per-row layer glue:
+// RMSNorm -> q8_0, SwiGLU -> q8_0, argmax.
+//
+// Activation quantization follows "#1209 ... fix QFUSE", What changed and
+// why, item 2: a fused producer must quantize with exactly the consumer's
+// division and rounding convention.  Here the fused kernels (RMSNorm +
+// quantize, SwiGLU + quantize) call the very same per-lane routine as the
+// standalone quantizer, on the same fp32 value they also store, so their
+// codes equal a standalone quantization of their fp32 output bit for bit.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace luce {
+
+// One warp per 32-value block; lane i quantizes element i.
+__global__ void __launch_bounds__(256)
+quantize_kernel(const float* __restrict__ x, int T, int K, int64_t ldx, int8_t* __restrict__ q,
+                float* __restrict__ d)
+{
+    const int lane = threadIdx.x & 31;
+    const int nb = K >> 5;
+    const int64_t blk = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (blk >= (int64_t)T * nb) return;
+    const int t = (int)(blk / nb), b = (int)(blk - (int64_t)t * nb);
+    const float v = x[(size_t)t * ldx + (size_t)b * 32 + lane];
+    float dd;
+    const int code = q8_quantize_lane(v, &dd);
+    q[(size_t)t * K + (size_t)b * 32 + lane] = (int8_t)code;
+    if (lane == 0) d[(size_t)t * nb + b] = dd;
+}
+
+cudaError_t launch_quantize(const float* x, int T, int K, int64_t ldx, int8_t* q, float* d, cudaStream_t s)
+{
+    const int64_t blocks = (int64_t)T * (K >> 5);
+    quantize_kernel<<<(unsigned)((blocks + 7) / 8), 256, 0, s>>>(x, T, K, ldx, q, d);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+// RMSNorm of one row per CTA, then q8_0 quantization of the normalised row.
+// Sum of squares: thread i adds x[i], x[i+256], ... with fma in ascending
+// order; warp partials by butterfly; thread 0 adds the 8 warp sums in order.
+// r = 1 / sqrt(ss / H + eps) with IEEE division and square root.
+__global__ void __launch_bounds__(256)
+rmsnorm_quant_kernel(const float* __restrict__ x, int H, const float* __restrict__ gamma, float eps,
+                     float* __restrict__ xn, int8_t* __restrict__ q, float* __restrict__ d)
+{
+    __shared__ float red[8];
+    __shared__ float rs;
+    const int t = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float* xr = x + (size_t)t * H;
+    float ss = 0.0f;
+    for (int i = tid; i < H; i += 256) {
+        const float v = xr[i];
+        ss = __fmaf_rn(v, v, ss);
+    }
+    ss = warp_sum_butterfly(ss);
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    if (tid == 0) {
+        float tot = red[0];
+        for (int w = 1; w < 8; ++w) tot = __fadd_rn(tot, red[w]);
+        const float mean = __fdiv_rn(tot, (float)H);
+        rs = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
+    }
+    __syncthreads();
+    const float r = rs;
+    const int nb = H >> 5;
+    for (int b = warp; b < nb; b += 8) {
+        const int i = b * 32 + lane;
+        const float v = __fmul_rn(__fmul_rn(xr[i], r), gamma[i]);
+        xn[(size_t)t * H + i] = v;
+        float dd;
+        const int code = q8_quantize_lane(v, &dd);
+        q[(size_t)t * H + i] = (int8_t)code;
+        if (lane == 0) d[(size_t)t * nb + b] = dd;
+    }
+}
+
+cudaError_t launch_rmsnorm_quant(const float* x, int T, int H, const float* gamma, float eps,
+                                 float* xn, int8_t* q, float* d, cudaStream_t s)
+{
+    rmsnorm_quant_kernel<<<T, 256, 0, s>>>(x, H, gamma, eps, xn, q, d);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+// SwiGLU of the concatenated gate||up row (gate first), then q8_0.
+__global__ void __launch_bounds__(256)
+swiglu_quant_kernel(const float* __restrict__ gu, int T, int F, float* __restrict__ h,
+                    int8_t* __restrict__ q, float* __restrict__ d)
+{
+    const int lane = threadIdx.x & 31;
+    const int nb = F >> 5;
+    const int64_t blk = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (blk >= (int64_t)T * nb) return;
+    const int t = (int)(blk / nb), b = (int)(blk - (int64_t)t * nb);
+    const int i = b * 32 + lane;
+    const float g = gu[(size_t)t * 2 * F + i];
+    const float u = gu[(size_t)t * 2 * F + F + i];
+    const float v = silu_mul(g, u);
+    h[(size_t)t * F + i] = v;
+    float dd;
+    const int code = q8_quantize_lane(v, &dd);
+    q[(size_t)t * F + i] = (int8_t)code;
+    if (lane == 0) d[(size_t)t * nb + b] = dd;
+}
+
+cudaError_t launch_swiglu_quant(const float* gu, int T, int F, float* h, int8_t* q, float* d,
+                                cudaStream_t s)
+{
+    const int64_t blocks = (int64_t)T * (F >> 5);
+    swiglu_quant_kernel<<<(unsigned)((blocks + 7) / 8), 256, 0, s>>>(gu, T, F, h, q, d);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+// Argmax of each row, lowest index on ties, NaN never chosen (all-NaN -> 0).
+// The (value, index) winner is unique, so the reduction order is free.
+__device__ __forceinline__ void better(float& bv, int& bi, float v, int i)
+{
+    if (v != v) return;
+    if (bi < 0 || v > bv || (v == bv && i < bi)) {
+        bv = v;
+        bi = i;
+    }
+}
+
+__global__ void __launch_bounds__(1024)
+argmax_kernel(const float* __restrict__ x, int V, int32_t* __restrict__ out)
+{
+    __shared__ float sv[32];
+    __shared__ int si[32];
+    const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float* r = x + (size_t)t * V;
+    float bv = 0.0f;
+    int bi = -1;
+    for (int i = tid; i < V; i += blockDim.x) better(bv, bi, r[i], i);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+        if (oi >= 0) better(bv, bi, ov, oi);
+    }
+    if (lane == 0) {
+        sv[warp] = bv;
+        si[warp] = bi;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        float fv = 0.0f;
+        int fi = -1;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w)
+            if (si[w] >= 0) better(fv, fi, sv[w], si[w]);
+        out[t] = fi < 0 ? 0 : fi;
+    }
+}
+
+cudaError_t launch_argmax(const float* x, int T, int V, int32_t* out, cudaStream_t s)
+{
+    argmax_kernel<<<T, 1024, 0, s>>>(x, V, out);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace luce

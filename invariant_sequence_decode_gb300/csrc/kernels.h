@@ -1,0 +1,81 @@
+// kernels.h - host-side launchers of the libluce kernels (internal).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace luce {
+
+// Counts kernel launches (bumped by every launcher below).
+void count_launches(int n);
+
+// Per-row destination of a K/V append: element (g, d) of the row goes to
+// k[g * head_stride + d] (the pointers already point at the row's position).
+struct KvRow {
+    __half* k;
+    __half* v;
+    int64_t head_stride;
+};
+struct KvRows {
+    KvRow row[16];
+    int n_rows;
+};
+
+// One query row of decode attention: its keys are k/v[g*head_stride + j*tok_stride + d]
+// for j < len; chunk0 is the index of its first split-K chunk in the scratch.
+struct AttnRow {
+    const __half* k;
+    const __half* v;
+    int64_t head_stride;
+    int64_t tok_stride;
+    int len;
+    int chunk0;
+};
+struct AttnRows {
+    AttnRow row[16];
+    int n_rows;
+    int total_chunks;
+};
+
+// Positions of up to 16 rows, passed by value.
+struct RowPos {
+    int pos[16];
+    int n_rows;
+};
+
+cudaError_t launch_quantize(const float* x, int T, int K, int64_t ldx, int8_t* q, float* d, cudaStream_t s);
+
+cudaError_t launch_matvec(const int8_t* wq, const __half* wd, int N, int K, const int8_t* aq,
+                          const float* ad, int T, float* y, int64_t ldy, const float* resid,
+                          int64_t ldr, cudaStream_t s);
+
+cudaError_t launch_block_dots(const int8_t* wq, int N, int K, const int8_t* aq, int T, int32_t* out,
+                              cudaStream_t s);
+
+cudaError_t launch_rope_posvec(float* x, int T, int n_heads, int64_t ldx, const int32_t* pos,
+                               double theta, cudaStream_t s);
+
+cudaError_t launch_kv_append(const float* k, const float* v, int64_t ld, int Hkv, const KvRows& rows,
+                             cudaStream_t s);
+
+// Scratch floats for `total_chunks` chunks of Hq heads.
+size_t attn_part_floats(int total_chunks, int Hq);
+
+cudaError_t launch_attention(const float* q, int64_t ldq, const AttnRows& rows, int Hq, int Hkv,
+                             float scale, float* part, float* out, int64_t ldo, cudaStream_t s);
+
+cudaError_t launch_rmsnorm_quant(const float* x, int T, int H, const float* gamma, float eps,
+                                 float* xn, int8_t* q, float* d, cudaStream_t s);
+
+cudaError_t launch_swiglu_quant(const float* gu, int T, int F, float* h, int8_t* q, float* d,
+                                cudaStream_t s);
+
+cudaError_t launch_rope_table(const RowPos& pos, double theta, float2* cs, cudaStream_t s);
+
+cudaError_t launch_rope_kv(const float* qkv, int T, int Hq, int Hkv, const float2* cs, float* q_rot,
+                           const KvRows& rows, cudaStream_t s);
+
+cudaError_t launch_argmax(const float* x, int T, int V, int32_t* out, cudaStream_t s);
+
+}  // namespace luce

@@ -1,0 +1,248 @@
+"""GPU parity of each kernel against the CPU oracle, plus batched == solo.
+
+Tolerances: quantized activations and per-block int32 dots bit-exact; fp32
+matvec rows within 1e-5 of the row's L2 norm; attention within 2e-3 absolute
+(fp32 accumulation over an f16 cache); RoPE within 1e-6 of each pair's norm
+(fp32 rotation by double-evaluated cos/sin); batched vs solo bitwise.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from invariant_sequence_decode_gb300 import synth, workloads as wl
+
+torch = pytest.importorskip("torch")
+import invariant_sequence_decode_gb300 as luce  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+SENTINEL = np.uint32(0x7FC0DEAD)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from invariant_sequence_decode_gb300 import build
+    build.build()
+    luce.load_library()
+
+
+def cuda(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def rel_row_err(y, ref):
+    return np.max(np.abs(y - ref), axis=1) / np.maximum(np.linalg.norm(ref, axis=1), 1e-30)
+
+
+# ------------------------------------------------------------ quantizer
+
+def crafted_rows(K):
+    ties = np.array([127.0, -126.5, 126.5, 63.5, -63.5, 2.5, -2.5, 0.5, -0.5, 1.5] + [0.25] * 22, np.float32)
+    rows = np.zeros((4, K), np.float32)
+    rows[0, :32] = ties
+    rows[1, :32] = 3.0                       # constant block -> all 127
+    rows[1, 32:64] = 0.0                     # zero block -> d = 0
+    rows[2, :32] = np.linspace(-1, 1, 32)
+    rows[2, 5] = np.nan                      # NaN entry -> 0, ignored by amax
+    rows[3, :32] = np.float32(1e-40) * np.arange(32)  # subnormal block
+    return rows
+
+
+@pytest.mark.parametrize("T,K", [(1, 32), (4, 1024), (3, 5120), (16, 17408)])
+def test_quantize_bit_exact(T, K):
+    x = wl.acts(0, T, K) * np.float32(3.0)
+    x = np.concatenate([x, crafted_rows(K)])
+    q, d = luce.luce_q8_quantize_act(cuda(x))
+    qo, do = oracle.quantize_act(x)
+    assert np.array_equal(host(q), qo)
+    assert np.array_equal(host(d).view(np.uint32), do.view(np.uint32))
+
+
+# ------------------------------------------------------------ block dots / matvec
+
+MV_SHAPES = [(1024, 1024), (1000, 1056), (33, 96), (7, 32), (301, 5120), (64, 17408)]
+
+
+def mv_inputs(N, K, T, seed=0):
+    wq, wd = wl.q8_weights(seed, wl.tid(wl.W_MAT, N % 4096, K % 16), N, K)
+    aq, ad = oracle.quantize_act(wl.acts(seed, T, K, sub=3))
+    return wq, wd, aq, ad
+
+
+@pytest.mark.parametrize("N,K", MV_SHAPES)
+def test_block_dots_bit_exact(N, K):
+    wq, wd, aq, ad = mv_inputs(N, K, 3)
+    got = host(luce.luce_q8_block_dots(cuda(wq), cuda(aq)))
+    assert np.array_equal(got, oracle.block_dots(wq, aq))
+
+
+def test_block_dots_extremes():
+    wq = np.full((2, 64), -127, np.int8)
+    wq[1] = 127
+    aq = np.full((1, 64), -127, np.int8)
+    got = host(luce.luce_q8_block_dots(cuda(wq), cuda(aq)))
+    assert got[0, 0].tolist() == [516128, 516128] and got[0, 1].tolist() == [-516128, -516128]
+
+
+@pytest.mark.parametrize("N,K", MV_SHAPES)
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 8, 12, 16])
+def test_matvec_parity(N, K, T):
+    wq, wd, aq, ad = mv_inputs(N, K, T)
+    y = host(luce.luce_q8_matvec_batch(cuda(wq), cuda(wd), cuda(aq), cuda(ad)))
+    ref = oracle.matvec(wq, wd, aq, ad)
+    assert np.all(rel_row_err(y.astype(np.float64), ref) <= 1e-5)
+
+
+@pytest.mark.parametrize("N,K", [(1024, 1024), (1000, 1056), (33, 96), (301, 5120)])
+def test_matvec_batched_equals_solo_bitwise(N, K):
+    wq, wd, aq, ad = mv_inputs(N, K, 16, seed=2)
+    W, D = cuda(wq), cuda(wd)
+    solo = [host(luce.luce_q8_matvec_batch(W, D, cuda(aq[t:t + 1]), cuda(ad[t:t + 1])))[0] for t in range(16)]
+    for T in range(1, 17):
+        yb = host(luce.luce_q8_matvec_batch(W, D, cuda(aq[:T]), cuda(ad[:T])))
+        for t in range(T):
+            assert np.array_equal(yb[t].view(np.uint32), solo[t].view(np.uint32)), (T, t)
+    perm = synth.permutation(2, 77, 16)
+    yp = host(luce.luce_q8_matvec_batch(W, D, cuda(aq[perm]), cuda(ad[perm])))
+    for i, t in enumerate(perm):
+        assert np.array_equal(yp[i].view(np.uint32), solo[t].view(np.uint32))
+
+
+def test_matvec_writes_only_its_outputs():
+    N, K, T = 100, 256, 3
+    wq, wd, aq, ad = mv_inputs(N, K, T)
+    buf = np.full((T + 1, N + 12), SENTINEL, np.uint32).view(np.float32)
+    yb = cuda(buf)
+    y = yb[:T, :N]
+    luce.load_library()
+    rc = luce.load_library().luce_q8_matvec_batch(cuda(wq).data_ptr(), cuda(wd).data_ptr(), N, K,
+                                                  cuda(aq).data_ptr(), cuda(ad).data_ptr(), T, y.data_ptr(),
+                                                  N + 12, torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    out = host(yb).view(np.uint32)
+    assert np.all(out[:T, N:] == SENTINEL) and np.all(out[T] == SENTINEL)
+    assert not np.any(out[:T, :N] == SENTINEL)
+
+
+# ------------------------------------------------------------ RoPE
+
+def test_rope_parity_and_rows_match_single_row_launches():
+    T, Hq = 16, 40
+    x = wl.qvec(2, T, Hq, sub=1)
+    pos = wl.positions(2, T)
+    pos[0], pos[1] = 0, 32767
+    xg = cuda(x)
+    luce.luce_rope_posvec(xg, cuda(pos), 1e6)
+    y = host(xg).astype(np.float64)
+    ref = oracle.rope(x, pos, 1e6)
+    pair = np.sqrt(ref[..., :64] ** 2 + ref[..., 64:] ** 2)
+    err = np.maximum(np.abs(y[..., :64] - ref[..., :64]), np.abs(y[..., 64:] - ref[..., 64:]))
+    assert np.all(err <= 1e-6 * pair + 1e-30)
+    assert np.array_equal(y[0], x[0].astype(np.float64))  # position 0 is the identity
+    for t in range(T):
+        x1 = cuda(x[t:t + 1])
+        luce.luce_rope_posvec(x1, cuda(pos[t:t + 1]), 1e6)
+        assert np.array_equal(host(x1)[0].view(np.uint32), host(xg)[t].view(np.uint32))
+
+
+# ------------------------------------------------------------ KV append
+
+def test_kv_append_bit_exact_and_in_place():
+    Hkv, cap, D = 2, 64, 128
+    k = wl.qvec(3, 4, Hkv, sub=2) * np.float32(7.0)
+    v = wl.qvec(3, 4, Hkv, sub=3)
+    kc = [cuda(np.full((Hkv, cap, D), 0x7E00, np.uint16).view(np.float16)) for _ in range(2)]
+    vc = [cuda(np.full((Hkv, cap, D), 0x7E00, np.uint16).view(np.float16)) for _ in range(2)]
+    views = [luce.SeqView(kc[0], vc[0], len=10, n_q=1, row0=0), luce.SeqView(kc[1], vc[1], len=40, n_q=3, row0=1)]
+    luce.luce_kv_append(cuda(k), cuda(v), views)
+    for s, (pos0, rows) in enumerate([(9, [0]), (37, [1, 2, 3])]):
+        kh = host(kc[s]).view(np.uint16)
+        vh = host(vc[s]).view(np.uint16)
+        for j, r in enumerate(rows):
+            assert np.array_equal(kh[:, pos0 + j], oracle.float_to_half_bits(k[r]).reshape(Hkv, D))
+            assert np.array_equal(vh[:, pos0 + j], oracle.float_to_half_bits(v[r]).reshape(Hkv, D))
+        mask = np.ones(cap, bool)
+        mask[pos0:pos0 + len(rows)] = False
+        assert np.all(kh[:, mask] == 0x7E00) and np.all(vh[:, mask] == 0x7E00)
+
+
+# ------------------------------------------------------------ attention
+
+def attn_case(seed, lens, nq, Hq, Hkv, cap=None):
+    D = 128
+    views, caches = [], []
+    row0 = 0
+    for s, (L, n) in enumerate(zip(lens, nq)):
+        c = cap or L
+        k, v = wl.cache_host(seed, s, 0, wl.Dims(0, Hq, Hkv, D, 0), c, L)
+        caches.append((k, v))
+        views.append((L, n, row0))
+        row0 += n
+    q = wl.qvec(seed, row0, Hq, sub=4)
+    return q, caches, views
+
+
+def run_attn(q, caches, views, Hkv, scale):
+    dev = [(cuda(k), cuda(v)) for k, v in caches]
+    sv = [luce.SeqView(k, v, L, n, r0) for (k, v), (L, n, r0) in zip(dev, views)]
+    return host(luce.luce_decode_attn_multiseq(cuda(q), sv, Hkv, scale))
+
+
+def oracle_attn(q, caches, views, Hkv, scale):
+    out = np.empty(q.shape, np.float64)
+    for (k, v), (L, n, r0) in zip(caches, views):
+        for j in range(n):
+            out[r0 + j] = oracle.attention_row(q[r0 + j], k, v, L - n + 1 + j, Hkv, scale)
+    return out
+
+
+@pytest.mark.parametrize("lens,nq,Hq,Hkv", [
+    (wl.TINY_ATTN_LENS, [1, 1, 1, 1], 8, 2),          # the tiny decode slice
+    ([1, 255, 256, 257], [1, 1, 1, 1], 8, 2),          # chunk edges
+    ([2051, 2051, 2051, 2051], [1, 1, 1, 1], 40, 8),   # the 27B layer's attention
+    ([1030, 1800, 2051, 1500], [4, 3, 2, 4], 40, 8),   # verify rows (causal)
+    ([600], [4], 4, 4),
+])
+def test_attention_parity(lens, nq, Hq, Hkv):
+    scale = np.float32(1 / math.sqrt(128))
+    q, caches, views = attn_case(5, lens, nq, Hq, Hkv)
+    got = run_attn(q, caches, views, Hkv, float(scale))
+    ref = oracle_attn(q, caches, views, Hkv, float(scale))
+    assert np.max(np.abs(got - ref)) <= 2e-3
+
+
+def test_attention_long_context_parity():
+    lens = wl.lens(3, 4, 16384, 32768)
+    scale = float(np.float32(1 / math.sqrt(128)))
+    q, caches, views = attn_case(3, lens, [1] * 4, 32, 8)
+    got = run_attn(q, caches, views, 8, scale)
+    ref = oracle_attn(q, caches, views, 8, scale)
+    assert np.max(np.abs(got - ref)) <= 2e-3
+
+
+def test_attention_batched_equals_solo_bitwise():
+    lens, nq = [1030, 1800, 2051, 700], [4, 3, 2, 1]
+    q, caches, views = attn_case(7, lens, nq, 40, 8)
+    batched = run_attn(q, caches, views, 8, 0.08838834764831845)
+    for s, (L, n, r0) in enumerate(views):
+        solo = run_attn(q[r0:r0 + n], [caches[s]], [(L, n, 0)], 8, 0.08838834764831845)
+        assert np.array_equal(solo.view(np.uint32), batched[r0:r0 + n].view(np.uint32))
+    # sequences in another order
+    order = [2, 0, 3, 1]
+    vv, qq, r0 = [], [], 0
+    for s in order:
+        L, n, old = views[s]
+        vv.append((L, n, r0))
+        qq.append(q[old:old + n])
+        r0 += n
+    perm = run_attn(np.concatenate(qq), [caches[s] for s in order], vv, 8, 0.08838834764831845)
+    for (L, n, newr0), s in zip(vv, order):
+        old = views[s][2]
+        assert np.array_equal(perm[newr0:newr0 + n].view(np.uint32), batched[old:old + n].view(np.uint32))
