@@ -29,7 +29,9 @@
  *     payloads.  q8_0 weights are stored as int8 wq[N][K] (row-major) plus
  *     binary16 wd[N][K/32]: 32 weights per block share one scale, 34 bytes
  *     per block in all.
- *   - Alignment: int8 rows and K/V rows start on 16-byte boundaries.
+ *   - Alignment: int8 weight and activation arrays start on 32-byte
+ *     boundaries (each q8_0 block is fetched as one 32-byte load); K/V
+ *     cache rows on 16-byte boundaries.
  */
 #ifndef LUCE_H
 #define LUCE_H
@@ -91,8 +93,8 @@ int luce_q8_quantize_act(const float* x, int T, int K, int64_t ldx, int8_t* q, f
  * 32 partials are summed pairwise by an xor butterfly over offsets
  * 16, 8, 4, 2, 1.  Hence y[t][.] is bitwise independent of T, of the other
  * rows and of the launch shape.
- *   wq (device) int8 [N][K], 16-byte aligned;  wd (device) binary16 [N][K/32]
- *   aq (device) int8 [T][K], 16-byte aligned;  ad (device) fp32 [T][K/32]
+ *   wq (device) int8 [N][K], 32-byte aligned;  wd (device) binary16 [N][K/32]
+ *   aq (device) int8 [T][K], 32-byte aligned;  ad (device) fp32 [T][K/32]
  *   y  (device) fp32 [T][ldy] (ldy >= N)
  * 1 <= T <= LUCE_MAX_ROWS, K % 32 == 0, N >= 1.
  */
@@ -111,7 +113,8 @@ int luce_q8_block_dots(const int8_t* wq, int N, int K, const int8_t* aq, int T, 
  * sequences sit at arbitrary positions; a row equals a single-row launch at
  * its own position].  Dims (i, i + D/2) of every head of row t rotate by
  * pos[t] * theta^(-2i/D).  The cosine and sine are evaluated in double
- * precision and rounded to fp32; the rotation itself is fp32.
+ * precision (theta^(-2i/D) and the angle in double, reduced modulo 2*pi before
+ * an fp32 sincos) and rounded to fp32; the rotation itself is fp32.
  *   x   (device) fp32, element (t, h, d) at t*ldx + h*D + d, rotated in place
  *   pos (device) int32 [T]
  * D == 128, 1 <= T <= LUCE_MAX_ROWS (any T >= 1 is accepted), n_heads >= 1,
@@ -160,7 +163,10 @@ int luce_kv_append(const float* k, const float* v, int64_t ldkv, int Hkv, int D,
  * by the exact log-sum-exp rule.  No output depends on the other rows.
  *   q   (device) fp32 [T][Hq][D] with T = max(row0 + n_q)
  *   out (device) fp32 [T][Hq][D]
- *   ws  (device) scratch of at least luce_decode_attn_workspace_size(...) bytes
+ *   ws  (device) scratch of at least luce_decode_attn_workspace_size(...)
+ *       bytes, 16-byte aligned; the call zeroes its first bytes itself.
+ * The chunk merge is done by whichever CTA of a (row, KV head) finishes last
+ * (an atomic ticket, no waiting); the merge order is the chunk order.
  * D == 128, Hq % Hkv == 0, Hq / Hkv <= 8, 1 <= n_seq <= LUCE_MAX_SEQ,
  * 1 <= len - n_q + 1, len <= cap.
  */
@@ -204,7 +210,7 @@ typedef struct luce_slot {
 /* Byte offsets of the step's intermediates inside its workspace (the last
  * layer's values remain there after the call; useful for inspection). */
 typedef struct luce_step_layout {
-    size_t rope_cs, xn, xn_q, xn_d, qkv, q_rot, part, attn, attn_q, attn_d, x1,
+    size_t tickets, xn, xn_q, xn_d, qkv, q_rot, part, attn, attn_q, attn_d, x1,
            xn2, xn2_q, xn2_d, gu, h, h_q, h_d, xf, xf_q, xf_d, total;
 } luce_step_layout;
 

@@ -20,6 +20,13 @@ using namespace luce;
 static std::atomic<uint64_t> g_launches{0};
 void luce::count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
+RopeFreq luce::rope_freq(double theta)
+{
+    RopeFreq f;
+    for (int i = 0; i < kHeadDim / 2; ++i) f.inv[i] = pow(theta, -2.0 * (double)i / (double)kHeadDim);
+    return f;
+}
+
 namespace {
 
 thread_local std::string g_err;
@@ -86,7 +93,7 @@ static int check_matvec(const int8_t* wq, const uint16_t* wd, int N, int K, cons
     REQUIRE(K >= 32 && K % 32 == 0, LUCE_EINVAL, "%s: K=%d must be a positive multiple of 32", who, K);
     REQUIRE(T >= 1 && T <= LUCE_MAX_ROWS, LUCE_EINVAL, "%s: T=%d outside 1..%d", who, T, LUCE_MAX_ROWS);
     REQUIRE(ldy >= N, LUCE_EINVAL, "%s: ldy=%lld < N", who, (long long)ldy);
-    REQUIRE(aligned(wq, 16) && aligned(aq, 16), LUCE_EINVAL, "%s: wq and aq must be 16-byte aligned", who);
+    REQUIRE(aligned(wq, 32) && aligned(aq, 32), LUCE_EINVAL, "%s: wq and aq must be 32-byte aligned", who);
     REQUIRE(aligned(wd, 2) && aligned(ad, 4) && aligned(y, 4), LUCE_EINVAL, "%s: misaligned wd/ad/y", who);
     REQUIRE((int64_t)N * K < ((int64_t)1 << 40), LUCE_EINVAL, "%s: N*K too large", who);
     return LUCE_OK;
@@ -107,7 +114,7 @@ int luce_q8_block_dots(const int8_t* wq, int N, int K, const int8_t* aq, int T, 
     REQUIRE(wq && aq && out, LUCE_EINVAL, "q8_block_dots: null pointer");
     REQUIRE(N >= 1 && T >= 1 && T <= LUCE_MAX_ROWS, LUCE_EINVAL, "q8_block_dots: bad N=%d or T=%d", N, T);
     REQUIRE(K >= 32 && K % 32 == 0, LUCE_EINVAL, "q8_block_dots: K=%d must be a positive multiple of 32", K);
-    REQUIRE(aligned(wq, 16) && aligned(aq, 16) && aligned(out, 4), LUCE_EINVAL, "q8_block_dots: misaligned");
+    REQUIRE(aligned(wq, 32) && aligned(aq, 32) && aligned(out, 4), LUCE_EINVAL, "q8_block_dots: misaligned");
     return cuda_status(launch_block_dots(wq, N, K, aq, T, out, (cudaStream_t)stream), "q8_block_dots");
 }
 
@@ -120,7 +127,8 @@ int luce_rope_posvec(float* x, int T, int n_heads, int D, int64_t ldx, const int
     REQUIRE(ldx >= (int64_t)n_heads * D, LUCE_EINVAL, "rope_posvec: ldx too small");
     REQUIRE(theta > 0 && isfinite(theta), LUCE_EINVAL, "rope_posvec: theta must be positive");
     REQUIRE(aligned(x, 4) && aligned(pos, 4), LUCE_EINVAL, "rope_posvec: misaligned");
-    return cuda_status(launch_rope_posvec(x, T, n_heads, ldx, pos, theta, (cudaStream_t)stream), "rope_posvec");
+    return cuda_status(launch_rope_posvec(x, T, n_heads, ldx, pos, rope_freq(theta), (cudaStream_t)stream),
+                       "rope_posvec");
 }
 
 // Validates views and returns the number of rows they cover (rows 0..T-1,
@@ -179,10 +187,14 @@ int luce_kv_append(const float* k, const float* v, int64_t ldkv, int Hkv, int D,
     return cuda_status(launch_kv_append(k, v, ldkv, Hkv, rows, (cudaStream_t)stream), "kv_append");
 }
 
+// Attention scratch: tickets (one int per row and KV head, at most
+// LUCE_MAX_ROWS * Hq of them) in the first bytes, then the chunk partials.
+static size_t attn_ticket_bytes(int Hq) { return align_up((size_t)LUCE_MAX_ROWS * Hq * sizeof(int), 256); }
+
 size_t luce_decode_attn_workspace_size(int n_rows, int Hq, int D, int max_len)
 {
     if (n_rows < 1 || Hq < 1 || D != LUCE_HEAD_DIM || max_len < 1) return 0;
-    return attn_part_floats(n_rows * chunks_of(max_len), Hq) * sizeof(float);
+    return attn_ticket_bytes(Hq) + attn_part_floats(n_rows * chunks_of(max_len), Hq) * sizeof(float);
 }
 
 static void build_attn_rows(const luce_seqview* views, int n_seq, AttnRows& rows, int T)
@@ -219,10 +231,14 @@ int luce_decode_attn_multiseq(const float* q, const luce_seqview* views, int n_s
     if (rc) return rc;
     AttnRows rows{};
     build_attn_rows(views, n_seq, rows, T);
-    const size_t need = attn_part_floats(rows.total_chunks, Hq) * sizeof(float);
+    const size_t tb = attn_ticket_bytes(Hq);
+    const size_t need = tb + attn_part_floats(rows.total_chunks, Hq) * sizeof(float);
     REQUIRE(ws_bytes >= need, LUCE_ENOSPACE, "decode_attn: workspace %zu bytes < %zu needed", ws_bytes, need);
-    return cuda_status(launch_attention(q, (int64_t)Hq * D, rows, Hq, Hkv, scale, (float*)ws, out,
-                                        (int64_t)Hq * D, (cudaStream_t)stream),
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaMemsetAsync(ws, 0, (size_t)T * Hkv * sizeof(int), st);
+    if (e != cudaSuccess) return cuda_status(e, "decode_attn");
+    return cuda_status(launch_attention(q, (int64_t)Hq * D, rows, Hq, Hkv, scale, (float*)((char*)ws + tb), (int*)ws,
+                                        out, (int64_t)Hq * D, nullptr, nullptr, st),
                        "decode_attn");
 }
 
@@ -256,7 +272,7 @@ static void layout_of(const luce_model* m, int T, int max_ctx, luce_step_layout*
         o = align_up(o + bytes, 256);
         return at;
     };
-    L->rope_cs = take(T * (D / 2) * sizeof(float2));
+    L->tickets = take((size_t)T * Hkv * sizeof(int));
     L->xn = take(T * H * 4);
     L->xn_q = take(T * H);
     L->xn_d = take(T * H / 32 * 4);
@@ -330,17 +346,17 @@ int luce_decode_step(const luce_model* m, const luce_slot* slots, const int32_t*
         REQUIRE(w.attn_norm && w.wqkv_q && w.wqkv_d && w.wo_q && w.wo_d && w.ffn_norm && w.wgu_q && w.wgu_d &&
                     w.wdown_q && w.wdown_d,
                 LUCE_EINVAL, "%s: layer %d has a null weight", who, l);
-        REQUIRE(aligned(w.wqkv_q, 16) && aligned(w.wo_q, 16) && aligned(w.wgu_q, 16) && aligned(w.wdown_q, 16),
-                LUCE_EINVAL, "%s: layer %d int8 weights must be 16-byte aligned", who, l);
+        REQUIRE(aligned(w.wqkv_q, 32) && aligned(w.wo_q, 32) && aligned(w.wgu_q, 32) && aligned(w.wdown_q, 32),
+                LUCE_EINVAL, "%s: layer %d int8 weights must be 32-byte aligned", who, l);
     }
-    REQUIRE(!logits || aligned(m->head_q, 16), LUCE_EINVAL, "%s: head weights must be 16-byte aligned", who);
+    REQUIRE(!logits || aligned(m->head_q, 32), LUCE_EINVAL, "%s: head weights must be 32-byte aligned", who);
 
     luce_step_layout L;
     layout_of(m, T, max_len, &L);
     REQUIRE(ws_bytes >= L.total, LUCE_ENOSPACE, "%s: workspace %zu bytes < %zu needed", who, ws_bytes, L.total);
 
     char* wsb = (char*)ws;
-    float2* rope_cs = (float2*)(wsb + L.rope_cs);
+    int* tickets = (int*)(wsb + L.tickets);
     float* xn = (float*)(wsb + L.xn);
     int8_t* xn_q = (int8_t*)(wsb + L.xn_q);
     float* xn_d = (float*)(wsb + L.xn_d);
@@ -372,7 +388,9 @@ int luce_decode_step(const luce_model* m, const luce_slot* slots, const int32_t*
                 pos.pos[r] = slots[s].len + j;
             }
     }
-    cudaError_t e = launch_rope_table(pos, m->rope_theta, rope_cs, st);
+    const RopeFreq freq = rope_freq(m->rope_theta);
+    // attention tickets start at zero; every launch leaves them zero again
+    cudaError_t e = cudaMemsetAsync(tickets, 0, (size_t)T * Hkv * sizeof(int), st);
     if (e != cudaSuccess) return cuda_status(e, who);
 
     const float scale = (float)(1.0 / sqrt((double)D));
@@ -408,10 +426,10 @@ int luce_decode_step(const luce_model* m, const luce_slot* slots, const int32_t*
         if ((e = launch_matvec(w.wqkv_q, (const __half*)w.wqkv_d, (int)qkv_rows, H, xn_q, xn_d, T, qkv, qkv_rows,
                                nullptr, 0, st)))
             break;
-        if ((e = launch_rope_kv(qkv, T, Hq, Hkv, rope_cs, q_rot, kv, st))) break;
-        if ((e = launch_attention(q_rot, (int64_t)Hq * D, ar, Hq, Hkv, scale, part, attn, (int64_t)Hq * D, st)))
+        if ((e = launch_rope_kv(qkv, T, Hq, Hkv, pos, freq, q_rot, kv, st))) break;
+        if ((e = launch_attention(q_rot, (int64_t)Hq * D, ar, Hq, Hkv, scale, part, tickets, attn, (int64_t)Hq * D,
+                                  attn_q, attn_d, st)))
             break;
-        if ((e = launch_quantize(attn, T, Hq * D, (int64_t)Hq * D, attn_q, attn_d, st))) break;
         if ((e = launch_matvec(w.wo_q, (const __half*)w.wo_d, H, Hq * D, attn_q, attn_d, T, x1, H, x, H, st)))
             break;
         if ((e = launch_rmsnorm_quant(x1, T, H, w.ffn_norm, m->rms_eps, xn2, xn2_q, xn2_d, st))) break;

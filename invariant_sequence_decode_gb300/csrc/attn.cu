@@ -5,8 +5,8 @@
 // each attending to its own cache, per-sequence views passed by value (max 4);
 // section 2: one multi-sequence attention launch with no position limit.
 //
-// Pass 1 (one CTA per (row, chunk of 256 keys, KV head g)): the CTA serves
-// all Hq/Hkv query heads of g, so each K/V byte is read once per row.
+// One CTA per (row, chunk of 256 keys, KV head g) serves all Hq/Hkv query
+// heads of g, so each K/V byte is read once per row:
 //   scores   thread j owns key j of the chunk: 16 x 16-byte loads of its K row,
 //            s_h = scale * (q_h . k_j) with fma over d = 0..127 ascending;
 //   softmax  warp h owns head h: m = max_j s_h, p_j = exp(s_h - m),
@@ -15,11 +15,13 @@
 //            o_h += p_hj * v_j (fma, keys ascending); the 8 warp partials are
 //            added in warp order.
 //   -> scratch (o_h[128], m_h, l_h) for the chunk.
-// Pass 2 (one CTA per (row, q head), thread = dim): M = max_c m_c,
-//   L = sum_c l_c e^(m_c - M), O = sum_c o_c e^(m_c - M) in chunk order,
-//   out = O / L.
+// The CTA that finishes last for its (row, g) (an atomic ticket; nobody
+// waits) merges the row's chunks in chunk order:
+//   M = max_c m_c, L = sum_c l_c e^(m_c - M), O = sum_c o_c e^(m_c - M),
+//   out = O / L,
+// and optionally quantizes out to q8_0 blocks (the Wo projection's input).
 // The chunking and every reduction order depend only on the row's own key
-// count, never on the other rows or on the grid.
+// count, never on the other rows, on which CTA merges or on the grid.
 #include <math.h>
 
 #include "common.cuh"
@@ -33,12 +35,14 @@ size_t attn_part_floats(int total_chunks, int Hq) { return (size_t)total_chunks 
 
 template <int GQ>
 __global__ void __launch_bounds__(256)
-attn_partial_kernel(const float* __restrict__ q, int64_t ldq, AttnRows rows, int Hq, float scale,
-                    float* __restrict__ part)
+attn_kernel(const float* __restrict__ q, int64_t ldq, AttnRows rows, int Hq, int Hkv, float scale,
+            float* __restrict__ part, int* __restrict__ tickets, float* __restrict__ out, int64_t ldo,
+            int8_t* __restrict__ out_q, float* __restrict__ out_d)
 {
     __shared__ __align__(16) float q_s[GQ][kHeadDim];
     __shared__ float p_s[GQ][kAttnChunk];
     __shared__ __align__(16) float red[8][GQ][kHeadDim];
+    __shared__ int last;
 
     const int chunk = blockIdx.x, g = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -49,9 +53,17 @@ attn_partial_kernel(const float* __restrict__ q, int64_t ldq, AttnRows rows, int
         if (chunk >= rows.row[i].chunk0) r = i;
     const AttnRow row = rows.row[r];
     const int c = chunk - row.chunk0;
+    const int nch = (row.len + kAttnChunk - 1) / kAttnChunk;
     const int key0 = c * kAttnChunk;
     const int nvalid = min(kAttnChunk, row.len - key0);
     const int h0 = g * GQ;
+    const __half* kbase = row.k + g * row.head_stride + (int64_t)key0 * row.tok_stride;
+    const __half* vbase = row.v + g * row.head_stride + (int64_t)key0 * row.tok_stride;
+    if (tid == 0) {
+        // the chunk's V rows are needed after the scores: stage them in L2 now
+        const uint32_t span = (uint32_t)(((int64_t)(nvalid - 1) * row.tok_stride + kHeadDim) * 2);
+        prefetch_l2(vbase, span);
+    }
 
     for (int i = tid; i < GQ * kHeadDim; i += 256)
         q_s[i / kHeadDim][i % kHeadDim] = q[(size_t)r * ldq + (size_t)(h0 + i / kHeadDim) * kHeadDim + i % kHeadDim];
@@ -64,7 +76,7 @@ attn_partial_kernel(const float* __restrict__ q, int64_t ldq, AttnRows rows, int
         for (int h = 0; h < GQ; ++h) dot[h] = 0.0f;
         const int j = tid;
         if (j < nvalid) {
-            const int4* kp = reinterpret_cast<const int4*>(row.k + g * row.head_stride + (int64_t)(key0 + j) * row.tok_stride);
+            const int4* kp = reinterpret_cast<const int4*>(kbase + (int64_t)j * row.tok_stride);
             int4 kv[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) kv[i] = __ldg(kp + i);
@@ -115,25 +127,36 @@ attn_partial_kernel(const float* __restrict__ q, int64_t ldq, AttnRows rows, int
     }
     __syncthreads();
 
-    // ---- p . V
+    // ---- p . V  (keys w, w+8, ...; loads issued 8 keys at a time)
     {
         float o[GQ][4];
 #pragma unroll
         for (int h = 0; h < GQ; ++h)
 #pragma unroll
             for (int e = 0; e < 4; ++e) o[h][e] = 0.0f;
-        const __half* vbase = row.v + g * row.head_stride + (int64_t)key0 * row.tok_stride + lane * 4;
-        for (int j = warp; j < nvalid; j += 8) {
-            const uint2 raw = __ldg(reinterpret_cast<const uint2*>(vbase + (int64_t)j * row.tok_stride));
-            const float2 v01 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
-            const float2 v23 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+        const __half* vl = vbase + lane * 4;
+        for (int j0 = warp; j0 < nvalid; j0 += 64) {
+            uint2 raw[8];
 #pragma unroll
-            for (int h = 0; h < GQ; ++h) {
-                const float p = p_s[h][j];
-                o[h][0] = __fmaf_rn(p, v01.x, o[h][0]);
-                o[h][1] = __fmaf_rn(p, v01.y, o[h][1]);
-                o[h][2] = __fmaf_rn(p, v23.x, o[h][2]);
-                o[h][3] = __fmaf_rn(p, v23.y, o[h][3]);
+            for (int u = 0; u < 8; ++u) {
+                const int j = j0 + 8 * u;
+                if (j < nvalid) raw[u] = __ldg(reinterpret_cast<const uint2*>(vl + (int64_t)j * row.tok_stride));
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int j = j0 + 8 * u;
+                if (j < nvalid) {
+                    const float2 v01 = __half22float2(*reinterpret_cast<const __half2*>(&raw[u].x));
+                    const float2 v23 = __half22float2(*reinterpret_cast<const __half2*>(&raw[u].y));
+#pragma unroll
+                    for (int h = 0; h < GQ; ++h) {
+                        const float p = p_s[h][j];
+                        o[h][0] = __fmaf_rn(p, v01.x, o[h][0]);
+                        o[h][1] = __fmaf_rn(p, v01.y, o[h][1]);
+                        o[h][2] = __fmaf_rn(p, v23.x, o[h][2]);
+                        o[h][3] = __fmaf_rn(p, v23.y, o[h][3]);
+                    }
+                }
             }
         }
 #pragma unroll
@@ -148,56 +171,68 @@ attn_partial_kernel(const float* __restrict__ q, int64_t ldq, AttnRows rows, int
         for (int w = 1; w < 8; ++w) s = __fadd_rn(s, red[w][h][d]);
         pout[(size_t)h * kPartStride + d] = s;
     }
-}
 
-__global__ void __launch_bounds__(128)
-attn_merge_kernel(AttnRows rows, int Hq, const float* __restrict__ part, float* __restrict__ out, int64_t ldo)
-{
-    const int r = blockIdx.x / Hq, h = blockIdx.x - (blockIdx.x / Hq) * Hq;
-    const int d = threadIdx.x;
-    const AttnRow row = rows.row[r];
-    const int nch = (row.len + kAttnChunk - 1) / kAttnChunk;
-    const float* base = part + ((size_t)row.chunk0 * Hq + h) * kPartStride;
+    // ---- the last CTA of (row, g) merges the row's chunks
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) last = (atomicAdd(&tickets[r * Hkv + g], 1) == nch - 1);
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    const float* base = part + ((size_t)row.chunk0 * Hq + h0) * kPartStride;
     const size_t cstride = (size_t)Hq * kPartStride;
-    float M = -INFINITY;
-    for (int c = 0; c < nch; ++c) M = fmaxf(M, base[c * cstride + 128]);
-    float L = 0.0f, O = 0.0f;
-    for (int c = 0; c < nch; ++c) {
-        const float* pc = base + c * cstride;
-        const float w = expf(__fsub_rn(pc[128], M));
-        L = __fmaf_rn(pc[129], w, L);
-        O = __fmaf_rn(pc[d], w, O);
+    for (int blk = warp; blk < GQ * (kHeadDim / 32); blk += 8) {
+        const int h = blk / (kHeadDim / 32), d = (blk % (kHeadDim / 32)) * 32 + lane;
+        const float* bh = base + (size_t)h * kPartStride;
+        float M = -INFINITY;
+        for (int cc = 0; cc < nch; ++cc) M = fmaxf(M, __ldcg(bh + cc * cstride + 128));
+        float L = 0.0f, O = 0.0f;
+        for (int cc = 0; cc < nch; ++cc) {
+            const float* pc = bh + cc * cstride;
+            const float w = expf(__fsub_rn(__ldcg(pc + 128), M));
+            L = __fmaf_rn(__ldcg(pc + 129), w, L);
+            O = __fmaf_rn(__ldcg(pc + d), w, O);
+        }
+        const float val = __fdiv_rn(O, L);
+        const size_t oi = (size_t)r * ldo + (size_t)(h0 + h) * kHeadDim + d;
+        out[oi] = val;
+        if (out_q) {
+            float dd;
+            const int code = q8_quantize_lane(val, &dd);
+            out_q[oi] = (int8_t)code;
+            if (lane == 0) out_d[oi / 32] = dd;
+        }
     }
-    out[(size_t)r * ldo + (size_t)h * kHeadDim + d] = __fdiv_rn(O, L);
+    if (tid == 0) tickets[r * Hkv + g] = 0;  // ready for the next launch
 }
 
 template <int GQ>
-static void launch_partial(const float* q, int64_t ldq, const AttnRows& rows, int Hq, int Hkv, float scale,
-                           float* part, cudaStream_t s)
+static void launch_g(const float* q, int64_t ldq, const AttnRows& rows, int Hq, int Hkv, float scale, float* part,
+                     int* tickets, float* out, int64_t ldo, int8_t* out_q, float* out_d, cudaStream_t s)
 {
-    dim3 grid(rows.total_chunks, Hkv);
-    attn_partial_kernel<GQ><<<grid, 256, 0, s>>>(q, ldq, rows, Hq, scale, part);
+    attn_kernel<GQ><<<dim3(rows.total_chunks, Hkv), 256, 0, s>>>(q, ldq, rows, Hq, Hkv, scale, part, tickets, out,
+                                                                   ldo, out_q, out_d);
     count_launches(1);
 }
 
-cudaError_t launch_attention(const float* q, int64_t ldq, const AttnRows& rows, int Hq, int Hkv,
-                             float scale, float* part, float* out, int64_t ldo, cudaStream_t s)
+cudaError_t launch_attention(const float* q, int64_t ldq, const AttnRows& rows, int Hq, int Hkv, float scale,
+                             float* part, int* tickets, float* out, int64_t ldo, int8_t* out_q, float* out_d,
+                             cudaStream_t s)
 {
     switch (Hq / Hkv) {
-        case 1: launch_partial<1>(q, ldq, rows, Hq, Hkv, scale, part, s); break;
-        case 2: launch_partial<2>(q, ldq, rows, Hq, Hkv, scale, part, s); break;
-        case 3: launch_partial<3>(q, ldq, rows, Hq, Hkv, scale, part, s); break;
-        case 4: launch_partial<4>(q, ldq, rows, Hq, Hkv, scale, part, s); break;
-        case 5: launch_partial<5>(q, ldq, rows, Hq, Hkv, scale, part, s); break;
-        case 6: launch_partial<6>(q, ldq, rows, Hq, Hkv, scale, part, s); break;
-        case 7: launch_partial<7>(q, ldq, rows, Hq, Hkv, scale, part, s); break;
-        case 8: launch_partial<8>(q, ldq, rows, Hq, Hkv, scale, part, s); break;
+#define LUCE_AT(G) \
+    case G: launch_g<G>(q, ldq, rows, Hq, Hkv, scale, part, tickets, out, ldo, out_q, out_d, s); break;
+        LUCE_AT(1)
+        LUCE_AT(2)
+        LUCE_AT(3)
+        LUCE_AT(4)
+        LUCE_AT(5)
+        LUCE_AT(6)
+        LUCE_AT(7)
+        LUCE_AT(8)
+#undef LUCE_AT
         default: return cudaErrorInvalidValue;
     }
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    attn_merge_kernel<<<rows.n_rows * Hq, kHeadDim, 0, s>>>(rows, Hq, part, out, ldo);
-    count_launches(1);
     return cudaGetLastError();
 }
 

@@ -41,10 +41,49 @@ __device__ __forceinline__ unsigned short ld_stream_u16(const void* p)
     return r;
 }
 
+// 32-byte loads (one whole q8_0 block per lane); the address must be 32-byte
+// aligned.  Streaming variant for weights, L1-cached variant for activations
+// that every warp of the CTA re-reads.
+__device__ __forceinline__ void ld_stream_v8(const void* p, uint32_t (&v)[8])
+{
+    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+                 : "l"(p));
+}
+
+__device__ __forceinline__ void ld_cached_v8(const void* p, uint32_t (&v)[8])
+{
+    asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+                 : "l"(p));
+}
+
+// Ask the memory system to stage `bytes` (multiple of 16, 16-byte aligned
+// address) into L2 ahead of use.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // ---------------------------------------------------------------- q8_0
 
-// Integer dot of one 32-value block held as two 16-byte vectors per side.
+// Integer dot of one 32-value block held as 8 words per side, as two
+// independent dp4a chains (integer sums are exact in any order).
 // Exact: |result| <= 32 * 127 * 127 < 2^24.
+__device__ __forceinline__ int block_dot8(const uint32_t (&w)[8], const uint32_t (&a)[8])
+{
+    int s0 = __dp4a((int)w[0], (int)a[0], 0);
+    int s1 = __dp4a((int)w[4], (int)a[4], 0);
+    s0 = __dp4a((int)w[1], (int)a[1], s0);
+    s1 = __dp4a((int)w[5], (int)a[5], s1);
+    s0 = __dp4a((int)w[2], (int)a[2], s0);
+    s1 = __dp4a((int)w[6], (int)a[6], s1);
+    s0 = __dp4a((int)w[3], (int)a[3], s0);
+    s1 = __dp4a((int)w[7], (int)a[7], s1);
+    return s0 + s1;
+}
+
+// Integer dot of one 32-value block held as two 16-byte vectors per side.
 __device__ __forceinline__ int block_dot(const int4 w0, const int4 w1, const int4 a0, const int4 a1)
 {
     int s = __dp4a(w0.x, a0.x, 0);
@@ -111,14 +150,20 @@ __device__ __forceinline__ void rope_rotate(float& x0, float& x1, float c, float
     x1 = b;
 }
 
-// cos/sin of pos * theta^(-2i/D), evaluated in double and rounded to fp32.
-__device__ __forceinline__ float2 rope_cs(int pos, int i, int D, double theta)
+// cos/sin of the angle pos * inv_freq (inv_freq = theta^(-2i/D), evaluated
+// in double on the host).  The angle is formed in double and reduced modulo
+// 2*pi by Cody-Waite with a two-term 2*pi (the remainder keeps ~1e-12
+// absolute accuracy up to position 32767 and far beyond), then rounded to
+// fp32 (|r| <= pi, error <= 2e-7) for sincosf.
+__device__ __forceinline__ float2 rope_cs(int pos, double inv_freq)
 {
-    const double inv = pow(theta, -2.0 * (double)i / (double)D);
-    const double ang = (double)pos * inv;
-    double s, c;
-    sincos(ang, &s, &c);
-    return make_float2((float)c, (float)s);
+    const double ang = (double)pos * inv_freq;
+    const double k = rint(ang * 0.15915494309189535);
+    double r = fma(-k, 6.283185307179586, ang);
+    r = fma(-k, 2.4492935982947064e-16, r);
+    float s, c;
+    sincosf((float)r, &s, &c);
+    return make_float2(c, s);
 }
 
 // ---------------------------------------------------------------- SwiGLU

@@ -37,21 +37,34 @@ cudaError_t launch_quantize(const float* x, int T, int K, int64_t ldx, int8_t* q
     return cudaGetLastError();
 }
 
-// RMSNorm of one row per CTA, then q8_0 quantization of the normalised row.
-// Sum of squares: thread i adds x[i], x[i+256], ... with fma in ascending
-// order; warp partials by butterfly; thread 0 adds the 8 warp sums in order.
-// r = 1 / sqrt(ss / H + eps) with IEEE division and square root.
-__global__ void __launch_bounds__(256)
+// RMSNorm of one row per CTA (512 threads), then q8_0 quantization of the
+// normalised row.  Sum of squares: thread i adds x[i], x[i+512], ... with fma
+// in ascending order (its loads are all issued before the adds); warp
+// partials by butterfly; thread 0 adds the 16 warp sums in warp order.
+// r = 1 / sqrt(ss / H + eps) with IEEE division and square root.  The order
+// depends on H only.
+constexpr int kNormThreads = 512;
+
+__global__ void __launch_bounds__(kNormThreads)
 rmsnorm_quant_kernel(const float* __restrict__ x, int H, const float* __restrict__ gamma, float eps,
                      float* __restrict__ xn, int8_t* __restrict__ q, float* __restrict__ d)
 {
-    __shared__ float red[8];
+    constexpr int NW = kNormThreads / 32;
+    __shared__ float red[NW];
     __shared__ float rs;
     const int t = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float* xr = x + (size_t)t * H;
     float ss = 0.0f;
-    for (int i = tid; i < H; i += 256) {
+    int i = tid;
+    for (; i + 3 * kNormThreads < H; i += 4 * kNormThreads) {
+        const float v0 = xr[i], v1 = xr[i + kNormThreads], v2 = xr[i + 2 * kNormThreads], v3 = xr[i + 3 * kNormThreads];
+        ss = __fmaf_rn(v0, v0, ss);
+        ss = __fmaf_rn(v1, v1, ss);
+        ss = __fmaf_rn(v2, v2, ss);
+        ss = __fmaf_rn(v3, v3, ss);
+    }
+    for (; i < H; i += kNormThreads) {
         const float v = xr[i];
         ss = __fmaf_rn(v, v, ss);
     }
@@ -60,20 +73,20 @@ rmsnorm_quant_kernel(const float* __restrict__ x, int H, const float* __restrict
     __syncthreads();
     if (tid == 0) {
         float tot = red[0];
-        for (int w = 1; w < 8; ++w) tot = __fadd_rn(tot, red[w]);
+        for (int w = 1; w < NW; ++w) tot = __fadd_rn(tot, red[w]);
         const float mean = __fdiv_rn(tot, (float)H);
         rs = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
     }
     __syncthreads();
     const float r = rs;
     const int nb = H >> 5;
-    for (int b = warp; b < nb; b += 8) {
-        const int i = b * 32 + lane;
-        const float v = __fmul_rn(__fmul_rn(xr[i], r), gamma[i]);
-        xn[(size_t)t * H + i] = v;
+    for (int b = warp; b < nb; b += NW) {
+        const int k = b * 32 + lane;
+        const float v = __fmul_rn(__fmul_rn(xr[k], r), gamma[k]);
+        xn[(size_t)t * H + k] = v;
         float dd;
         const int code = q8_quantize_lane(v, &dd);
-        q[(size_t)t * H + i] = (int8_t)code;
+        q[(size_t)t * H + k] = (int8_t)code;
         if (lane == 0) d[(size_t)t * nb + b] = dd;
     }
 }
@@ -81,7 +94,7 @@ rmsnorm_quant_kernel(const float* __restrict__ x, int H, const float* __restrict
 cudaError_t launch_rmsnorm_quant(const float* x, int T, int H, const float* gamma, float eps,
                                  float* xn, int8_t* q, float* d, cudaStream_t s)
 {
-    rmsnorm_quant_kernel<<<T, 256, 0, s>>>(x, H, gamma, eps, xn, q, d);
+    rmsnorm_quant_kernel<<<T, kNormThreads, 0, s>>>(x, H, gamma, eps, xn, q, d);
     count_launches(1);
     return cudaGetLastError();
 }

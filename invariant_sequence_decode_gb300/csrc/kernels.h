@@ -44,6 +44,13 @@ struct RowPos {
     int n_rows;
 };
 
+// RoPE inverse frequencies theta^(-2i/128), i < 64, evaluated in double on
+// the host and passed by value.
+struct RopeFreq {
+    double inv[64];
+};
+RopeFreq rope_freq(double theta);
+
 cudaError_t launch_quantize(const float* x, int T, int K, int64_t ldx, int8_t* q, float* d, cudaStream_t s);
 
 cudaError_t launch_matvec(const int8_t* wq, const __half* wd, int N, int K, const int8_t* aq,
@@ -54,7 +61,7 @@ cudaError_t launch_block_dots(const int8_t* wq, int N, int K, const int8_t* aq, 
                               cudaStream_t s);
 
 cudaError_t launch_rope_posvec(float* x, int T, int n_heads, int64_t ldx, const int32_t* pos,
-                               double theta, cudaStream_t s);
+                               const RopeFreq& f, cudaStream_t s);
 
 cudaError_t launch_kv_append(const float* k, const float* v, int64_t ld, int Hkv, const KvRows& rows,
                              cudaStream_t s);
@@ -62,8 +69,11 @@ cudaError_t launch_kv_append(const float* k, const float* v, int64_t ld, int Hkv
 // Scratch floats for `total_chunks` chunks of Hq heads.
 size_t attn_part_floats(int total_chunks, int Hq);
 
+// tickets: n_rows * Hkv ints that are zero on entry (and zero again on exit).
+// out_q / out_d (nullable): q8_0 codes and scales of out (requires ldo == Hq*128).
 cudaError_t launch_attention(const float* q, int64_t ldq, const AttnRows& rows, int Hq, int Hkv,
-                             float scale, float* part, float* out, int64_t ldo, cudaStream_t s);
+                             float scale, float* part, int* tickets, float* out, int64_t ldo,
+                             int8_t* out_q, float* out_d, cudaStream_t s);
 
 cudaError_t launch_rmsnorm_quant(const float* x, int T, int H, const float* gamma, float eps,
                                  float* xn, int8_t* q, float* d, cudaStream_t s);
@@ -71,10 +81,8 @@ cudaError_t launch_rmsnorm_quant(const float* x, int T, int H, const float* gamm
 cudaError_t launch_swiglu_quant(const float* gu, int T, int F, float* h, int8_t* q, float* d,
                                 cudaStream_t s);
 
-cudaError_t launch_rope_table(const RowPos& pos, double theta, float2* cs, cudaStream_t s);
-
-cudaError_t launch_rope_kv(const float* qkv, int T, int Hq, int Hkv, const float2* cs, float* q_rot,
-                           const KvRows& rows, cudaStream_t s);
+cudaError_t launch_rope_kv(const float* qkv, int T, int Hq, int Hkv, const RowPos& pos, const RopeFreq& f,
+                           float* q_rot, const KvRows& rows, cudaStream_t s);
 
 cudaError_t launch_argmax(const float* x, int T, int V, int32_t* out, cudaStream_t s);
 

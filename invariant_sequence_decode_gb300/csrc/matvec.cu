@@ -5,113 +5,111 @@
 // concurrent serving", How it stays exact: a 4-row batch must use the same
 // arithmetic as one row.
 //
-// Work split: one warp owns G consecutive output rows n and sweeps the whole
-// K extent; lane l owns the blocks b = l, l + 32, l + 64, ... of those rows.
-// Per block the lane loads the 32 weights (two 16-byte streaming loads, L1
-// bypassed) and the fp16 scale once, then for each of the T activation rows
-// (L1-resident, shared by all warps) forms the exact int32 block dot with
-// eight dp4a and folds it into that row's partial:
-//     acc[t] = fma(fp16(wd) * ad[t][b], (float)sumi, acc[t])
-// The 32 lane partials are then summed by an xor butterfly (16, 8, 4, 2, 1).
-// The order of every floating-point operation on y[t][n] depends only on K:
-// not on T, G, the unroll depth U or the grid, so any launch gives the same
-// bits for a row as a launch of that row alone.
+// Reduction order (a function of K only): the blocks b of a weight row feed
+// 32 partial sums ("chains"), block b into chain b mod 32; each chain adds
+// its blocks in ascending order, acc = fma(fp16(wd) * ad[t], (float)sumi, acc),
+// where sumi is the block's exact int32 dot; the 32 chain values are then
+// summed pairwise as an xor butterfly over offsets 16, 8, 4, 2, 1.  Nothing
+// in that order depends on the number of activation rows T, on the other
+// rows or on the launch shape, so a row of any launch equals the same row
+// launched alone, bit for bit.
+//
+// Work split (GB300): a CTA owns RW = 32/KL consecutive weight rows and has
+// 32/KL warps.  Lane (r = lane / KL, kb = lane % KL) of warp w runs chain
+// c = kb + KL*w of row r, so each warp instruction reads KL consecutive
+// 32-byte blocks of each of RW rows (KL*32 contiguous bytes per row, one
+// 32-byte load per lane, L1 bypassed) and every activation block is one
+// address shared by RW lanes (a broadcast through L1).  A lane keeps one
+// block in flight while it computes the previous one.  The chain values
+// meet in shared memory, where one thread per (row, token) applies the
+// butterfly's pairings in the same order.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace luce {
 
-template <int T, int G, int U>
-__global__ void __launch_bounds__(256)
+template <int T, int KL, bool PF>
+__global__ void __launch_bounds__(32 * (32 / KL))
 q8_matvec_kernel(const int8_t* __restrict__ wq, const __half* __restrict__ wd, int N, int K,
                  const int8_t* __restrict__ aq, const float* __restrict__ ad,
                  float* y, int64_t ldy, const float* resid, int64_t ldr)
 {
-    const int lane = threadIdx.x & 31;
-    const int warp = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int n0 = warp * G;
-    if (n0 >= N) return;
+    constexpr int RW = 32 / KL;
+    __shared__ float part[RW][T][33];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int r = lane / KL, kb = lane - (lane / KL) * KL;
+    const int c = kb + KL * w;
+    const int row0 = blockIdx.x * RW;
+    const int rowc = min(row0 + r, N - 1);
     const int nb = K >> 5;
+    const int8_t* wp = wq + (size_t)rowc * K + (size_t)c * 32;
+    const __half* dp = wd + (size_t)rowc * nb + c;
+    if (PF && threadIdx.x == 0) prefetch_l2(wq + (size_t)row0 * K, (uint32_t)(min(RW, N - row0) * K));
+    const int nj = (nb - c + 31) >> 5;  // blocks of this chain (>= 0)
 
-    const int8_t* wrow[G];
-    const __half* drow[G];
+    float acc[T];
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-        const int n = min(n0 + g, N - 1);
-        wrow[g] = wq + (size_t)n * (size_t)K;
-        drow[g] = wd + (size_t)n * (size_t)nb;
-    }
+    for (int t = 0; t < T; ++t) acc[t] = 0.0f;
 
-    float acc[G][T];
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-        for (int t = 0; t < T; ++t) acc[g][t] = 0.0f;
-
-    for (int b0 = lane; b0 < nb; b0 += 32 * U) {
-        int4 w0[U][G], w1[U][G];
-        float dw[U][G];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int b = b0 + 32 * u;
-            if (b < nb) {
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const int8_t* p = wrow[g] + (size_t)b * 32;
-                    w0[u][g] = ld_stream_v4(p);
-                    w1[u][g] = ld_stream_v4(p + 16);
-                    dw[u][g] = __half2float(__ushort_as_half(ld_stream_u16(drow[g] + b)));
-                }
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int b = b0 + 32 * u;
-            if (b < nb) {
-#pragma unroll
-                for (int t = 0; t < T; ++t) {
-                    const int4* pa = reinterpret_cast<const int4*>(aq + (size_t)t * K + (size_t)b * 32);
-                    const int4 a0 = __ldg(pa);
-                    const int4 a1 = __ldg(pa + 1);
-                    const float da = __ldg(ad + (size_t)t * nb + b);
-#pragma unroll
-                    for (int g = 0; g < G; ++g) {
-                        const int s = block_dot(w0[u][g], w1[u][g], a0, a1);
-                        acc[g][t] = __fmaf_rn(__fmul_rn(dw[u][g], da), (float)s, acc[g][t]);
-                    }
-                }
-            }
-        }
-    }
-
-    // Butterfly over the 32 lane partials, then lane (g*T + t) stores y[t][n0+g].
-    float mine = 0.0f;
-#pragma unroll
-    for (int g = 0; g < G; ++g)
+    auto compute = [&](const uint32_t (&wv)[8], float dw, int j) {
+        const int b = c + 32 * j;
 #pragma unroll
         for (int t = 0; t < T; ++t) {
-            const float v = warp_sum_butterfly(acc[g][t]);
-            if (lane == g * T + t) mine = v;
+            uint32_t av[8];
+            ld_cached_v8(aq + (size_t)t * K + (size_t)b * 32, av);
+            const float da = __ldg(ad + (size_t)t * nb + b);
+            const int s = block_dot8(wv, av);
+            acc[t] = __fmaf_rn(__fmul_rn(dw, da), (float)s, acc[t]);
         }
-    if (lane < G * T) {
-        const int g = lane / T, t = lane - (lane / T) * T;
-        const int n = n0 + g;
+    };
+    uint32_t wa[8], wb[8];
+    float sa = 0.0f, sb = 0.0f;
+    if (nj > 0) {
+        ld_stream_v8(wp, wa);
+        sa = __half2float(__ushort_as_half(ld_stream_u16(dp)));
+    }
+    for (int j = 0; j < nj; j += 2) {
+        if (j + 1 < nj) {
+            ld_stream_v8(wp + (size_t)(j + 1) * 1024, wb);
+            sb = __half2float(__ushort_as_half(ld_stream_u16(dp + (j + 1) * 32)));
+        }
+        compute(wa, sa, j);
+        if (j + 2 < nj) {
+            ld_stream_v8(wp + (size_t)(j + 2) * 1024, wa);
+            sa = __half2float(__ushort_as_half(ld_stream_u16(dp + (j + 2) * 32)));
+        }
+        if (j + 1 < nj) compute(wb, sb, j + 1);
+    }
+
+#pragma unroll
+    for (int t = 0; t < T; ++t) part[r][t][c] = acc[t];
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < RW * T; idx += blockDim.x) {
+        const int rr = idx / T, t = idx - (idx / T) * T;
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = part[rr][t][i];
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1)
+#pragma unroll
+            for (int i = 0; i < off; ++i) v[i] = __fadd_rn(v[i], v[i + off]);
+        const int n = row0 + rr;
         if (n < N) {
-            float out = mine;
-            if (resid) out = __fadd_rn(resid[(size_t)t * ldr + n], mine);
+            float out = v[0];
+            if (resid) out = __fadd_rn(resid[(size_t)t * ldr + n], out);
             y[(size_t)t * ldy + n] = out;
         }
     }
 }
 
-template <int T, int G, int U>
+template <int T, int KL, bool PF>
 static cudaError_t launch_t(const int8_t* wq, const __half* wd, int N, int K, const int8_t* aq,
                             const float* ad, float* y, int64_t ldy, const float* resid, int64_t ldr,
                             cudaStream_t s)
 {
-    const int warps = (N + G - 1) / G;
-    const int blocks = (warps + 7) / 8;
-    q8_matvec_kernel<T, G, U><<<blocks, 256, 0, s>>>(wq, wd, N, K, aq, ad, y, ldy, resid, ldr);
+    constexpr int RW = 32 / KL;
+    q8_matvec_kernel<T, KL, PF><<<(N + RW - 1) / RW, 32 * (32 / KL), 0, s>>>(wq, wd, N, K, aq, ad, y, ldy, resid,
+                                                                              ldr);
     count_launches(1);
     return cudaGetLastError();
 }
@@ -120,27 +118,27 @@ cudaError_t launch_matvec(const int8_t* wq, const __half* wd, int N, int K, cons
                           const float* ad, int T, float* y, int64_t ldy, const float* resid,
                           int64_t ldr, cudaStream_t s)
 {
-    // G (rows per warp) and U (blocks in flight per lane) only shape the
-    // memory pipeline; neither changes any row's arithmetic.
+    // KL (lanes per row) and the L2 prefetch only shape the memory pipeline;
+    // neither changes any row's arithmetic.
     switch (T) {
-#define LUCE_MV(TT, GG, UU) \
-    case TT: return launch_t<TT, GG, UU>(wq, wd, N, K, aq, ad, y, ldy, resid, ldr, s);
-        LUCE_MV(1, 2, 4)
-        LUCE_MV(2, 2, 4)
-        LUCE_MV(3, 2, 4)
-        LUCE_MV(4, 2, 4)
-        LUCE_MV(5, 2, 2)
-        LUCE_MV(6, 2, 2)
-        LUCE_MV(7, 2, 2)
-        LUCE_MV(8, 2, 2)
-        LUCE_MV(9, 1, 2)
-        LUCE_MV(10, 1, 2)
-        LUCE_MV(11, 1, 2)
-        LUCE_MV(12, 1, 2)
-        LUCE_MV(13, 1, 2)
-        LUCE_MV(14, 1, 2)
-        LUCE_MV(15, 1, 2)
-        LUCE_MV(16, 1, 2)
+#define LUCE_MV(TT, KK, PP) \
+    case TT: return launch_t<TT, KK, PP>(wq, wd, N, K, aq, ad, y, ldy, resid, ldr, s);
+        LUCE_MV(1, 8, false)
+        LUCE_MV(2, 8, false)
+        LUCE_MV(3, 8, false)
+        LUCE_MV(4, 8, false)
+        LUCE_MV(5, 4, true)
+        LUCE_MV(6, 4, true)
+        LUCE_MV(7, 4, true)
+        LUCE_MV(8, 4, true)
+        LUCE_MV(9, 4, true)
+        LUCE_MV(10, 4, true)
+        LUCE_MV(11, 4, true)
+        LUCE_MV(12, 4, true)
+        LUCE_MV(13, 4, true)
+        LUCE_MV(14, 4, true)
+        LUCE_MV(15, 4, true)
+        LUCE_MV(16, 4, true)
 #undef LUCE_MV
         default: return cudaErrorInvalidValue;
     }
@@ -159,9 +157,10 @@ __global__ void q8_block_dots_kernel(const int8_t* __restrict__ wq, int N, int K
         const int64_t tn = i / nb;
         const int n = (int)(tn % N);
         const int t = (int)(tn / N);
-        const int4* pw = reinterpret_cast<const int4*>(wq + (size_t)n * K + (size_t)b * 32);
-        const int4* pa = reinterpret_cast<const int4*>(aq + (size_t)t * K + (size_t)b * 32);
-        out[i] = block_dot(pw[0], pw[1], pa[0], pa[1]);
+        uint32_t wv[8], av[8];
+        ld_stream_v8(wq + (size_t)n * K + (size_t)b * 32, wv);
+        ld_cached_v8(aq + (size_t)t * K + (size_t)b * 32, av);
+        out[i] = block_dot8(wv, av);
     }
 }
 

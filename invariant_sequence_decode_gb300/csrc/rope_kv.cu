@@ -6,51 +6,32 @@
 // section 2: KV append runs per sequence with the single-token helpers.
 //
 // Pairing: dims (i, i + 64) of a 128-dim head rotate by pos * theta^(-i/64).
-// cos/sin come from a double-precision evaluation rounded to fp32 (so the
-// angle carries no fp32 error even at position 32767); the rotation is fp32.
+// theta^(-i/64) is evaluated in double on the host; the angle is formed and
+// reduced in double on the device and only the reduced angle goes through
+// fp32 sincosf (see rope_cs), so even position 32767 carries no fp32 angle
+// error.  The rotation is fp32 with explicit rounding.  One CTA of 64 threads
+// per (row, head): thread i owns pair i.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace luce {
 
-// Standalone RoPE: one CTA per row; 64 threads evaluate the row's cos/sin.
-__global__ void __launch_bounds__(256)
-rope_posvec_kernel(float* __restrict__ x, int n_heads, int64_t ldx, const int32_t* __restrict__ pos,
-                   double theta)
+__global__ void __launch_bounds__(64)
+rope_posvec_kernel(float* __restrict__ x, int64_t ldx, const int32_t* __restrict__ pos, RopeFreq f)
 {
-    __shared__ float2 cs[kHeadDim / 2];
-    const int t = blockIdx.x;
-    if (threadIdx.x < kHeadDim / 2) cs[threadIdx.x] = rope_cs(pos[t], threadIdx.x, kHeadDim, theta);
-    __syncthreads();
-    float* xr = x + (size_t)t * ldx;
-    for (int idx = threadIdx.x; idx < n_heads * (kHeadDim / 2); idx += blockDim.x) {
-        const int h = idx >> 6, i = idx & 63;
-        float* p = xr + h * kHeadDim + i;
-        float x0 = p[0], x1 = p[kHeadDim / 2];
-        rope_rotate(x0, x1, cs[i].x, cs[i].y);
-        p[0] = x0;
-        p[kHeadDim / 2] = x1;
-    }
+    const int t = blockIdx.x, h = blockIdx.y, i = threadIdx.x;
+    const float2 cs = rope_cs(pos[t], f.inv[i]);
+    float* p = x + (size_t)t * ldx + (size_t)h * kHeadDim + i;
+    float x0 = p[0], x1 = p[kHeadDim / 2];
+    rope_rotate(x0, x1, cs.x, cs.y);
+    p[0] = x0;
+    p[kHeadDim / 2] = x1;
 }
 
 cudaError_t launch_rope_posvec(float* x, int T, int n_heads, int64_t ldx, const int32_t* pos,
-                               double theta, cudaStream_t s)
+                               const RopeFreq& f, cudaStream_t s)
 {
-    rope_posvec_kernel<<<T, 256, 0, s>>>(x, n_heads, ldx, pos, theta);
-    count_launches(1);
-    return cudaGetLastError();
-}
-
-// Per-step cos/sin table [T][64] (float2), positions by value.
-__global__ void rope_table_kernel(RowPos pos, double theta, float2* __restrict__ cs)
-{
-    const int t = blockIdx.x, i = threadIdx.x;
-    cs[t * (kHeadDim / 2) + i] = rope_cs(pos.pos[t], i, kHeadDim, theta);
-}
-
-cudaError_t launch_rope_table(const RowPos& pos, double theta, float2* cs, cudaStream_t s)
-{
-    rope_table_kernel<<<pos.n_rows, kHeadDim / 2, 0, s>>>(pos, theta, cs);
+    rope_posvec_kernel<<<dim3(T, n_heads), 64, 0, s>>>(x, ldx, pos, f);
     count_launches(1);
     return cudaGetLastError();
 }
@@ -76,46 +57,41 @@ cudaError_t launch_kv_append(const float* k, const float* v, int64_t ld, int Hkv
     return cudaGetLastError();
 }
 
-// Decode-step glue, one CTA per row: rotate the row's q heads into q_rot,
-// rotate its k heads and append k and v to the row's cache position.  Uses
-// the same rotation and conversion as the standalone kernels above.
-__global__ void __launch_bounds__(256)
-rope_kv_kernel(const float* __restrict__ qkv, int Hq, int Hkv, const float2* __restrict__ cs_tab,
+// Decode-step glue, one CTA per (row, head of the fused q|k|v projection):
+// q heads are rotated into q_rot, k heads rotated and appended to the row's
+// cache position as binary16, v heads appended.  Same rotation and
+// conversion as the standalone kernels above.
+__global__ void __launch_bounds__(64)
+rope_kv_kernel(const float* __restrict__ qkv, int Hq, int Hkv, RowPos pos, RopeFreq f,
                float* __restrict__ q_rot, KvRows rows)
 {
-    __shared__ float2 cs[kHeadDim / 2];
-    const int t = blockIdx.x;
-    const int ld = (Hq + 2 * Hkv) * kHeadDim;
-    if (threadIdx.x < kHeadDim / 2) cs[threadIdx.x] = cs_tab[t * (kHeadDim / 2) + threadIdx.x];
-    __syncthreads();
-    const float* row = qkv + (size_t)t * ld;
-    // q and k heads: (Hq + Hkv) heads x 64 pairs
-    for (int idx = threadIdx.x; idx < (Hq + Hkv) * (kHeadDim / 2); idx += blockDim.x) {
-        const int h = idx >> 6, i = idx & 63;
-        float x0 = row[h * kHeadDim + i], x1 = row[h * kHeadDim + i + 64];
-        rope_rotate(x0, x1, cs[i].x, cs[i].y);
+    const int t = blockIdx.x, h = blockIdx.y, i = threadIdx.x;
+    const float* src = qkv + (size_t)t * (Hq + 2 * Hkv) * kHeadDim + (size_t)h * kHeadDim;
+    const KvRow r = rows.row[t];
+    if (h < Hq + Hkv) {
+        const float2 cs = rope_cs(pos.pos[t], f.inv[i]);
+        float x0 = src[i], x1 = src[i + 64];
+        rope_rotate(x0, x1, cs.x, cs.y);
         if (h < Hq) {
-            q_rot[(size_t)t * Hq * kHeadDim + h * kHeadDim + i] = x0;
-            q_rot[(size_t)t * Hq * kHeadDim + h * kHeadDim + i + 64] = x1;
+            float* dst = q_rot + (size_t)t * Hq * kHeadDim + (size_t)h * kHeadDim;
+            dst[i] = x0;
+            dst[i + 64] = x1;
         } else {
-            const KvRow r = rows.row[t];
             __half* dst = r.k + (h - Hq) * r.head_stride;
             dst[i] = __float2half_rn(x0);
             dst[i + 64] = __float2half_rn(x1);
         }
-    }
-    const KvRow r = rows.row[t];
-    const float* vrow = row + (Hq + Hkv) * kHeadDim;
-    for (int idx = threadIdx.x; idx < Hkv * kHeadDim; idx += blockDim.x) {
-        const int g = idx >> 7, dd = idx & 127;
-        r.v[g * r.head_stride + dd] = __float2half_rn(vrow[idx]);
+    } else {
+        __half* dst = r.v + (h - Hq - Hkv) * r.head_stride;
+        dst[i] = __float2half_rn(src[i]);
+        dst[i + 64] = __float2half_rn(src[i + 64]);
     }
 }
 
-cudaError_t launch_rope_kv(const float* qkv, int T, int Hq, int Hkv, const float2* cs, float* q_rot,
-                           const KvRows& rows, cudaStream_t s)
+cudaError_t launch_rope_kv(const float* qkv, int T, int Hq, int Hkv, const RowPos& pos, const RopeFreq& f,
+                           float* q_rot, const KvRows& rows, cudaStream_t s)
 {
-    rope_kv_kernel<<<T, 256, 0, s>>>(qkv, Hq, Hkv, cs, q_rot, rows);
+    rope_kv_kernel<<<dim3(T, Hq + 2 * Hkv), 64, 0, s>>>(qkv, Hq, Hkv, pos, f, q_rot, rows);
     count_launches(1);
     return cudaGetLastError();
 }

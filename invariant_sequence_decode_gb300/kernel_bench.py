@@ -1,0 +1,131 @@
+"""Per-kernel microbenchmark (CUDA events, L2 flushed between launches).
+
+  python -m invariant_sequence_decode_gb300.kernel_bench matvec --N 34816 --K 5120 --T 4
+  python -m invariant_sequence_decode_gb300.kernel_bench attn --lens 2051,2051,2051,2051 --hq 40 --hkv 8
+  python -m invariant_sequence_decode_gb300.kernel_bench step --nseq 4
+
+Prints one JSON line per case with the mean launch time and the algorithmic
+GB/s (weights N*K*34/32 + activations + outputs for the matvec; K/V bytes
+for attention).  `--reps` launches are timed; use a small `--reps` under a
+profiler.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import statistics
+
+import numpy as np
+
+
+class L2Flush:
+    """Write, then read, a 256 MiB buffer: the L2 ends up holding clean lines
+    of an unrelated buffer, so the next launch pays neither hits nor dirty
+    write-backs."""
+
+    def __init__(self, torch):
+        self.torch = torch
+        self.buf = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        self.sink = torch.empty(1, dtype=torch.int64, device="cuda")
+
+    def __call__(self):
+        self.buf.fill_(1)
+        self.sink.copy_(self.buf.view(self.torch.int64).sum().view(1))
+
+
+def time_launches(torch, fn, flush, reps: int):
+    st = torch.cuda.current_stream()
+    out = []
+    for _ in range(reps):
+        if flush:
+            flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        fn()
+        b.record(st)
+        out.append((a, b))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in out]
+
+
+def main(argv=None):
+    import torch
+    import invariant_sequence_decode_gb300 as luce
+    from invariant_sequence_decode_gb300 import build, workloads as wl
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("kernel", choices=["matvec", "attn", "step"])
+    ap.add_argument("--N", type=int, default=34816)
+    ap.add_argument("--K", type=int, default=5120)
+    ap.add_argument("--T", default="4")
+    ap.add_argument("--lens", default="2051,2051,2051,2051")
+    ap.add_argument("--hq", type=int, default=40)
+    ap.add_argument("--hkv", type=int, default=8)
+    ap.add_argument("--nseq", type=int, default=4)
+    ap.add_argument("--reps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--no-flush", action="store_true")
+    a = ap.parse_args(argv)
+    build.build()
+    luce.load_library()
+    flush = None if a.no_flush else L2Flush(torch)
+    cu = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+    if a.kernel == "matvec":
+        wq, wd = wl.q8_weights(0, wl.tid(wl.W_MAT, 1), a.N, a.K)
+        W, D = cu(wq), cu(wd)
+        for T in [int(t) for t in a.T.split(",")]:
+            aq, ad = luce.luce_q8_quantize_act(cu(wl.acts(0, T, a.K)))
+            y = torch.empty((T, a.N), dtype=torch.float32, device="cuda")
+            fn = lambda: luce.luce_q8_matvec_batch(W, D, aq, ad, y)
+            for _ in range(a.warmup):
+                fn()
+            ms = time_launches(torch, fn, flush, a.reps)
+            b = a.N * a.K * 34 // 32 + T * a.K + T * (a.K // 32) * 4 + T * a.N * 4
+            m = statistics.mean(ms)
+            print(json.dumps({"kernel": "q8_matvec", "N": a.N, "K": a.K, "T": T, "us_mean": round(m * 1e3, 2),
+                              "us_min": round(min(ms) * 1e3, 2), "gbps": round(b / m / 1e6, 1)}))
+    elif a.kernel == "attn":
+        lens = [int(x) for x in a.lens.split(",")]
+        d = wl.Dims(0, a.hq, a.hkv, 128, 0)
+        views = []
+        for s, L in enumerate(lens):
+            k, v = wl.cache_host(0, s, 0, d, L, L)
+            views.append(luce.SeqView(cu(k), cu(v), L, 1, s))
+        q = cu(wl.qvec(0, len(lens), a.hq))
+        out = torch.empty_like(q)
+        ws = torch.empty(luce.luce_decode_attn_workspace_size(len(lens), a.hq, 128, max(lens)), dtype=torch.uint8,
+                         device="cuda")
+        fn = lambda: luce.luce_decode_attn_multiseq(q, views, a.hkv, 0.08838834764831845, out, ws)
+        for _ in range(a.warmup):
+            fn()
+        ms = time_launches(torch, fn, flush, a.reps)
+        b = sum(lens) * a.hkv * 128 * 2 * 2
+        m = statistics.mean(ms)
+        print(json.dumps({"kernel": "decode_attn", "lens": lens, "hq": a.hq, "hkv": a.hkv,
+                          "us_mean": round(m * 1e3, 2), "gbps": round(b / m / 1e6, 1)}))
+    else:
+        d = wl.LAYER27B
+        fields = ["attn_norm", "wqkv_q", "wqkv_d", "wo_q", "wo_d", "ffn_norm", "wgu_q", "wgu_d", "wdown_q",
+                  "wdown_d"]
+        Lh = wl.layer_host(1, 0, d)
+        model = luce.Model([luce.LayerTensors(*[cu(getattr(Lh, f)) for f in fields])], d.hidden, d.n_q_heads,
+                           d.n_kv_heads, d.ffn)
+        slots = []
+        for s in range(a.nseq):
+            k, v = wl.cache_host(1, s, 0, d, 2051, 2050)
+            slots.append(luce.Slot(cu(k[None]), cu(v[None]), 2050))
+        x = cu(wl.acts(1, a.nseq, d.hidden))
+        ws = model.workspace(a.nseq, 2051)
+        fn = lambda: luce.luce_decode_step(model, slots, [1] * a.nseq, x, ws)
+        for _ in range(a.warmup):
+            fn()
+        ms = time_launches(torch, fn, flush, a.reps)
+        m = statistics.mean(ms)
+        print(json.dumps({"kernel": "decode_step", "nseq": a.nseq, "us_mean": round(m * 1e3, 2),
+                          "tok_s": round(a.nseq / (m / 1e3), 1)}))
+
+
+if __name__ == "__main__":
+    main()
