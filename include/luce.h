@@ -178,6 +178,37 @@ int luce_decode_attn_multiseq(const float* q, const luce_seqview* views, int n_s
  * counts are at most max_len. */
 size_t luce_decode_attn_workspace_size(int n_rows, int Hq, int D, int max_len);
 
+/*
+ * luce_decode_attn_multiseq without a caller workspace.  The pages have no
+ * counterpart: this entry point exists for callers that cannot allocate
+ * device memory themselves (a serving loop that must not call cudaMalloc
+ * once it is running, or a host runtime whose device allocator is not
+ * reachable from C).  Arguments, results and numerics are those of
+ * luce_decode_attn_multiseq; only the scratch differs.
+ *
+ * The scratch is one fixed array of luce_decode_attn_noalloc_max_bytes()
+ * bytes (16 MiB) in the library's device memory; every GPU that loads the
+ * library holds it until the process exits.  The call needs
+ * roundup256(64 * Hq) + (sum over rows of ceil(keys / 256)) * Hq * 528 bytes
+ * of it and returns LUCE_ENOSPACE, launching nothing, when that exceeds the
+ * array (at Hq = 40: 4 rows of up to 32,768 keys, or 16 rows of up to about
+ * 6,000 keys, fit).  It allocates nothing:
+ * no cudaMalloc, cudaFree or allocating library routine.  It clears the
+ * part of the array that must start at zero (with cudaMemsetAsync on
+ * `stream`) on every call.
+ *
+ * The first call on each device (the calling thread's current device) looks
+ * up the array's device address with cudaGetSymbolAddress; make that first
+ * call before any stream capture.  All calls share the one array and it
+ * keeps the last call's contents, so calls that can overlap on the GPU
+ * (different streams without ordering between them) race: order them.
+ */
+int luce_decode_attn_multiseq_noalloc(const float* q, const luce_seqview* views, int n_seq,
+                                      int Hq, int Hkv, int D, float scale, float* out, void* stream);
+
+/* Size in bytes of the fixed scratch array of luce_decode_attn_multiseq_noalloc. */
+size_t luce_decode_attn_noalloc_max_bytes(void);
+
 /* ---------------------------------------------------------------- decode step */
 
 /* One pre-norm decoder layer, all projections q8_0 (device pointers). */

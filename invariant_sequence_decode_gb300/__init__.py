@@ -67,7 +67,8 @@ class StepLayoutC(ctypes.Structure):
 
 EXPORTS = ("luce_last_error", "luce_version", "luce_launch_count", "luce_q8_quantize_act", "luce_q8_matvec_batch",
            "luce_q8_block_dots", "luce_rope_posvec", "luce_kv_append", "luce_decode_attn_multiseq",
-           "luce_decode_attn_workspace_size", "luce_decode_step_layout", "luce_decode_step")
+           "luce_decode_attn_workspace_size", "luce_decode_step_layout", "luce_decode_step",
+           "luce_decode_attn_multiseq_noalloc", "luce_decode_attn_noalloc_max_bytes")
 
 _lib = None
 
@@ -98,8 +99,12 @@ def load_library(path: str = LIB_PATH):
     lib.luce_decode_step_layout.argtypes = [ctypes.POINTER(ModelC), i32, i32, ctypes.POINTER(StepLayoutC)]
     lib.luce_decode_step.argtypes = [ctypes.POINTER(ModelC), ctypes.POINTER(SlotC), ctypes.POINTER(ctypes.c_int32),
                                      i32, vp, vp, vp, vp, sz, vp]
+    lib.luce_decode_attn_multiseq_noalloc.argtypes = [vp, ctypes.POINTER(SeqViewC), i32, i32, i32, i32, f32, vp, vp]
+    lib.luce_decode_attn_noalloc_max_bytes.argtypes = []
+    lib.luce_decode_attn_noalloc_max_bytes.restype = sz
     for name in EXPORTS:
-        if name not in ("luce_last_error", "luce_version", "luce_launch_count", "luce_decode_attn_workspace_size"):
+        if name not in ("luce_last_error", "luce_version", "luce_launch_count", "luce_decode_attn_workspace_size",
+                        "luce_decode_attn_noalloc_max_bytes"):
             getattr(lib, name).restype = i32
     _lib = lib
     return lib
@@ -232,6 +237,20 @@ def luce_decode_attn_multiseq(q, views: Sequence[SeqView], n_kv_heads: int, scal
     _check(load_library().luce_decode_attn_multiseq(q.data_ptr(), _views(views), len(views), Hq, n_kv_heads, D,
                                                     float(scale), out.data_ptr(), ws.data_ptr(), ws.numel(),
                                                     _stream(stream)))
+    return out
+
+
+def luce_decode_attn_multiseq_noalloc(q, views: Sequence[SeqView], n_kv_heads: int, scale: float, out=None,
+                                      stream=None):
+    """luce_decode_attn_multiseq using the library's fixed scratch array instead
+    of a workspace, for callers that cannot allocate device memory.  Calls that
+    can overlap on the GPU share that array and must be ordered."""
+    import torch
+    _need(q, torch.float32, "q")
+    T, Hq, D = q.shape
+    out = torch.empty_like(q) if out is None else out
+    _check(load_library().luce_decode_attn_multiseq_noalloc(q.data_ptr(), _views(views), len(views), Hq, n_kv_heads,
+                                                            D, float(scale), out.data_ptr(), _stream(stream)))
     return out
 
 

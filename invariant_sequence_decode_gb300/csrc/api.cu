@@ -9,6 +9,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <mutex>
 #include <string>
 
 #include "../../include/luce.h"
@@ -240,6 +241,74 @@ int luce_decode_attn_multiseq(const float* q, const luce_seqview* views, int n_s
     return cuda_status(launch_attention(q, (int64_t)Hq * D, rows, Hq, Hkv, scale, (float*)((char*)ws + tb), (int*)ws,
                                         out, (int64_t)Hq * D, nullptr, nullptr, st),
                        "decode_attn");
+}
+
+// ------------------------------------------------------------ attention, no allocation
+//
+// For callers that cannot allocate device memory themselves (a real-time
+// serving loop that must not call cudaMalloc after start-up, an embedding
+// runtime whose allocator is not reachable from C): the split-K scratch lives
+// in this fixed, file-scope device array instead of a caller workspace.  The
+// host-side name of the array is only a stand-in; its device address is
+// looked up once per device with cudaGetSymbolAddress.
+
+static constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;
+static constexpr int kNoAllocMaxDevices = 64;
+static __device__ __align__(256) unsigned char g_attn_noalloc_scratch[kNoAllocScratchBytes];
+static std::mutex g_noalloc_mu;
+static void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+static int noalloc_scratch(void** out)
+{
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e, "decode_attn_noalloc: cudaGetDevice");
+    REQUIRE(dev >= 0 && dev < kNoAllocMaxDevices, LUCE_EUNSUPPORTED, "decode_attn_noalloc: device %d >= %d", dev,
+            kNoAllocMaxDevices);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_attn_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_status(e, "decode_attn_noalloc: cudaGetSymbolAddress");
+        REQUIRE(p != nullptr, LUCE_ECUDA, "decode_attn_noalloc: null scratch address");
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return LUCE_OK;
+}
+
+size_t luce_decode_attn_noalloc_max_bytes(void) { return kNoAllocScratchBytes; }
+
+int luce_decode_attn_multiseq_noalloc(const float* q, const luce_seqview* views, int n_seq, int Hq, int Hkv, int D,
+                                      float scale, float* out, void* stream)
+{
+    const char* who = "decode_attn_noalloc";
+    REQUIRE(q && out, LUCE_EINVAL, "%s: null q/out", who);
+    REQUIRE(Hkv >= 1 && Hq >= Hkv && Hq % Hkv == 0, LUCE_EINVAL, "%s: Hq=%d must be a multiple of Hkv=%d", who, Hq,
+            Hkv);
+    REQUIRE(Hq / Hkv <= 8, LUCE_EUNSUPPORTED, "%s: group size %d > 8", who, Hq / Hkv);
+    REQUIRE(isfinite(scale), LUCE_EINVAL, "%s: scale must be finite", who);
+    REQUIRE(aligned(q, 16) && aligned(out, 4), LUCE_EINVAL, "%s: misaligned q/out", who);
+    int T = 0;
+    int rc = check_views(views, n_seq, Hkv, D, &T, who);
+    if (rc) return rc;
+    AttnRows rows{};
+    build_attn_rows(views, n_seq, rows, T);
+    const size_t tb = attn_ticket_bytes(Hq);
+    const size_t need = tb + attn_part_floats(rows.total_chunks, Hq) * sizeof(float);
+    REQUIRE(need <= kNoAllocScratchBytes, LUCE_ENOSPACE,
+            "%s: needs %zu bytes of scratch, more than the fixed %zu-byte array (fewer rows, shorter contexts or "
+            "fewer heads fit)",
+            who, need, kNoAllocScratchBytes);
+    void* scratch = nullptr;
+    rc = noalloc_scratch(&scratch);
+    if (rc) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaMemsetAsync(scratch, 0, (size_t)T * Hkv * sizeof(int), st);
+    if (e != cudaSuccess) return cuda_status(e, who);
+    return cuda_status(launch_attention(q, (int64_t)Hq * D, rows, Hq, Hkv, scale, (float*)((char*)scratch + tb),
+                                        (int*)scratch, out, (int64_t)Hq * D, nullptr, nullptr, st),
+                       who);
 }
 
 // ------------------------------------------------------------ decode step
