@@ -56,7 +56,7 @@ typedef enum luce_status {
 #define LUCE_MAX_ROWS_PER_SEQ 4  /* rows per slot (1 decode + up to 3 drafts) */
 #define LUCE_MAX_ROWS 16         /* 8/12/16-row verify capacities [qfuse, item 1] */
 #define LUCE_HEAD_DIM 128
-#define LUCE_ATTN_CHUNK 256      /* keys per split-K chunk of decode attention */
+#define LUCE_MAX_KEYS 261888     /* keys one attention row may see (1023 chunks of 256) */
 
 /* Message of the calling thread's last non-OK status ("" if none). */
 const char* luce_last_error(void);
@@ -157,10 +157,11 @@ int luce_kv_append(const float* k, const float* v, int64_t ldkv, int Hkv, int D,
  * token per sequence against its own cache; here up to 4 causal rows per
  * sequence].  For row r of view s and query head h (KV head g = h / (Hq/Hkv)):
  *   out[r][h] = sum_j softmax_j(scale * q[r][h] . K[g][j]) V[g][j]
- * over the row's keys.  The keys are split into fixed chunks of
- * LUCE_ATTN_CHUNK (a function of the row's own key count only); each chunk
- * yields (max, sum, unnormalised output) and the chunks are merged in order
- * by the exact log-sum-exp rule.  No output depends on the other rows.
+ * over the row's keys.  The keys are split into chunks of 64 keys (rows with
+ * at most 4,096 keys), 128 (at most 16,384) or 256 (more): a function of the
+ * row's own key count only; each chunk yields (max, sum, unnormalised
+ * output) and the chunks are merged in order by the exact log-sum-exp rule.
+ * No output depends on the other rows.
  *   q   (device) fp32 [T][Hq][D] with T = max(row0 + n_q)
  *   out (device) fp32 [T][Hq][D]
  *   ws  (device) scratch of at least luce_decode_attn_workspace_size(...)
@@ -168,7 +169,7 @@ int luce_kv_append(const float* k, const float* v, int64_t ldkv, int Hkv, int D,
  * The chunk merge is done by whichever CTA of a (row, KV head) finishes last
  * (an atomic ticket, no waiting); the merge order is the chunk order.
  * D == 128, Hq % Hkv == 0, Hq / Hkv <= 8, 1 <= n_seq <= LUCE_MAX_SEQ,
- * 1 <= len - n_q + 1, len <= cap.
+ * 1 <= len - n_q + 1, len <= cap, len <= LUCE_MAX_KEYS.
  */
 int luce_decode_attn_multiseq(const float* q, const luce_seqview* views, int n_seq,
                               int Hq, int Hkv, int D, float scale, float* out,
@@ -189,10 +190,10 @@ size_t luce_decode_attn_workspace_size(int n_rows, int Hq, int D, int max_len);
  * The scratch is one fixed array of luce_decode_attn_noalloc_max_bytes()
  * bytes (16 MiB) in the library's device memory; every GPU that loads the
  * library holds it until the process exits.  The call needs
- * roundup256(64 * Hq) + (sum over rows of ceil(keys / 256)) * Hq * 528 bytes
- * of it and returns LUCE_ENOSPACE, launching nothing, when that exceeds the
- * array (at Hq = 40: 4 rows of up to 32,768 keys, or 16 rows of up to about
- * 6,000 keys, fit).  It allocates nothing:
+ * roundup256(64 * Hq) + (sum over rows of its chunk count) * Hq * 528 bytes
+ * of it (chunks as in luce_decode_attn_multiseq) and returns LUCE_ENOSPACE,
+ * launching nothing, when that exceeds the array (at Hq = 40: 4 rows of up
+ * to 32,768 keys, or 16 rows of up to 2,051 keys, fit).  It allocates nothing:
  * no cudaMalloc, cudaFree or allocating library routine.  It clears the
  * part of the array that must start at zero (with cudaMemsetAsync on
  * `stream`) on every call.

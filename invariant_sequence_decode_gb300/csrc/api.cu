@@ -64,7 +64,22 @@ bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-int chunks_of(int len) { return (len + kAttnChunk - 1) / kAttnChunk; }
+int chunks_of(int len)
+{
+    const int ch = attn_chunk_keys(len);
+    return (len + ch - 1) / ch;
+}
+
+// Largest chunk count of any row with at most max_len keys.
+int max_chunks_upto(int max_len)
+{
+    int m = chunks_of(std::min(max_len, 4096));
+    if (max_len > 4096) m = std::max(m, chunks_of(std::min(max_len, 16384)));
+    if (max_len > 16384) m = std::max(m, chunks_of(max_len));
+    return m;
+}
+
+constexpr int kMaxKeys = 256 * kAttnMaxChunksPerRow;
 
 }  // namespace
 
@@ -151,6 +166,7 @@ static int check_views(const luce_seqview* views, int n_seq, int Hkv, int D, int
                 s, v.n_q, LUCE_MAX_ROWS_PER_SEQ);
         REQUIRE(v.len >= v.n_q && v.len <= v.cap, LUCE_EINVAL, "%s: view %d len=%d outside [n_q, cap=%d]", who, s,
                 v.len, v.cap);
+        REQUIRE(v.len <= kMaxKeys, LUCE_EUNSUPPORTED, "%s: view %d has %d keys (at most %d)", who, s, v.len, kMaxKeys);
         REQUIRE(v.tok_stride >= D && v.tok_stride % 8 == 0 && v.head_stride % 8 == 0, LUCE_EINVAL,
                 "%s: view %d strides must be multiples of 8 with tok_stride >= D", who, s);
         REQUIRE(v.head_stride >= (int64_t)v.cap * v.tok_stride || Hkv == 1, LUCE_EINVAL,
@@ -195,7 +211,7 @@ static size_t attn_ticket_bytes(int Hq) { return align_up((size_t)LUCE_MAX_ROWS 
 size_t luce_decode_attn_workspace_size(int n_rows, int Hq, int D, int max_len)
 {
     if (n_rows < 1 || Hq < 1 || D != LUCE_HEAD_DIM || max_len < 1) return 0;
-    return attn_ticket_bytes(Hq) + attn_part_floats(n_rows * chunks_of(max_len), Hq) * sizeof(float);
+    return attn_ticket_bytes(Hq) + attn_part_floats(n_rows * max_chunks_upto(max_len), Hq) * sizeof(float);
 }
 
 static void build_attn_rows(const luce_seqview* views, int n_seq, AttnRows& rows, int T)
@@ -209,6 +225,7 @@ static void build_attn_rows(const luce_seqview* views, int n_seq, AttnRows& rows
             r.head_stride = views[s].head_stride;
             r.tok_stride = views[s].tok_stride;
             r.len = views[s].len - views[s].n_q + 1 + j;
+            r.chunk = attn_chunk_keys(r.len);
         }
     int c = 0;
     for (int r = 0; r < T; ++r) {
@@ -363,7 +380,7 @@ static void layout_of(const luce_model* m, int T, int max_ctx, luce_step_layout*
     L->xf_d = take(T * H / 32 * 4);
     // The split-K scratch comes last so that the offsets above do not depend
     // on the context bound.
-    L->part = take(attn_part_floats(T * chunks_of(std::max(max_ctx, 1)), (int)Hq) * 4);
+    L->part = take(attn_part_floats(T * max_chunks_upto(std::max(max_ctx, 1)), (int)Hq) * 4);
     L->total = o;
 }
 
@@ -403,6 +420,8 @@ int luce_decode_step(const luce_model* m, const luce_slot* slots, const int32_t*
                 "%s: slot %d cache null or not 16-byte aligned", who, s);
         REQUIRE(sl.len >= 0 && sl.cap >= 1 && (int64_t)sl.len + n <= sl.cap, LUCE_EINVAL,
                 "%s: slot %d len=%d + rows=%d exceeds cap=%d", who, s, sl.len, n, sl.cap);
+        REQUIRE(sl.len + n <= kMaxKeys, LUCE_EUNSUPPORTED, "%s: slot %d would hold %d keys (at most %d)", who, s,
+                sl.len + n, kMaxKeys);
         for (int p = 0; p < s; ++p)
             REQUIRE(slots[p].k != sl.k && slots[p].v != sl.v, LUCE_EINVAL, "%s: slots %d and %d share a cache", who,
                     p, s);
@@ -483,6 +502,7 @@ int luce_decode_step(const luce_model* m, const luce_slot* slots, const int32_t*
             ar.row[r].head_stride = head_stride;
             ar.row[r].tok_stride = D;
             ar.row[r].len = pos.pos[r] + 1;
+            ar.row[r].chunk = attn_chunk_keys(ar.row[r].len);
         }
         int c = 0;
         for (int r = 0; r < T; ++r) {

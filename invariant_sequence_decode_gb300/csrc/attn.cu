@@ -5,10 +5,14 @@
 // each attending to its own cache, per-sequence views passed by value (max 4);
 // section 2: one multi-sequence attention launch with no position limit.
 //
-// One CTA per (row, chunk of 256 keys, KV head g) serves all Hq/Hkv query
-// heads of g, so each K/V byte is read once per row:
-//   scores   thread j owns key j of the chunk: 16 x 16-byte loads of its K row,
-//            s_h = scale * (q_h . k_j) with fma over d = 0..127 ascending;
+// A row's keys are cut into chunks of CH keys, CH = attn_chunk_keys(row's key
+// count) (64, 128 or 256: small contexts get more, smaller chunks so the GPU
+// has enough independent work).  One CTA of 256 threads per (row, chunk, KV
+// head g) serves all Hq/Hkv query heads of g, so each K/V byte is read once:
+//   scores   TPK = 256/CH threads per key, thread part p covers dims
+//            [p*128/TPK, (p+1)*128/TPK): fma over its dims ascending, then the
+//            TPK partial dots are summed by an xor butterfly (1, then 2);
+//            s_h = scale * dot;
 //   softmax  warp h owns head h: m = max_j s_h, p_j = exp(s_h - m),
 //            l = sum p_j (lane-serial over j = lane + 32i, then butterfly);
 //   values   warp w owns keys w, w+8, ... and lane l dims 4l..4l+3:
@@ -17,10 +21,10 @@
 //   -> scratch (o_h[128], m_h, l_h) for the chunk.
 // The CTA that finishes last for its (row, g) (an atomic ticket; nobody
 // waits) merges the row's chunks in chunk order:
-//   M = max_c m_c, L = sum_c l_c e^(m_c - M), O = sum_c o_c e^(m_c - M),
-//   out = O / L,
+//   M = max_c m_c, w_c = e^(m_c - M), L = sum_c l_c w_c, O = sum_c o_c w_c,
+//   out = O / L  (the sums sequential over c),
 // and optionally quantizes out to q8_0 blocks (the Wo projection's input).
-// The chunking and every reduction order depend only on the row's own key
+// Every chunking and reduction order depends only on the row's own key
 // count, never on the other rows, on which CTA merges or on the grid.
 #include <math.h>
 
@@ -33,90 +37,79 @@ constexpr int kPartStride = 132;  // o[128], m, l, 2 pad floats per (chunk, head
 
 size_t attn_part_floats(int total_chunks, int Hq) { return (size_t)total_chunks * Hq * kPartStride; }
 
+int attn_chunk_keys(int len) { return len <= 4096 ? 64 : (len <= 16384 ? 128 : 256); }
+
 template <int GQ>
-__global__ void __launch_bounds__(256)
-attn_kernel(const float* __restrict__ q, int64_t ldq, AttnRows rows, int Hq, int Hkv, float scale,
-            float* __restrict__ part, int* __restrict__ tickets, float* __restrict__ out, int64_t ldo,
-            int8_t* __restrict__ out_q, float* __restrict__ out_d)
+struct AttnSmem {
+    float q[GQ][kHeadDim];
+    float p[GQ][kAttnChunk];
+    float red[8][GQ][kHeadDim];  // also the merge's scratch
+    int last;
+};
+
+// Scores, softmax statistics and p.V of one chunk of CH keys.
+template <int GQ, int CH>
+__device__ __forceinline__ void attn_chunk(AttnSmem<GQ>& sm, const __half* kbase, const __half* vbase,
+                                           int64_t tok_stride, int nvalid, float scale, float* pout)
 {
-    __shared__ __align__(16) float q_s[GQ][kHeadDim];
-    __shared__ float p_s[GQ][kAttnChunk];
-    __shared__ __align__(16) float red[8][GQ][kHeadDim];
-    __shared__ int last;
-
-    const int chunk = blockIdx.x, g = blockIdx.y;
+    constexpr int TPK = 256 / CH;
+    constexpr int DPT = kHeadDim / TPK;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-
-    int r = 0;
-#pragma unroll 1
-    for (int i = 1; i < rows.n_rows; ++i)
-        if (chunk >= rows.row[i].chunk0) r = i;
-    const AttnRow row = rows.row[r];
-    const int c = chunk - row.chunk0;
-    const int nch = (row.len + kAttnChunk - 1) / kAttnChunk;
-    const int key0 = c * kAttnChunk;
-    const int nvalid = min(kAttnChunk, row.len - key0);
-    const int h0 = g * GQ;
-    const __half* kbase = row.k + g * row.head_stride + (int64_t)key0 * row.tok_stride;
-    const __half* vbase = row.v + g * row.head_stride + (int64_t)key0 * row.tok_stride;
-    if (tid == 0) {
-        // the chunk's V rows are needed after the scores: stage them in L2 now
-        const uint32_t span = (uint32_t)(((int64_t)(nvalid - 1) * row.tok_stride + kHeadDim) * 2);
-        prefetch_l2(vbase, span);
-    }
-
-    for (int i = tid; i < GQ * kHeadDim; i += 256)
-        q_s[i / kHeadDim][i % kHeadDim] = q[(size_t)r * ldq + (size_t)(h0 + i / kHeadDim) * kHeadDim + i % kHeadDim];
-    __syncthreads();
 
     // ---- scores
     {
+        const int j = tid / TPK, part = tid % TPK;
         float dot[GQ];
 #pragma unroll
         for (int h = 0; h < GQ; ++h) dot[h] = 0.0f;
-        const int j = tid;
         if (j < nvalid) {
-            const int4* kp = reinterpret_cast<const int4*>(kbase + (int64_t)j * row.tok_stride);
-            int4 kv[16];
+            const int4* kp = reinterpret_cast<const int4*>(kbase + (int64_t)j * tok_stride + part * DPT);
+            int4 kv[DPT / 8];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) kv[i] = __ldg(kp + i);
+            for (int i = 0; i < DPT / 8; ++i) kv[i] = __ldg(kp + i);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
+            for (int i = 0; i < DPT / 8; ++i) {
                 const __half2* hp = reinterpret_cast<const __half2*>(&kv[i]);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float2 kf = __half22float2(hp[e]);
-                    const int d = i * 8 + e * 2;
+                    const int d = part * DPT + i * 8 + e * 2;
 #pragma unroll
                     for (int h = 0; h < GQ; ++h) {
-                        dot[h] = __fmaf_rn(q_s[h][d], kf.x, dot[h]);
-                        dot[h] = __fmaf_rn(q_s[h][d + 1], kf.y, dot[h]);
+                        dot[h] = __fmaf_rn(sm.q[h][d], kf.x, dot[h]);
+                        dot[h] = __fmaf_rn(sm.q[h][d + 1], kf.y, dot[h]);
                     }
                 }
             }
         }
 #pragma unroll
-        for (int h = 0; h < GQ; ++h) p_s[h][j] = (j < nvalid) ? __fmul_rn(dot[h], scale) : -INFINITY;
+        for (int h = 0; h < GQ; ++h) {
+#pragma unroll
+            for (int off = 1; off < TPK; off <<= 1) dot[h] = __fadd_rn(dot[h], __shfl_xor_sync(0xffffffffu, dot[h], off));
+        }
+        if (part == 0) {
+#pragma unroll
+            for (int h = 0; h < GQ; ++h) sm.p[h][j] = (j < nvalid) ? __fmul_rn(dot[h], scale) : -INFINITY;
+        }
     }
     __syncthreads();
 
     // ---- chunk softmax statistics, warp h per head
-    float* pout = part + ((size_t)chunk * Hq + h0) * kPartStride;
     for (int h = warp; h < GQ; h += 8) {
-        float sv[kAttnChunk / 32];
+        float sv[CH / 32];
         float m = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < kAttnChunk / 32; ++i) {
-            sv[i] = p_s[h][lane + 32 * i];
+        for (int i = 0; i < CH / 32; ++i) {
+            sv[i] = sm.p[h][lane + 32 * i];
             m = fmaxf(m, sv[i]);
         }
         m = warp_max(m);
         float l = 0.0f;
 #pragma unroll
-        for (int i = 0; i < kAttnChunk / 32; ++i) {
+        for (int i = 0; i < CH / 32; ++i) {
             const int j = lane + 32 * i;
             const float p = (j < nvalid) ? expf(__fsub_rn(sv[i], m)) : 0.0f;
-            p_s[h][j] = p;
+            sm.p[h][j] = p;
             l = __fadd_rn(l, p);
         }
         l = warp_sum_butterfly(l);
@@ -127,7 +120,7 @@ attn_kernel(const float* __restrict__ q, int64_t ldq, AttnRows rows, int Hq, int
     }
     __syncthreads();
 
-    // ---- p . V  (keys w, w+8, ...; loads issued 8 keys at a time)
+    // ---- p . V  (keys w, w+8, ...; all of this warp's loads issued first)
     {
         float o[GQ][4];
 #pragma unroll
@@ -135,22 +128,25 @@ attn_kernel(const float* __restrict__ q, int64_t ldq, AttnRows rows, int Hq, int
 #pragma unroll
             for (int e = 0; e < 4; ++e) o[h][e] = 0.0f;
         const __half* vl = vbase + lane * 4;
-        for (int j0 = warp; j0 < nvalid; j0 += 64) {
-            uint2 raw[8];
+        constexpr int KPW = CH / 8;  // keys per warp
+        constexpr int UB = KPW < 8 ? KPW : 8;
+#pragma unroll 1
+        for (int u0 = 0; u0 < KPW; u0 += UB) {
+            uint2 raw[UB];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int j = j0 + 8 * u;
-                if (j < nvalid) raw[u] = __ldg(reinterpret_cast<const uint2*>(vl + (int64_t)j * row.tok_stride));
+            for (int u = 0; u < UB; ++u) {
+                const int j = warp + 8 * (u0 + u);
+                if (j < nvalid) raw[u] = __ldg(reinterpret_cast<const uint2*>(vl + (int64_t)j * tok_stride));
             }
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int j = j0 + 8 * u;
+            for (int u = 0; u < UB; ++u) {
+                const int j = warp + 8 * (u0 + u);
                 if (j < nvalid) {
                     const float2 v01 = __half22float2(*reinterpret_cast<const __half2*>(&raw[u].x));
                     const float2 v23 = __half22float2(*reinterpret_cast<const __half2*>(&raw[u].y));
 #pragma unroll
                     for (int h = 0; h < GQ; ++h) {
-                        const float p = p_s[h][j];
+                        const float p = sm.p[h][j];
                         o[h][0] = __fmaf_rn(p, v01.x, o[h][0]);
                         o[h][1] = __fmaf_rn(p, v01.y, o[h][1]);
                         o[h][2] = __fmaf_rn(p, v23.x, o[h][2]);
@@ -161,39 +157,98 @@ attn_kernel(const float* __restrict__ q, int64_t ldq, AttnRows rows, int Hq, int
         }
 #pragma unroll
         for (int h = 0; h < GQ; ++h)
-            *reinterpret_cast<float4*>(&red[warp][h][lane * 4]) = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
+            *reinterpret_cast<float4*>(&sm.red[warp][h][lane * 4]) = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
     }
     __syncthreads();
     for (int i = tid; i < GQ * kHeadDim; i += 256) {
         const int h = i / kHeadDim, d = i % kHeadDim;
-        float s = red[0][h][d];
+        float s = sm.red[0][h][d];
 #pragma unroll
-        for (int w = 1; w < 8; ++w) s = __fadd_rn(s, red[w][h][d]);
+        for (int w = 1; w < 8; ++w) s = __fadd_rn(s, sm.red[w][h][d]);
         pout[(size_t)h * kPartStride + d] = s;
     }
+}
+
+template <int GQ>
+__global__ void __launch_bounds__(256)
+attn_kernel(const float* __restrict__ q, int64_t ldq, AttnRows rows, int Hq, int Hkv, float scale,
+            float* __restrict__ part, int* __restrict__ tickets, float* __restrict__ out, int64_t ldo,
+            int8_t* __restrict__ out_q, float* __restrict__ out_d)
+{
+    __shared__ __align__(16) AttnSmem<GQ> sm;
+    const int chunk = blockIdx.x, g = blockIdx.y;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    int r = 0;
+#pragma unroll 1
+    for (int i = 1; i < rows.n_rows; ++i)
+        if (chunk >= rows.row[i].chunk0) r = i;
+    const AttnRow row = rows.row[r];
+    const int CH = row.chunk;
+    const int c = chunk - row.chunk0;
+    const int nch = (row.len + CH - 1) / CH;
+    const int key0 = c * CH;
+    const int nvalid = min(CH, row.len - key0);
+    const int h0 = g * GQ;
+    const __half* kbase = row.k + g * row.head_stride + (int64_t)key0 * row.tok_stride;
+    const __half* vbase = row.v + g * row.head_stride + (int64_t)key0 * row.tok_stride;
+    if (tid == 0) {
+        // the chunk's V rows are needed after the scores: stage them in L2 now
+        prefetch_l2(vbase, (uint32_t)(((int64_t)(nvalid - 1) * row.tok_stride + kHeadDim) * 2));
+    }
+    for (int i = tid; i < GQ * kHeadDim; i += 256)
+        sm.q[i / kHeadDim][i % kHeadDim] = q[(size_t)r * ldq + (size_t)(h0 + i / kHeadDim) * kHeadDim + i % kHeadDim];
+    __syncthreads();
+
+    float* pout = part + ((size_t)chunk * Hq + h0) * kPartStride;
+    if (CH == 64)
+        attn_chunk<GQ, 64>(sm, kbase, vbase, row.tok_stride, nvalid, scale, pout);
+    else if (CH == 128)
+        attn_chunk<GQ, 128>(sm, kbase, vbase, row.tok_stride, nvalid, scale, pout);
+    else
+        attn_chunk<GQ, 256>(sm, kbase, vbase, row.tok_stride, nvalid, scale, pout);
 
     // ---- the last CTA of (row, g) merges the row's chunks
     __threadfence();
     __syncthreads();
-    if (tid == 0) last = (atomicAdd(&tickets[r * Hkv + g], 1) == nch - 1);
+    if (tid == 0) sm.last = (atomicAdd(&tickets[r * Hkv + g], 1) == nch - 1);
     __syncthreads();
-    if (!last) return;
+    if (!sm.last) return;
     __threadfence();
     const float* base = part + ((size_t)row.chunk0 * Hq + h0) * kPartStride;
     const size_t cstride = (size_t)Hq * kPartStride;
-    for (int blk = warp; blk < GQ * (kHeadDim / 32); blk += 8) {
-        const int h = blk / (kHeadDim / 32), d = (blk % (kHeadDim / 32)) * 32 + lane;
+    // chunk weights w[h][c] = e^(m_c - M_h) and L_h, in the reduction scratch
+    float* wts = &sm.red[0][0][0];               // [GQ][nch]
+    float* Ls = &sm.red[0][0][0] + GQ * nch;     // [GQ]
+    for (int h = warp; h < GQ; h += 8) {
         const float* bh = base + (size_t)h * kPartStride;
         float M = -INFINITY;
-        for (int cc = 0; cc < nch; ++cc) M = fmaxf(M, __ldcg(bh + cc * cstride + 128));
-        float L = 0.0f, O = 0.0f;
-        for (int cc = 0; cc < nch; ++cc) {
-            const float* pc = bh + cc * cstride;
-            const float w = expf(__fsub_rn(__ldcg(pc + 128), M));
-            L = __fmaf_rn(__ldcg(pc + 129), w, L);
-            O = __fmaf_rn(__ldcg(pc + d), w, O);
+        for (int cc = lane; cc < nch; cc += 32) M = fmaxf(M, __ldcg(bh + cc * cstride + 128));
+        M = warp_max(M);
+        for (int cc = lane; cc < nch; cc += 32) wts[h * nch + cc] = expf(__fsub_rn(__ldcg(bh + cc * cstride + 128), M));
+        __syncwarp();
+        if (lane == 0) {
+            float L = 0.0f;
+            for (int cc = 0; cc < nch; ++cc) L = __fmaf_rn(__ldcg(bh + cc * cstride + 129), wts[h * nch + cc], L);
+            Ls[h] = L;
         }
-        const float val = __fdiv_rn(O, L);
+    }
+    __syncthreads();
+    for (int blk = warp; blk < GQ * (kHeadDim / 32); blk += 8) {
+        const int h = blk / (kHeadDim / 32), d = (blk % (kHeadDim / 32)) * 32 + lane;
+        const float* bh = base + (size_t)h * kPartStride + d;
+        const float* wh = wts + h * nch;
+        float O = 0.0f;
+        int cc = 0;
+        for (; cc + 8 <= nch; cc += 8) {
+            float ov[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) ov[u] = __ldcg(bh + (cc + u) * cstride);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) O = __fmaf_rn(ov[u], wh[cc + u], O);
+        }
+        for (; cc < nch; ++cc) O = __fmaf_rn(__ldcg(bh + cc * cstride), wh[cc], O);
+        const float val = __fdiv_rn(O, Ls[h]);
         const size_t oi = (size_t)r * ldo + (size_t)(h0 + h) * kHeadDim + d;
         out[oi] = val;
         if (out_q) {

@@ -19,7 +19,7 @@ constexpr int kQK = 32;
 constexpr int kHeadDim = 128;
 constexpr int kMaxRows = 16;
 constexpr int kMaxSeq = 4;
-constexpr int kAttnChunk = 256;
+constexpr int kAttnChunk = 256;  // largest split-K chunk (keys)
 
 // ---------------------------------------------------------------- loads
 

@@ -31,6 +31,7 @@ struct AttnRow {
     int64_t tok_stride;
     int len;
     int chunk0;
+    int chunk;  // keys per split-K chunk of this row: attn_chunk_keys(len)
 };
 struct AttnRows {
     AttnRow row[16];
@@ -68,6 +69,10 @@ cudaError_t launch_kv_append(const float* k, const float* v, int64_t ld, int Hkv
 
 // Scratch floats for `total_chunks` chunks of Hq heads.
 size_t attn_part_floats(int total_chunks, int Hq);
+
+// Keys per split-K chunk for a row with `len` keys (a function of len only).
+int attn_chunk_keys(int len);
+constexpr int kAttnMaxChunksPerRow = 1023;  // the merge keeps one weight per chunk in shared memory
 
 // tickets: n_rows * Hkv ints that are zero on entry (and zero again on exit).
 // out_q / out_d (nullable): q8_0 codes and scales of out (requires ldo == Hq*128).

@@ -14,13 +14,16 @@
 // rows or on the launch shape, so a row of any launch equals the same row
 // launched alone, bit for bit.
 //
-// Work split (GB300): a CTA owns RW = 32/KL consecutive weight rows and has
-// 32/KL warps.  Lane (r = lane / KL, kb = lane % KL) of warp w runs chain
-// c = kb + KL*w of row r, so each warp instruction reads KL consecutive
-// 32-byte blocks of each of RW rows (KL*32 contiguous bytes per row, one
-// 32-byte load per lane, L1 bypassed) and every activation block is one
-// address shared by RW lanes (a broadcast through L1).  A lane keeps one
-// block in flight while it computes the previous one.  The chain values
+// Work split (GB300): a CTA has 32/KL warps and owns RC = G * 32/KL
+// consecutive weight rows.  Lane (r = lane / KL, kb = lane % KL) of warp w runs
+// chain c = kb + KL*w of the G rows r, r + 32/KL, ..., so each warp
+// instruction reads KL consecutive 32-byte blocks of each of 32/KL rows
+// (KL*32 contiguous bytes per row, one 32-byte load per lane, L1 bypassed).
+// Each activation block is loaded once per lane and reused for its G rows,
+// and is one address shared by the 32/KL lanes of a kb column; this keeps the
+// L1-to-register traffic per weight block at (G*32 + T*36)/G bytes, the
+// quantity that bounds this kernel at T >= 2.  A lane keeps the next block of
+// its G rows in flight while it computes the current one.  The chain values
 // meet in shared memory, where one thread per (row, token) applies the
 // butterfly's pairings in the same order.
 #include "common.cuh"
@@ -28,63 +31,74 @@
 
 namespace luce {
 
-template <int T, int KL, bool PF>
+template <int T, int KL, int G, bool PF>
 __global__ void __launch_bounds__(32 * (32 / KL))
 q8_matvec_kernel(const int8_t* __restrict__ wq, const __half* __restrict__ wd, int N, int K,
                  const int8_t* __restrict__ aq, const float* __restrict__ ad,
                  float* y, int64_t ldy, const float* resid, int64_t ldr)
 {
     constexpr int RW = 32 / KL;
-    __shared__ float part[RW][T][33];
+    constexpr int RC = RW * G;
+    __shared__ float part[RC][T][33];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int r = lane / KL, kb = lane - (lane / KL) * KL;
     const int c = kb + KL * w;
-    const int row0 = blockIdx.x * RW;
-    const int rowc = min(row0 + r, N - 1);
+    const int row0 = blockIdx.x * RC;
     const int nb = K >> 5;
-    const int8_t* wp = wq + (size_t)rowc * K + (size_t)c * 32;
-    const __half* dp = wd + (size_t)rowc * nb + c;
-    if (PF && threadIdx.x == 0) prefetch_l2(wq + (size_t)row0 * K, (uint32_t)(min(RW, N - row0) * K));
+    const int8_t* wp[G];
+    const __half* dp[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        const int rowc = min(row0 + r + RW * g, N - 1);
+        wp[g] = wq + (size_t)rowc * K + (size_t)c * 32;
+        dp[g] = wd + (size_t)rowc * nb + c;
+    }
+    if (PF && threadIdx.x == 0) prefetch_l2(wq + (size_t)row0 * K, (uint32_t)(min(RC, N - row0) * K));
     const int nj = (nb - c + 31) >> 5;  // blocks of this chain (>= 0)
 
-    float acc[T];
+    float acc[G][T];
 #pragma unroll
-    for (int t = 0; t < T; ++t) acc[t] = 0.0f;
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int t = 0; t < T; ++t) acc[g][t] = 0.0f;
 
-    auto compute = [&](const uint32_t (&wv)[8], float dw, int j) {
+    auto load = [&](uint32_t (&wv)[G][8], float (&sv)[G], int j) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            ld_stream_v8(wp[g] + (size_t)j * 1024, wv[g]);
+            sv[g] = __half2float(__ushort_as_half(ld_stream_u16(dp[g] + j * 32)));
+        }
+    };
+    auto compute = [&](const uint32_t (&wv)[G][8], const float (&sv)[G], int j) {
         const int b = c + 32 * j;
 #pragma unroll
         for (int t = 0; t < T; ++t) {
             uint32_t av[8];
             ld_cached_v8(aq + (size_t)t * K + (size_t)b * 32, av);
             const float da = __ldg(ad + (size_t)t * nb + b);
-            const int s = block_dot8(wv, av);
-            acc[t] = __fmaf_rn(__fmul_rn(dw, da), (float)s, acc[t]);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const int s = block_dot8(wv[g], av);
+                acc[g][t] = __fmaf_rn(__fmul_rn(sv[g], da), (float)s, acc[g][t]);
+            }
         }
     };
-    uint32_t wa[8], wb[8];
-    float sa = 0.0f, sb = 0.0f;
-    if (nj > 0) {
-        ld_stream_v8(wp, wa);
-        sa = __half2float(__ushort_as_half(ld_stream_u16(dp)));
-    }
+    uint32_t wa[G][8], wb[G][8];
+    float sa[G], sb[G];
+    if (nj > 0) load(wa, sa, 0);
     for (int j = 0; j < nj; j += 2) {
-        if (j + 1 < nj) {
-            ld_stream_v8(wp + (size_t)(j + 1) * 1024, wb);
-            sb = __half2float(__ushort_as_half(ld_stream_u16(dp + (j + 1) * 32)));
-        }
+        if (j + 1 < nj) load(wb, sb, j + 1);
         compute(wa, sa, j);
-        if (j + 2 < nj) {
-            ld_stream_v8(wp + (size_t)(j + 2) * 1024, wa);
-            sa = __half2float(__ushort_as_half(ld_stream_u16(dp + (j + 2) * 32)));
-        }
+        if (j + 2 < nj) load(wa, sa, j + 2);
         if (j + 1 < nj) compute(wb, sb, j + 1);
     }
 
 #pragma unroll
-    for (int t = 0; t < T; ++t) part[r][t][c] = acc[t];
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int t = 0; t < T; ++t) part[r + RW * g][t][c] = acc[g][t];
     __syncthreads();
-    for (int idx = threadIdx.x; idx < RW * T; idx += blockDim.x) {
+    for (int idx = threadIdx.x; idx < RC * T; idx += blockDim.x) {
         const int rr = idx / T, t = idx - (idx / T) * T;
         float v[32];
 #pragma unroll
@@ -102,14 +116,14 @@ q8_matvec_kernel(const int8_t* __restrict__ wq, const __half* __restrict__ wd, i
     }
 }
 
-template <int T, int KL, bool PF>
+template <int T, int KL, int G, bool PF>
 static cudaError_t launch_t(const int8_t* wq, const __half* wd, int N, int K, const int8_t* aq,
                             const float* ad, float* y, int64_t ldy, const float* resid, int64_t ldr,
                             cudaStream_t s)
 {
-    constexpr int RW = 32 / KL;
-    q8_matvec_kernel<T, KL, PF><<<(N + RW - 1) / RW, 32 * (32 / KL), 0, s>>>(wq, wd, N, K, aq, ad, y, ldy, resid,
-                                                                              ldr);
+    constexpr int RC = (32 / KL) * G;
+    q8_matvec_kernel<T, KL, G, PF><<<(N + RC - 1) / RC, 32 * (32 / KL), 0, s>>>(wq, wd, N, K, aq, ad, y, ldy,
+                                                                                resid, ldr);
     count_launches(1);
     return cudaGetLastError();
 }
@@ -118,27 +132,27 @@ cudaError_t launch_matvec(const int8_t* wq, const __half* wd, int N, int K, cons
                           const float* ad, int T, float* y, int64_t ldy, const float* resid,
                           int64_t ldr, cudaStream_t s)
 {
-    // KL (lanes per row) and the L2 prefetch only shape the memory pipeline;
-    // neither changes any row's arithmetic.
+    // KL (lanes per row), G (rows per lane) and the L2 prefetch only shape the
+    // memory pipeline; none of them changes any row's arithmetic.
     switch (T) {
-#define LUCE_MV(TT, KK, PP) \
-    case TT: return launch_t<TT, KK, PP>(wq, wd, N, K, aq, ad, y, ldy, resid, ldr, s);
-        LUCE_MV(1, 8, false)
-        LUCE_MV(2, 8, false)
-        LUCE_MV(3, 8, false)
-        LUCE_MV(4, 8, false)
-        LUCE_MV(5, 4, true)
-        LUCE_MV(6, 4, true)
-        LUCE_MV(7, 4, true)
-        LUCE_MV(8, 4, true)
-        LUCE_MV(9, 4, true)
-        LUCE_MV(10, 4, true)
-        LUCE_MV(11, 4, true)
-        LUCE_MV(12, 4, true)
-        LUCE_MV(13, 4, true)
-        LUCE_MV(14, 4, true)
-        LUCE_MV(15, 4, true)
-        LUCE_MV(16, 4, true)
+#define LUCE_MV(TT, KK, GG, PP) \
+    case TT: return launch_t<TT, KK, GG, PP>(wq, wd, N, K, aq, ad, y, ldy, resid, ldr, s);
+        LUCE_MV(1, 8, 1, false)
+        LUCE_MV(2, 8, 2, false)
+        LUCE_MV(3, 8, 2, false)
+        LUCE_MV(4, 8, 4, false)
+        LUCE_MV(5, 8, 4, false)
+        LUCE_MV(6, 8, 4, false)
+        LUCE_MV(7, 8, 4, false)
+        LUCE_MV(8, 8, 4, false)
+        LUCE_MV(9, 8, 2, false)
+        LUCE_MV(10, 8, 2, false)
+        LUCE_MV(11, 8, 2, false)
+        LUCE_MV(12, 8, 2, false)
+        LUCE_MV(13, 8, 2, false)
+        LUCE_MV(14, 8, 2, false)
+        LUCE_MV(15, 8, 2, false)
+        LUCE_MV(16, 8, 2, false)
 #undef LUCE_MV
         default: return cudaErrorInvalidValue;
     }
