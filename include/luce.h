@@ -56,7 +56,7 @@ typedef enum luce_status {
 #define LUCE_MAX_ROWS_PER_SEQ 4  /* rows per slot (1 decode + up to 3 drafts) */
 #define LUCE_MAX_ROWS 16         /* 8/12/16-row verify capacities [qfuse, item 1] */
 #define LUCE_HEAD_DIM 128
-#define LUCE_MAX_KEYS 261888     /* keys one attention row may see (1023 chunks of 256) */
+#define LUCE_MAX_KEYS 130816     /* keys one attention row may see (511 chunks of 256) */
 
 /* Message of the calling thread's last non-OK status ("" if none). */
 const char* luce_last_error(void);
@@ -157,9 +157,9 @@ int luce_kv_append(const float* k, const float* v, int64_t ldkv, int Hkv, int D,
  * token per sequence against its own cache; here up to 4 causal rows per
  * sequence].  For row r of view s and query head h (KV head g = h / (Hq/Hkv)):
  *   out[r][h] = sum_j softmax_j(scale * q[r][h] . K[g][j]) V[g][j]
- * over the row's keys.  The keys are split into chunks of 64 keys (rows with
- * at most 4,096 keys), 128 (at most 16,384) or 256 (more): a function of the
- * row's own key count only; each chunk yields (max, sum, unnormalised
+ * over the row's keys.  The keys are split into chunks of 128 keys (rows with
+ * at most 16,384 keys) or 256 (more): a function of the row's own key count
+ * only; each chunk yields (max, sum, unnormalised
  * output) and the chunks are merged in order by the exact log-sum-exp rule.
  * No output depends on the other rows.
  *   q   (device) fp32 [T][Hq][D] with T = max(row0 + n_q)

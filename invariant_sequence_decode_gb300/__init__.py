@@ -21,7 +21,7 @@ MAX_SEQ = 4
 MAX_ROWS_PER_SEQ = 4
 MAX_ROWS = 16
 HEAD_DIM = 128
-MAX_KEYS = 261888
+MAX_KEYS = 130816
 
 LUCE_OK, LUCE_EINVAL, LUCE_EUNSUPPORTED, LUCE_ECUDA, LUCE_ENOSPACE = 0, -1, -2, -3, -4
 

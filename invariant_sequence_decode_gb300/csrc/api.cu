@@ -73,8 +73,7 @@ int chunks_of(int len)
 // Largest chunk count of any row with at most max_len keys.
 int max_chunks_upto(int max_len)
 {
-    int m = chunks_of(std::min(max_len, 4096));
-    if (max_len > 4096) m = std::max(m, chunks_of(std::min(max_len, 16384)));
+    int m = chunks_of(std::min(max_len, 16384));
     if (max_len > 16384) m = std::max(m, chunks_of(max_len));
     return m;
 }

@@ -6,8 +6,8 @@
 // section 2: one multi-sequence attention launch with no position limit.
 //
 // A row's keys are cut into chunks of CH keys, CH = attn_chunk_keys(row's key
-// count) (64, 128 or 256: small contexts get more, smaller chunks so the GPU
-// has enough independent work).  One CTA of 256 threads per (row, chunk, KV
+// count) (128 up to 16,384 keys, else 256: small contexts get smaller chunks
+// so the GPU has enough independent work).  One CTA of 256 threads per (row, chunk, KV
 // head g) serves all Hq/Hkv query heads of g, so each K/V byte is read once:
 //   scores   TPK = 256/CH threads per key, thread part p covers dims
 //            [p*128/TPK, (p+1)*128/TPK): fma over its dims ascending, then the
@@ -37,11 +37,17 @@ constexpr int kPartStride = 132;  // o[128], m, l, 2 pad floats per (chunk, head
 
 size_t attn_part_floats(int total_chunks, int Hq) { return (size_t)total_chunks * Hq * kPartStride; }
 
-int attn_chunk_keys(int len) { return len <= 4096 ? 64 : (len <= 16384 ? 128 : 256); }
+int attn_chunk_keys(int len) { return len <= 16384 ? 128 : 256; }
+
+// q row of head h in shared memory: dim d at qpad(d) = d + 4*(d/32), so the
+// up-to-4 threads of a key (dims 32 apart) hit different banks and four
+// consecutive dims are one aligned 16-byte load.
+constexpr int kQStride = kHeadDim + 16;
+__device__ __forceinline__ int qpad(int d) { return d + 4 * (d >> 5); }
 
 template <int GQ>
 struct AttnSmem {
-    float q[GQ][kHeadDim];
+    float q[GQ][kQStride];
     float p[GQ][kAttnChunk];
     float red[8][GQ][kHeadDim];  // also the merge's scratch
     int last;
@@ -71,13 +77,17 @@ __device__ __forceinline__ void attn_chunk(AttnSmem<GQ>& sm, const __half* kbase
             for (int i = 0; i < DPT / 8; ++i) {
                 const __half2* hp = reinterpret_cast<const __half2*>(&kv[i]);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 kf = __half22float2(hp[e]);
-                    const int d = part * DPT + i * 8 + e * 2;
+                for (int e = 0; e < 4; e += 2) {
+                    const float2 k01 = __half22float2(hp[e]);
+                    const float2 k23 = __half22float2(hp[e + 1]);
+                    const int dq = qpad(part * DPT + i * 8 + e * 2);
 #pragma unroll
                     for (int h = 0; h < GQ; ++h) {
-                        dot[h] = __fmaf_rn(sm.q[h][d], kf.x, dot[h]);
-                        dot[h] = __fmaf_rn(sm.q[h][d + 1], kf.y, dot[h]);
+                        const float4 qv = *reinterpret_cast<const float4*>(&sm.q[h][dq]);
+                        dot[h] = __fmaf_rn(qv.x, k01.x, dot[h]);
+                        dot[h] = __fmaf_rn(qv.y, k01.y, dot[h]);
+                        dot[h] = __fmaf_rn(qv.z, k23.x, dot[h]);
+                        dot[h] = __fmaf_rn(qv.w, k23.y, dot[h]);
                     }
                 }
             }
@@ -175,7 +185,8 @@ attn_kernel(const float* __restrict__ q, int64_t ldq, AttnRows rows, int Hq, int
             float* __restrict__ part, int* __restrict__ tickets, float* __restrict__ out, int64_t ldo,
             int8_t* __restrict__ out_q, float* __restrict__ out_d)
 {
-    __shared__ __align__(16) AttnSmem<GQ> sm;
+    __shared__ __align__(16) AttnSmem<GQ> sm;  // q rows stay 16-byte aligned: kQStride % 4 == 0
+    pdl_trigger();
     const int chunk = blockIdx.x, g = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
@@ -193,11 +204,15 @@ attn_kernel(const float* __restrict__ q, int64_t ldq, AttnRows rows, int Hq, int
     const __half* kbase = row.k + g * row.head_stride + (int64_t)key0 * row.tok_stride;
     const __half* vbase = row.v + g * row.head_stride + (int64_t)key0 * row.tok_stride;
     if (tid == 0) {
-        // the chunk's V rows are needed after the scores: stage them in L2 now
-        prefetch_l2(vbase, (uint32_t)(((int64_t)(nvalid - 1) * row.tok_stride + kHeadDim) * 2));
+        // stage the chunk's K and V rows in L2 while the previous kernel ends
+        // (a cache hint only: the rows it writes are read after pdl_wait)
+        const uint32_t span = (uint32_t)(((int64_t)(nvalid - 1) * row.tok_stride + kHeadDim) * 2);
+        prefetch_l2(kbase, span);
+        prefetch_l2(vbase, span);
     }
+    pdl_wait();
     for (int i = tid; i < GQ * kHeadDim; i += 256)
-        sm.q[i / kHeadDim][i % kHeadDim] = q[(size_t)r * ldq + (size_t)(h0 + i / kHeadDim) * kHeadDim + i % kHeadDim];
+        sm.q[i / kHeadDim][qpad(i % kHeadDim)] = q[(size_t)r * ldq + (size_t)(h0 + i / kHeadDim) * kHeadDim + i % kHeadDim];
     __syncthreads();
 
     float* pout = part + ((size_t)chunk * Hq + h0) * kPartStride;
@@ -217,19 +232,27 @@ attn_kernel(const float* __restrict__ q, int64_t ldq, AttnRows rows, int Hq, int
     __threadfence();
     const float* base = part + ((size_t)row.chunk0 * Hq + h0) * kPartStride;
     const size_t cstride = (size_t)Hq * kPartStride;
-    // chunk weights w[h][c] = e^(m_c - M_h) and L_h, in the reduction scratch
-    float* wts = &sm.red[0][0][0];               // [GQ][nch]
-    float* Ls = &sm.red[0][0][0] + GQ * nch;     // [GQ]
+    // chunk weights w[h][c] = e^(m_c - M_h), the chunk sums l[h][c] and L_h,
+    // in the reduction scratch; every load of the chunk statistics is issued
+    // lane-parallel, only the sum over c is sequential (in chunk order).
+    float* wts = &sm.red[0][0][0];                // [GQ][nch]
+    float* lsum = &sm.red[0][0][0] + GQ * nch;    // [GQ][nch]
+    float* Ls = &sm.red[0][0][0] + 2 * GQ * nch;  // [GQ]
     for (int h = warp; h < GQ; h += 8) {
         const float* bh = base + (size_t)h * kPartStride;
         float M = -INFINITY;
-        for (int cc = lane; cc < nch; cc += 32) M = fmaxf(M, __ldcg(bh + cc * cstride + 128));
+        for (int cc = lane; cc < nch; cc += 32) {
+            const float m = __ldcg(bh + cc * cstride + 128);
+            wts[h * nch + cc] = m;
+            lsum[h * nch + cc] = __ldcg(bh + cc * cstride + 129);
+            M = fmaxf(M, m);
+        }
         M = warp_max(M);
-        for (int cc = lane; cc < nch; cc += 32) wts[h * nch + cc] = expf(__fsub_rn(__ldcg(bh + cc * cstride + 128), M));
+        for (int cc = lane; cc < nch; cc += 32) wts[h * nch + cc] = expf(__fsub_rn(wts[h * nch + cc], M));
         __syncwarp();
         if (lane == 0) {
             float L = 0.0f;
-            for (int cc = 0; cc < nch; ++cc) L = __fmaf_rn(__ldcg(bh + cc * cstride + 129), wts[h * nch + cc], L);
+            for (int cc = 0; cc < nch; ++cc) L = __fmaf_rn(lsum[h * nch + cc], wts[h * nch + cc], L);
             Ls[h] = L;
         }
     }
@@ -240,12 +263,12 @@ attn_kernel(const float* __restrict__ q, int64_t ldq, AttnRows rows, int Hq, int
         const float* wh = wts + h * nch;
         float O = 0.0f;
         int cc = 0;
-        for (; cc + 8 <= nch; cc += 8) {
-            float ov[8];
+        for (; cc + 16 <= nch; cc += 16) {
+            float ov[16];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) ov[u] = __ldcg(bh + (cc + u) * cstride);
+            for (int u = 0; u < 16; ++u) ov[u] = __ldcg(bh + (cc + u) * cstride);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) O = __fmaf_rn(ov[u], wh[cc + u], O);
+            for (int u = 0; u < 16; ++u) O = __fmaf_rn(ov[u], wh[cc + u], O);
         }
         for (; cc < nch; ++cc) O = __fmaf_rn(__ldcg(bh + cc * cstride), wh[cc], O);
         const float val = __fdiv_rn(O, Ls[h]);
@@ -265,8 +288,8 @@ template <int GQ>
 static void launch_g(const float* q, int64_t ldq, const AttnRows& rows, int Hq, int Hkv, float scale, float* part,
                      int* tickets, float* out, int64_t ldo, int8_t* out_q, float* out_d, cudaStream_t s)
 {
-    attn_kernel<GQ><<<dim3(rows.total_chunks, Hkv), 256, 0, s>>>(q, ldq, rows, Hq, Hkv, scale, part, tickets, out,
-                                                                   ldo, out_q, out_d);
+    launch_pdl(attn_kernel<GQ>, dim3(rows.total_chunks, Hkv), dim3(256), s, q, ldq, rows, Hq, Hkv, scale, part, tickets,
+               out, ldo, out_q, out_d);
     count_launches(1);
 }
 

@@ -15,6 +15,34 @@
 
 namespace luce {
 
+// ---------------------------------------------------------------- launch
+
+// Programmatic dependent launch: every kernel lets the next kernel of the
+// stream start as soon as all of its own CTAs are running (pdl_trigger at
+// entry); the next kernel does only work that reads nothing the previous
+// kernel writes (weight loads, L2 prefetches) before pdl_wait, which returns
+// once the previous kernel has completed and its writes are visible.  Both
+// are no-ops for a launch without the attribute.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+static inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t s,
+                                     Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 constexpr int kQK = 32;
 constexpr int kHeadDim = 128;
 constexpr int kMaxRows = 16;

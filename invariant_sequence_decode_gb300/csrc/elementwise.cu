@@ -17,6 +17,8 @@ __global__ void __launch_bounds__(256)
 quantize_kernel(const float* __restrict__ x, int T, int K, int64_t ldx, int8_t* __restrict__ q,
                 float* __restrict__ d)
 {
+    pdl_trigger();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int nb = K >> 5;
     const int64_t blk = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -32,19 +34,23 @@ quantize_kernel(const float* __restrict__ x, int T, int K, int64_t ldx, int8_t* 
 cudaError_t launch_quantize(const float* x, int T, int K, int64_t ldx, int8_t* q, float* d, cudaStream_t s)
 {
     const int64_t blocks = (int64_t)T * (K >> 5);
-    quantize_kernel<<<(unsigned)((blocks + 7) / 8), 256, 0, s>>>(x, T, K, ldx, q, d);
+    const cudaError_t e = launch_pdl(quantize_kernel, dim3((unsigned)((blocks + 7) / 8)), dim3(256), s, x, T, K, ldx,
+                                     q, d);
     count_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 // RMSNorm of one row per CTA (512 threads), then q8_0 quantization of the
-// normalised row.  Sum of squares: thread i adds x[i], x[i+512], ... with fma
-// in ascending order (its loads are all issued before the adds); warp
-// partials by butterfly; thread 0 adds the 16 warp sums in warp order.
-// r = 1 / sqrt(ss / H + eps) with IEEE division and square root.  The order
-// depends on H only.
+// normalised row.  Warp w owns the 32-value blocks b = w, w + 16, ... and
+// lane l element 32b + l of each; the row is read once (all loads issued
+// together) and kept in registers.  Sum of squares: each thread adds its
+// elements' squares with fma in ascending b; warp partials by butterfly;
+// thread 0 adds the 16 warp sums in warp order.  r = 1 / sqrt(ss / H + eps)
+// with IEEE division and square root.  The order depends on H only.
 constexpr int kNormThreads = 512;
+constexpr int kNormMaxPerThread = 16;  // H <= 512 * 16 = 8192 on the register path
 
+template <bool REG>
 __global__ void __launch_bounds__(kNormThreads)
 rmsnorm_quant_kernel(const float* __restrict__ x, int H, const float* __restrict__ gamma, float eps,
                      float* __restrict__ xn, int8_t* __restrict__ q, float* __restrict__ d)
@@ -52,21 +58,28 @@ rmsnorm_quant_kernel(const float* __restrict__ x, int H, const float* __restrict
     constexpr int NW = kNormThreads / 32;
     __shared__ float red[NW];
     __shared__ float rs;
+    pdl_trigger();
+    pdl_wait();
     const int t = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float* xr = x + (size_t)t * H;
+    const int nb = H >> 5;
+    float v[kNormMaxPerThread];
     float ss = 0.0f;
-    int i = tid;
-    for (; i + 3 * kNormThreads < H; i += 4 * kNormThreads) {
-        const float v0 = xr[i], v1 = xr[i + kNormThreads], v2 = xr[i + 2 * kNormThreads], v3 = xr[i + 3 * kNormThreads];
-        ss = __fmaf_rn(v0, v0, ss);
-        ss = __fmaf_rn(v1, v1, ss);
-        ss = __fmaf_rn(v2, v2, ss);
-        ss = __fmaf_rn(v3, v3, ss);
-    }
-    for (; i < H; i += kNormThreads) {
-        const float v = xr[i];
-        ss = __fmaf_rn(v, v, ss);
+    if (REG) {
+#pragma unroll
+        for (int k = 0; k < kNormMaxPerThread; ++k) {
+            const int b = warp + NW * k;
+            v[k] = b < nb ? xr[b * 32 + lane] : 0.0f;
+        }
+#pragma unroll
+        for (int k = 0; k < kNormMaxPerThread; ++k)
+            if (warp + NW * k < nb) ss = __fmaf_rn(v[k], v[k], ss);
+    } else {
+        for (int b = warp; b < nb; b += NW) {
+            const float e = xr[b * 32 + lane];
+            ss = __fmaf_rn(e, e, ss);
+        }
     }
     ss = warp_sum_butterfly(ss);
     if (lane == 0) red[warp] = ss;
@@ -79,24 +92,30 @@ rmsnorm_quant_kernel(const float* __restrict__ x, int H, const float* __restrict
     }
     __syncthreads();
     const float r = rs;
-    const int nb = H >> 5;
-    for (int b = warp; b < nb; b += NW) {
-        const int k = b * 32 + lane;
-        const float v = __fmul_rn(__fmul_rn(xr[k], r), gamma[k]);
-        xn[(size_t)t * H + k] = v;
-        float dd;
-        const int code = q8_quantize_lane(v, &dd);
-        q[(size_t)t * H + k] = (int8_t)code;
-        if (lane == 0) d[(size_t)t * nb + b] = dd;
+#pragma unroll
+    for (int k = 0; k < (REG ? kNormMaxPerThread : 1); ++k) {
+        for (int b = warp + NW * k; b < nb; b += (REG ? nb : NW)) {
+            const int i = b * 32 + lane;
+            const float e = REG ? v[k] : xr[i];
+            const float vn = __fmul_rn(__fmul_rn(e, r), gamma[i]);
+            xn[(size_t)t * H + i] = vn;
+            float dd;
+            const int code = q8_quantize_lane(vn, &dd);
+            q[(size_t)t * H + i] = (int8_t)code;
+            if (lane == 0) d[(size_t)t * nb + b] = dd;
+        }
     }
 }
 
 cudaError_t launch_rmsnorm_quant(const float* x, int T, int H, const float* gamma, float eps,
                                  float* xn, int8_t* q, float* d, cudaStream_t s)
 {
-    rmsnorm_quant_kernel<<<T, kNormThreads, 0, s>>>(x, H, gamma, eps, xn, q, d);
+    const cudaError_t e =
+        H <= kNormThreads * kNormMaxPerThread
+            ? launch_pdl(rmsnorm_quant_kernel<true>, dim3(T), dim3(kNormThreads), s, x, H, gamma, eps, xn, q, d)
+            : launch_pdl(rmsnorm_quant_kernel<false>, dim3(T), dim3(kNormThreads), s, x, H, gamma, eps, xn, q, d);
     count_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 // SwiGLU of the concatenated gate||up row (gate first), then q8_0.
@@ -104,6 +123,8 @@ __global__ void __launch_bounds__(256)
 swiglu_quant_kernel(const float* __restrict__ gu, int T, int F, float* __restrict__ h,
                     int8_t* __restrict__ q, float* __restrict__ d)
 {
+    pdl_trigger();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int nb = F >> 5;
     const int64_t blk = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -124,9 +145,10 @@ cudaError_t launch_swiglu_quant(const float* gu, int T, int F, float* h, int8_t*
                                 cudaStream_t s)
 {
     const int64_t blocks = (int64_t)T * (F >> 5);
-    swiglu_quant_kernel<<<(unsigned)((blocks + 7) / 8), 256, 0, s>>>(gu, T, F, h, q, d);
+    const cudaError_t e = launch_pdl(swiglu_quant_kernel, dim3((unsigned)((blocks + 7) / 8)), dim3(256), s, gu, T, F,
+                                     h, q, d);
     count_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 // Argmax of each row, lowest index on ties, NaN never chosen (all-NaN -> 0).
@@ -145,6 +167,8 @@ argmax_kernel(const float* __restrict__ x, int V, int32_t* __restrict__ out)
 {
     __shared__ float sv[32];
     __shared__ int si[32];
+    pdl_trigger();
+    pdl_wait();
     const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float* r = x + (size_t)t * V;
     float bv = 0.0f;
@@ -172,9 +196,9 @@ argmax_kernel(const float* __restrict__ x, int V, int32_t* __restrict__ out)
 
 cudaError_t launch_argmax(const float* x, int T, int V, int32_t* out, cudaStream_t s)
 {
-    argmax_kernel<<<T, 1024, 0, s>>>(x, V, out);
+    const cudaError_t e = launch_pdl(argmax_kernel, dim3(T), dim3(1024), s, x, V, out);
     count_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace luce

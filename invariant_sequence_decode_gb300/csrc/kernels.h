@@ -72,7 +72,7 @@ size_t attn_part_floats(int total_chunks, int Hq);
 
 // Keys per split-K chunk for a row with `len` keys (a function of len only).
 int attn_chunk_keys(int len);
-constexpr int kAttnMaxChunksPerRow = 1023;  // the merge keeps one weight per chunk in shared memory
+constexpr int kAttnMaxChunksPerRow = 511;  // the merge keeps two floats per chunk in shared memory
 
 // tickets: n_rows * Hkv ints that are zero on entry (and zero again on exit).
 // out_q / out_d (nullable): q8_0 codes and scales of out (requires ldo == Hq*128).

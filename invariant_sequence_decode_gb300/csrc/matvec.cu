@@ -40,6 +40,7 @@ q8_matvec_kernel(const int8_t* __restrict__ wq, const __half* __restrict__ wd, i
     constexpr int RW = 32 / KL;
     constexpr int RC = RW * G;
     __shared__ float part[RC][T][33];
+    pdl_trigger();
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int r = lane / KL, kb = lane - (lane / KL) * KL;
     const int c = kb + KL * w;
@@ -85,7 +86,8 @@ q8_matvec_kernel(const int8_t* __restrict__ wq, const __half* __restrict__ wd, i
     };
     uint32_t wa[G][8], wb[G][8];
     float sa[G], sb[G];
-    if (nj > 0) load(wa, sa, 0);
+    if (nj > 0) load(wa, sa, 0);  // weights do not depend on the previous kernel
+    pdl_wait();                   // activations and the residual do
     for (int j = 0; j < nj; j += 2) {
         if (j + 1 < nj) load(wb, sb, j + 1);
         compute(wa, sa, j);
@@ -122,10 +124,10 @@ static cudaError_t launch_t(const int8_t* wq, const __half* wd, int N, int K, co
                             cudaStream_t s)
 {
     constexpr int RC = (32 / KL) * G;
-    q8_matvec_kernel<T, KL, G, PF><<<(N + RC - 1) / RC, 32 * (32 / KL), 0, s>>>(wq, wd, N, K, aq, ad, y, ldy,
-                                                                                resid, ldr);
+    const cudaError_t e = launch_pdl(q8_matvec_kernel<T, KL, G, PF>, dim3((N + RC - 1) / RC), dim3(32 * (32 / KL)), s,
+                                     wq, wd, N, K, aq, ad, y, ldy, resid, ldr);
     count_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_matvec(const int8_t* wq, const __half* wd, int N, int K, const int8_t* aq,
@@ -163,6 +165,8 @@ cudaError_t launch_matvec(const int8_t* wq, const __half* wd, int N, int K, cons
 __global__ void q8_block_dots_kernel(const int8_t* __restrict__ wq, int N, int K,
                                      const int8_t* __restrict__ aq, int T, int32_t* __restrict__ out)
 {
+    pdl_trigger();
+    pdl_wait();
     const int nb = K >> 5;
     const int64_t total = (int64_t)T * N * nb;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
@@ -183,9 +187,9 @@ cudaError_t launch_block_dots(const int8_t* wq, int N, int K, const int8_t* aq, 
 {
     const int64_t total = (int64_t)T * N * (K >> 5);
     const int blocks = (int)((total + 255) / 256 < 65536 ? (total + 255) / 256 : 65536);
-    q8_block_dots_kernel<<<blocks, 256, 0, s>>>(wq, N, K, aq, T, out);
+    const cudaError_t e = launch_pdl(q8_block_dots_kernel, dim3(blocks), dim3(256), s, wq, N, K, aq, T, out);
     count_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace luce

@@ -19,6 +19,8 @@ namespace luce {
 __global__ void __launch_bounds__(64)
 rope_posvec_kernel(float* __restrict__ x, int64_t ldx, const int32_t* __restrict__ pos, RopeFreq f)
 {
+    pdl_trigger();
+    pdl_wait();
     const int t = blockIdx.x, h = blockIdx.y, i = threadIdx.x;
     const float2 cs = rope_cs(pos[t], f.inv[i]);
     float* p = x + (size_t)t * ldx + (size_t)h * kHeadDim + i;
@@ -31,15 +33,17 @@ rope_posvec_kernel(float* __restrict__ x, int64_t ldx, const int32_t* __restrict
 cudaError_t launch_rope_posvec(float* x, int T, int n_heads, int64_t ldx, const int32_t* pos,
                                const RopeFreq& f, cudaStream_t s)
 {
-    rope_posvec_kernel<<<dim3(T, n_heads), 64, 0, s>>>(x, ldx, pos, f);
+    const cudaError_t e = launch_pdl(rope_posvec_kernel, dim3(T, n_heads), dim3(64), s, x, ldx, pos, f);
     count_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 // Standalone K/V append: one CTA per row; fp32 -> binary16 round-to-nearest.
 __global__ void __launch_bounds__(256)
 kv_append_kernel(const float* __restrict__ k, const float* __restrict__ v, int64_t ld, int Hkv, KvRows rows)
 {
+    pdl_trigger();
+    pdl_wait();
     const int t = blockIdx.x;
     const KvRow r = rows.row[t];
     for (int idx = threadIdx.x; idx < Hkv * kHeadDim; idx += blockDim.x) {
@@ -52,9 +56,9 @@ kv_append_kernel(const float* __restrict__ k, const float* __restrict__ v, int64
 cudaError_t launch_kv_append(const float* k, const float* v, int64_t ld, int Hkv, const KvRows& rows,
                              cudaStream_t s)
 {
-    kv_append_kernel<<<rows.n_rows, 256, 0, s>>>(k, v, ld, Hkv, rows);
+    const cudaError_t e = launch_pdl(kv_append_kernel, dim3(rows.n_rows), dim3(256), s, k, v, ld, Hkv, rows);
     count_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 // Decode-step glue, one CTA per (row, head of the fused q|k|v projection):
@@ -65,11 +69,13 @@ __global__ void __launch_bounds__(64)
 rope_kv_kernel(const float* __restrict__ qkv, int Hq, int Hkv, RowPos pos, RopeFreq f,
                float* __restrict__ q_rot, KvRows rows)
 {
+    pdl_trigger();
     const int t = blockIdx.x, h = blockIdx.y, i = threadIdx.x;
+    const float2 cs = h < Hq + Hkv ? rope_cs(pos.pos[t], f.inv[i]) : make_float2(1.0f, 0.0f);
+    pdl_wait();
     const float* src = qkv + (size_t)t * (Hq + 2 * Hkv) * kHeadDim + (size_t)h * kHeadDim;
     const KvRow r = rows.row[t];
     if (h < Hq + Hkv) {
-        const float2 cs = rope_cs(pos.pos[t], f.inv[i]);
         float x0 = src[i], x1 = src[i + 64];
         rope_rotate(x0, x1, cs.x, cs.y);
         if (h < Hq) {
@@ -91,9 +97,10 @@ rope_kv_kernel(const float* __restrict__ qkv, int Hq, int Hkv, RowPos pos, RopeF
 cudaError_t launch_rope_kv(const float* qkv, int T, int Hq, int Hkv, const RowPos& pos, const RopeFreq& f,
                            float* q_rot, const KvRows& rows, cudaStream_t s)
 {
-    rope_kv_kernel<<<dim3(T, Hq + 2 * Hkv), 64, 0, s>>>(qkv, Hq, Hkv, pos, f, q_rot, rows);
+    const cudaError_t e = launch_pdl(rope_kv_kernel, dim3(T, Hq + 2 * Hkv), dim3(64), s, qkv, Hq, Hkv, pos, f, q_rot,
+                                     rows);
     count_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace luce
