@@ -189,6 +189,51 @@ def matvec_roofline(torch, luce, wl, L: Layer27B, T: int, reps: int) -> dict:
     return out
 
 
+def verify64_detail(torch, luce, wl, flush, steps: int) -> dict:
+    """Wide speculative verify: 4 slots x 2/3/4 rows through 64 distinct layers
+    plus the 151,936 x 5120 q8_0 head (logits and argmax), cache lengths
+    uniform on [1024, 2051].  Returns rows/s and the step's algorithmic GB/s."""
+    d = wl.LAYER27B
+    seed, n_layers, cap = 4, 64, 2051 + 4
+    cu = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    layers = []
+    for l in range(n_layers):
+        h = wl.layer_host(seed, l, d)
+        layers.append(luce.LayerTensors(*[cu(getattr(h, f)) for f in LAYER_FIELDS]))
+        del h
+    fn, hq, hd = [cu(a) for a in wl.head_host(seed, d, wl.VOCAB)]
+    model = luce.Model(layers, d.hidden, d.n_q_heads, d.n_kv_heads, d.ffn, final_norm=fn, head_q=hq, head_d=hd)
+    lens = wl.lens(seed, 4, 1024, 2051, sub=4)
+    slots = []
+    for s, ln in enumerate(lens):
+        kk = torch.empty((n_layers, d.n_kv_heads, cap, d.head_dim), dtype=torch.float16, device="cuda")
+        vv = torch.empty_like(kk)
+        for l in range(n_layers):
+            k, v = wl.cache_host(seed, s, l, d, cap, ln)
+            kk[l].copy_(torch.from_numpy(k))
+            vv[l].copy_(torch.from_numpy(v))
+        slots.append(luce.Slot(kk, vv, ln))
+    out = {}
+    weight_bytes = n_layers * layer_bytes(d) + wl.VOCAB * d.hidden * 34 // 32
+    for rps in (2, 3, 4):
+        T = 4 * rps
+        x = cu(wl.acts(seed, T, d.hidden, sub=20 + rps))
+        ws = model.workspace(T, cap)
+        logits = torch.empty((T, wl.VOCAB), dtype=torch.float32, device="cuda")
+        am = torch.empty(T, dtype=torch.int32, device="cuda")
+        fn_step = lambda: luce.luce_decode_step(model, slots, [rps] * 4, x, ws, logits, am)
+        for _ in range(2):
+            fn_step()
+        ms = statistics.median(time_steps(torch, fn_step, flush, steps))
+        kv_bytes = sum((ln + j + 1) for ln in lens for j in range(rps)) * n_layers * d.n_kv_heads * 128 * 2 * 2
+        out[f"rows_{T}"] = {"ms_per_step": round(ms, 3), "tok_s": round(T / (ms / 1e3), 1),
+                            "steps_s": round(1e3 / ms, 2),
+                            "gbps": round((weight_bytes + kv_bytes) / (ms / 1e3) / 1e9, 1)}
+    del layers, model, slots
+    torch.cuda.empty_cache()
+    return out
+
+
 def cpu_baseline_oracle(wl, L_host, caches_host, x_host, n_seq: int) -> dict:
     import oracle
     d = wl.LAYER27B
@@ -272,6 +317,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     detail["matvec_gbps_by_ntok"] = {T: round(v["all"]["gbps"], 1) for T, v in mv.items()}
     detail["matvec_by_proj_ntok4"] = {k: {"gbps": round(v["gbps"], 1), "us": round(v["ms"] * 1e3, 2)}
                                       for k, v in mv["4"].items() if k != "all"}
+    detail["verify64"] = verify64_detail(torch, luce, wl, L.flush_l2, steps=5)
     detail["layer_weight_bytes"] = layer_bytes(L.d)
     detail["step_bytes_algorithmic"] = layer_bytes(L.d) + n_seq * 2 * L.d.n_kv_heads * KV_TOKENS * 128 * 2
     detail["step_gbps"] = detail["step_bytes_algorithmic"] / (ms_per_step / 1e3) / 1e9
@@ -308,7 +354,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
            "h2d_bytes_per_step": int(xh.numel() * 4), "d2h_bytes_per_step": int(outh.numel() * 4)}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1:
         cpu = cpu_baseline_oracle(wl, L.host, L.caches_host, L.x_host, n_seq)
 
     if rank == 0:
@@ -361,7 +407,6 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank = int(os.environ.get("RANK", "0"))
