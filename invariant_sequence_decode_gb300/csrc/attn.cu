@@ -9,10 +9,10 @@
 // count) (128 up to 16,384 keys, else 256: small contexts get smaller chunks
 // so the GPU has enough independent work).  One CTA of 256 threads per (row, chunk, KV
 // head g) serves all Hq/Hkv query heads of g, so each K/V byte is read once:
-//   scores   TPK = 256/CH threads per key, thread part p covers dims
-//            [p*128/TPK, (p+1)*128/TPK): fma over its dims ascending, then the
-//            TPK partial dots are summed by an xor butterfly (1, then 2);
-//            s_h = scale * dot;
+//   scores   P = 512/CH threads per key pair (j, j + CH/2); thread part p
+//            covers dims [p*128/P, (p+1)*128/P) of both keys: fma over its
+//            dims ascending, then the P partial dots of a key are summed by an
+//            xor butterfly (1, 2, ...); s_h = scale * dot;
 //   softmax  warp h owns head h: m = max_j s_h, p_j = exp(s_h - m),
 //            l = sum p_j (lane-serial over j = lane + 32i, then butterfly);
 //   values   warp w owns keys w, w+8, ... and lane l dims 4l..4l+3:
@@ -58,48 +58,63 @@ template <int GQ, int CH>
 __device__ __forceinline__ void attn_chunk(AttnSmem<GQ>& sm, const __half* kbase, const __half* vbase,
                                            int64_t tok_stride, int nvalid, float scale, float* pout)
 {
-    constexpr int TPK = 256 / CH;
-    constexpr int DPT = kHeadDim / TPK;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-    // ---- scores
+    // ---- scores: each thread computes 2 keys (j, j + CH/2) over DPT dims, so
+    // every q load from shared memory serves 8 fma
     {
-        const int j = tid / TPK, part = tid % TPK;
-        float dot[GQ];
+        constexpr int PARTS = 512 / CH;       // threads per key pair
+        constexpr int DPT2 = kHeadDim / PARTS;
+        const int j = tid / PARTS, part = tid % PARTS;
+        float dot0[GQ], dot1[GQ];
 #pragma unroll
-        for (int h = 0; h < GQ; ++h) dot[h] = 0.0f;
-        if (j < nvalid) {
-            const int4* kp = reinterpret_cast<const int4*>(kbase + (int64_t)j * tok_stride + part * DPT);
-            int4 kv[DPT / 8];
+        for (int h = 0; h < GQ; ++h) dot0[h] = dot1[h] = 0.0f;
+        const bool v0 = j < nvalid, v1 = j + CH / 2 < nvalid;
+        const int4* kp0 = reinterpret_cast<const int4*>(kbase + (int64_t)j * tok_stride + part * DPT2);
+        const int4* kp1 = reinterpret_cast<const int4*>(kbase + (int64_t)(j + CH / 2) * tok_stride + part * DPT2);
+        int4 ka[DPT2 / 8], kc[DPT2 / 8];
 #pragma unroll
-            for (int i = 0; i < DPT / 8; ++i) kv[i] = __ldg(kp + i);
+        for (int i = 0; i < DPT2 / 8; ++i) {
+            ka[i] = v0 ? __ldg(kp0 + i) : make_int4(0, 0, 0, 0);
+            kc[i] = v1 ? __ldg(kp1 + i) : make_int4(0, 0, 0, 0);
+        }
 #pragma unroll
-            for (int i = 0; i < DPT / 8; ++i) {
-                const __half2* hp = reinterpret_cast<const __half2*>(&kv[i]);
+        for (int i = 0; i < DPT2 / 8; ++i) {
+            const __half2* ha = reinterpret_cast<const __half2*>(&ka[i]);
+            const __half2* hc = reinterpret_cast<const __half2*>(&kc[i]);
 #pragma unroll
-                for (int e = 0; e < 4; e += 2) {
-                    const float2 k01 = __half22float2(hp[e]);
-                    const float2 k23 = __half22float2(hp[e + 1]);
-                    const int dq = qpad(part * DPT + i * 8 + e * 2);
+            for (int e = 0; e < 4; e += 2) {
+                const float2 a01 = __half22float2(ha[e]), a23 = __half22float2(ha[e + 1]);
+                const float2 c01 = __half22float2(hc[e]), c23 = __half22float2(hc[e + 1]);
+                const int dq = qpad(part * DPT2 + i * 8 + e * 2);
 #pragma unroll
-                    for (int h = 0; h < GQ; ++h) {
-                        const float4 qv = *reinterpret_cast<const float4*>(&sm.q[h][dq]);
-                        dot[h] = __fmaf_rn(qv.x, k01.x, dot[h]);
-                        dot[h] = __fmaf_rn(qv.y, k01.y, dot[h]);
-                        dot[h] = __fmaf_rn(qv.z, k23.x, dot[h]);
-                        dot[h] = __fmaf_rn(qv.w, k23.y, dot[h]);
-                    }
+                for (int h = 0; h < GQ; ++h) {
+                    const float4 qv = *reinterpret_cast<const float4*>(&sm.q[h][dq]);
+                    dot0[h] = __fmaf_rn(qv.x, a01.x, dot0[h]);
+                    dot0[h] = __fmaf_rn(qv.y, a01.y, dot0[h]);
+                    dot0[h] = __fmaf_rn(qv.z, a23.x, dot0[h]);
+                    dot0[h] = __fmaf_rn(qv.w, a23.y, dot0[h]);
+                    dot1[h] = __fmaf_rn(qv.x, c01.x, dot1[h]);
+                    dot1[h] = __fmaf_rn(qv.y, c01.y, dot1[h]);
+                    dot1[h] = __fmaf_rn(qv.z, c23.x, dot1[h]);
+                    dot1[h] = __fmaf_rn(qv.w, c23.y, dot1[h]);
                 }
             }
         }
 #pragma unroll
         for (int h = 0; h < GQ; ++h) {
 #pragma unroll
-            for (int off = 1; off < TPK; off <<= 1) dot[h] = __fadd_rn(dot[h], __shfl_xor_sync(0xffffffffu, dot[h], off));
+            for (int off = 1; off < PARTS; off <<= 1) {
+                dot0[h] = __fadd_rn(dot0[h], __shfl_xor_sync(0xffffffffu, dot0[h], off));
+                dot1[h] = __fadd_rn(dot1[h], __shfl_xor_sync(0xffffffffu, dot1[h], off));
+            }
         }
         if (part == 0) {
 #pragma unroll
-            for (int h = 0; h < GQ; ++h) sm.p[h][j] = (j < nvalid) ? __fmul_rn(dot[h], scale) : -INFINITY;
+            for (int h = 0; h < GQ; ++h) {
+                sm.p[h][j] = v0 ? __fmul_rn(dot0[h], scale) : -INFINITY;
+                sm.p[h][j + CH / 2] = v1 ? __fmul_rn(dot1[h], scale) : -INFINITY;
+            }
         }
     }
     __syncthreads();
