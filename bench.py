@@ -56,6 +56,23 @@ def layer_bytes(d) -> int:
     return nk * 34 // 32
 
 
+def measured_traffic():
+    """DRAM bytes (read + write) of the four projections at n_tok = 4 from the
+    committed ncu summary, or None when the matvec source has changed since
+    those counters were taken."""
+    import hashlib
+    import re
+    prof = os.path.join(ROOT, "profiles", "q8_matvec_27b_layer_t4_traffic.md")
+    src = os.path.join(ROOT, "invariant_sequence_decode_gb300", "csrc", "matvec.cu")
+    try:
+        m = re.search(r"traffic_bytes_layer_t4=(\d+) matvec_cu_sha256_16=([0-9a-f]+)", open(prof).read())
+        if m and hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] == m.group(2):
+            return int(m.group(1))
+    except OSError:
+        pass
+    return None
+
+
 def peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -327,7 +344,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     roofline = {"bound": "hbm", "kernel": "q8_matvec_kernel (the four projections of the layer, n_tok=4)",
                 "achieved": round(a, 1), "peak": pk["hbm_gbs"], "peak_source": pk["source"], "unit": "GB/s",
                 "frac": round(a / pk["hbm_gbs"], 4), "frac_of_8tbs_nominal": round(a / 8000.0, 4),
-                "traffic": None}
+                "traffic": measured_traffic(),
+                "unit_of_launch": "the four projection launches of one layer (qkv, o, gate||up, down) at n_tok=4",
+                "algorithmic_bytes": mv["4"]["all"]["bytes"]}
 
     # end to end through the public API with host buffers: pinned H2D of the
     # step's rows, the step, D2H of its output rows

@@ -42,8 +42,8 @@ cudaError_t launch_quantize(const float* x, int T, int K, int64_t ldx, int8_t* q
 
 // RMSNorm of one row per CTA (512 threads), then q8_0 quantization of the
 // normalised row.  Warp w owns the 32-value blocks b = w, w + 16, ... and
-// lane l element 32b + l of each; the row is read once (all loads issued
-// together) and kept in registers.  Sum of squares: each thread adds its
+// lane l element 32b + l of each; the row and its gamma are read once (all
+// loads issued together) and kept in registers.  Sum of squares: each thread adds its
 // elements' squares with fma in ascending b; warp partials by butterfly;
 // thread 0 adds the 16 warp sums in warp order.  r = 1 / sqrt(ss / H + eps)
 // with IEEE division and square root.  The order depends on H only.
@@ -64,13 +64,14 @@ rmsnorm_quant_kernel(const float* __restrict__ x, int H, const float* __restrict
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float* xr = x + (size_t)t * H;
     const int nb = H >> 5;
-    float v[kNormMaxPerThread];
+    float v[kNormMaxPerThread], gv[kNormMaxPerThread];
     float ss = 0.0f;
     if (REG) {
 #pragma unroll
         for (int k = 0; k < kNormMaxPerThread; ++k) {
             const int b = warp + NW * k;
             v[k] = b < nb ? xr[b * 32 + lane] : 0.0f;
+            gv[k] = b < nb ? gamma[b * 32 + lane] : 0.0f;
         }
 #pragma unroll
         for (int k = 0; k < kNormMaxPerThread; ++k)
@@ -97,7 +98,7 @@ rmsnorm_quant_kernel(const float* __restrict__ x, int H, const float* __restrict
         for (int b = warp + NW * k; b < nb; b += (REG ? nb : NW)) {
             const int i = b * 32 + lane;
             const float e = REG ? v[k] : xr[i];
-            const float vn = __fmul_rn(__fmul_rn(e, r), gamma[i]);
+            const float vn = __fmul_rn(__fmul_rn(e, r), REG ? gv[k] : gamma[i]);
             xn[(size_t)t * H + i] = vn;
             float dd;
             const int code = q8_quantize_lane(vn, &dd);

@@ -3,6 +3,7 @@
   python -m invariant_sequence_decode_gb300.kernel_bench matvec --N 34816 --K 5120 --T 4
   python -m invariant_sequence_decode_gb300.kernel_bench attn --lens 2051,2051,2051,2051 --hq 40 --hkv 8
   python -m invariant_sequence_decode_gb300.kernel_bench step --nseq 4
+  python -m invariant_sequence_decode_gb300.kernel_bench layer --T 4
 
 Prints one JSON line per case with the mean launch time and the algorithmic
 GB/s (weights N*K*34/32 + activations + outputs for the matvec; K/V bytes
@@ -55,7 +56,7 @@ def main(argv=None):
     from invariant_sequence_decode_gb300 import build, workloads as wl
 
     ap = argparse.ArgumentParser()
-    ap.add_argument("kernel", choices=["matvec", "attn", "step"])
+    ap.add_argument("kernel", choices=["matvec", "attn", "step", "layer"])
     ap.add_argument("--N", type=int, default=34816)
     ap.add_argument("--K", type=int, default=5120)
     ap.add_argument("--T", default="4")
@@ -86,6 +87,25 @@ def main(argv=None):
             m = statistics.mean(ms)
             print(json.dumps({"kernel": "q8_matvec", "N": a.N, "K": a.K, "T": T, "us_mean": round(m * 1e3, 2),
                               "us_min": round(min(ms) * 1e3, 2), "gbps": round(b / m / 1e6, 1)}))
+    elif a.kernel == "layer":
+        # the four q8_0 projections of the 27B-shaped layer (qkv, o, gate||up, down)
+        d = wl.LAYER27B
+        shapes = [((d.n_q_heads + 2 * d.n_kv_heads) * d.head_dim, d.hidden), (d.hidden, d.n_q_heads * d.head_dim),
+                  (2 * d.ffn, d.hidden), (d.hidden, d.ffn)]
+        mats = [tuple(cu(m) for m in wl.q8_weights(1, wl.tid(wl.W_MAT, 8 + i), N, K)) for i, (N, K) in enumerate(shapes)]
+        for T in [int(t) for t in a.T.split(",")]:
+            tot_b, tot_ms = 0, 0.0
+            for (N, K), (W, D) in zip(shapes, mats):
+                aq, ad = luce.luce_q8_quantize_act(cu(wl.acts(0, T, K)))
+                y = torch.empty((T, N), dtype=torch.float32, device="cuda")
+                fn = lambda: luce.luce_q8_matvec_batch(W, D, aq, ad, y)
+                for _ in range(a.warmup):
+                    fn()
+                m = statistics.mean(time_launches(torch, fn, flush, a.reps))
+                tot_b += N * K * 34 // 32 + T * K + T * (K // 32) * 4 + T * N * 4
+                tot_ms += m
+            print(json.dumps({"kernel": "q8_matvec x4 (27B layer)", "T": T, "us_sum": round(tot_ms * 1e3, 2),
+                              "bytes": tot_b, "gbps": round(tot_b / tot_ms / 1e6, 1)}))
     elif a.kernel == "attn":
         lens = [int(x) for x in a.lens.split(",")]
         d = wl.Dims(0, a.hq, a.hkv, 128, 0)
