@@ -269,7 +269,7 @@ def cpu_baseline_oracle(wl, L_host, caches_host, x_host, n_seq: int) -> dict:
 def run_ours(args, rank: int, world: int, local_rank: int):
     import torch
     import invariant_sequence_decode_gb300 as luce
-    from invariant_sequence_decode_gb300 import build, workloads as wl
+    from invariant_sequence_decode_gb300 import build, replicas, workloads as wl
     build.build()
     luce.load_library()
     torch.cuda.set_device(local_rank)
@@ -305,15 +305,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         launches = luce.launch_count() - c0
         if dist:
             dist.barrier()
-    total_ms = sum(step_ms)
-    ms_per_step = total_ms / args.steps
-    if dist:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-        ms_per_step = total_ms / args.steps
-    rows_total = n_seq * args.steps * world
-    value = rows_total / (total_ms / 1e3)
+    agg = replicas.aggregate(sum(step_ms), n_seq * args.steps, device="cuda")
+    ms_per_step = agg["max_ms"] / args.steps
+    value = agg["rows_per_s"]
 
     # aggregate tok/s at n_seq = 1..3 and the k-solo-launch arm (untimed in the contract, reported)
     detail = {"tok_s_by_n_seq": {}, "solo_launches_tok_s": {}, "step_ms_by_n_seq": {}}
@@ -364,12 +358,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         torch.cuda.synchronize()
         if i >= args.warmup:
             e2e_ms.append((time.perf_counter() - t0) * 1e3)
-    e2e_total = sum(e2e_ms)
-    if dist:
-        t = torch.tensor([e2e_total], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_total = float(t.item())
-    e2e = {"value": n_seq * args.steps * world / (e2e_total / 1e3), "unit": "tok/s",
+    e2e = {"value": replicas.aggregate(sum(e2e_ms), n_seq * args.steps, device="cuda")["rows_per_s"], "unit": "tok/s",
            "h2d_bytes_per_step": int(xh.numel() * 4), "d2h_bytes_per_step": int(outh.numel() * 4)}
 
     cpu = None

@@ -165,9 +165,10 @@ int luce_kv_append(const float* k, const float* v, int64_t ldkv, int Hkv, int D,
  *   q   (device) fp32 [T][Hq][D] with T = max(row0 + n_q)
  *   out (device) fp32 [T][Hq][D]
  *   ws  (device) scratch of at least luce_decode_attn_workspace_size(...)
- *       bytes, 16-byte aligned; the call zeroes its first bytes itself.
- * The chunk merge is done by whichever CTA of a (row, KV head) finishes last
- * (an atomic ticket, no waiting); the merge order is the chunk order.
+ *       bytes, 16-byte aligned (the chunk partials; no initial contents).
+ * Two kernels: the chunks, then their merge, launched behind it on the same
+ * stream (it starts once every chunk is written); no kernel waits on another
+ * CTA and nothing needs zeroing between calls.
  * D == 128, Hq % Hkv == 0, Hq / Hkv <= 8, 1 <= n_seq <= LUCE_MAX_SEQ,
  * 1 <= len - n_q + 1, len <= cap, len <= LUCE_MAX_KEYS.
  */
@@ -242,7 +243,7 @@ typedef struct luce_slot {
 /* Byte offsets of the step's intermediates inside its workspace (the last
  * layer's values remain there after the call; useful for inspection). */
 typedef struct luce_step_layout {
-    size_t tickets, xn, xn_q, xn_d, qkv, q_rot, part, attn, attn_q, attn_d, x1,
+    size_t xn, xn_q, xn_d, qkv, q_rot, part, attn, attn_q, attn_d, x1,
            xn2, xn2_q, xn2_d, gu, h, h_q, h_d, xf, xf_q, xf_d, total;
 } luce_step_layout;
 

@@ -57,7 +57,7 @@ class SlotC(ctypes.Structure):
     _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("len", ctypes.c_int32), ("cap", ctypes.c_int32)]
 
 
-_LAYOUT_FIELDS = ("tickets", "xn", "xn_q", "xn_d", "qkv", "q_rot", "part", "attn", "attn_q", "attn_d", "x1",
+_LAYOUT_FIELDS = ("xn", "xn_q", "xn_d", "qkv", "q_rot", "part", "attn", "attn_q", "attn_d", "x1",
                   "xn2", "xn2_q", "xn2_d", "gu", "h", "h_q", "h_d", "xf", "xf_q", "xf_d", "total")
 
 

@@ -203,14 +203,11 @@ int luce_kv_append(const float* k, const float* v, int64_t ldkv, int Hkv, int D,
     return cuda_status(launch_kv_append(k, v, ldkv, Hkv, rows, (cudaStream_t)stream), "kv_append");
 }
 
-// Attention scratch: tickets (one int per row and KV head, at most
-// LUCE_MAX_ROWS * Hq of them) in the first bytes, then the chunk partials.
-static size_t attn_ticket_bytes(int Hq) { return align_up((size_t)LUCE_MAX_ROWS * Hq * sizeof(int), 256); }
-
+// Attention scratch: the chunk partials (o[128], m, l per chunk and head).
 size_t luce_decode_attn_workspace_size(int n_rows, int Hq, int D, int max_len)
 {
     if (n_rows < 1 || Hq < 1 || D != LUCE_HEAD_DIM || max_len < 1) return 0;
-    return attn_ticket_bytes(Hq) + attn_part_floats(n_rows * max_chunks_upto(max_len), Hq) * sizeof(float);
+    return attn_part_floats(n_rows * max_chunks_upto(max_len), Hq) * sizeof(float);
 }
 
 static void build_attn_rows(const luce_seqview* views, int n_seq, AttnRows& rows, int T)
@@ -248,14 +245,10 @@ int luce_decode_attn_multiseq(const float* q, const luce_seqview* views, int n_s
     if (rc) return rc;
     AttnRows rows{};
     build_attn_rows(views, n_seq, rows, T);
-    const size_t tb = attn_ticket_bytes(Hq);
-    const size_t need = tb + attn_part_floats(rows.total_chunks, Hq) * sizeof(float);
+    const size_t need = attn_part_floats(rows.total_chunks, Hq) * sizeof(float);
     REQUIRE(ws_bytes >= need, LUCE_ENOSPACE, "decode_attn: workspace %zu bytes < %zu needed", ws_bytes, need);
-    cudaStream_t st = (cudaStream_t)stream;
-    cudaError_t e = cudaMemsetAsync(ws, 0, (size_t)T * Hkv * sizeof(int), st);
-    if (e != cudaSuccess) return cuda_status(e, "decode_attn");
-    return cuda_status(launch_attention(q, (int64_t)Hq * D, rows, Hq, Hkv, scale, (float*)((char*)ws + tb), (int*)ws,
-                                        out, (int64_t)Hq * D, nullptr, nullptr, st),
+    return cuda_status(launch_attention(q, (int64_t)Hq * D, rows, Hq, Hkv, scale, (float*)ws, out, (int64_t)Hq * D,
+                                        nullptr, nullptr, (cudaStream_t)stream),
                        "decode_attn");
 }
 
@@ -310,8 +303,7 @@ int luce_decode_attn_multiseq_noalloc(const float* q, const luce_seqview* views,
     if (rc) return rc;
     AttnRows rows{};
     build_attn_rows(views, n_seq, rows, T);
-    const size_t tb = attn_ticket_bytes(Hq);
-    const size_t need = tb + attn_part_floats(rows.total_chunks, Hq) * sizeof(float);
+    const size_t need = attn_part_floats(rows.total_chunks, Hq) * sizeof(float);
     REQUIRE(need <= kNoAllocScratchBytes, LUCE_ENOSPACE,
             "%s: needs %zu bytes of scratch, more than the fixed %zu-byte array (fewer rows, shorter contexts or "
             "fewer heads fit)",
@@ -319,11 +311,8 @@ int luce_decode_attn_multiseq_noalloc(const float* q, const luce_seqview* views,
     void* scratch = nullptr;
     rc = noalloc_scratch(&scratch);
     if (rc) return rc;
-    cudaStream_t st = (cudaStream_t)stream;
-    cudaError_t e = cudaMemsetAsync(scratch, 0, (size_t)T * Hkv * sizeof(int), st);
-    if (e != cudaSuccess) return cuda_status(e, who);
-    return cuda_status(launch_attention(q, (int64_t)Hq * D, rows, Hq, Hkv, scale, (float*)((char*)scratch + tb),
-                                        (int*)scratch, out, (int64_t)Hq * D, nullptr, nullptr, st),
+    return cuda_status(launch_attention(q, (int64_t)Hq * D, rows, Hq, Hkv, scale, (float*)scratch, out,
+                                        (int64_t)Hq * D, nullptr, nullptr, (cudaStream_t)stream),
                        who);
 }
 
@@ -357,7 +346,6 @@ static void layout_of(const luce_model* m, int T, int max_ctx, luce_step_layout*
         o = align_up(o + bytes, 256);
         return at;
     };
-    L->tickets = take((size_t)T * Hkv * sizeof(int));
     L->xn = take(T * H * 4);
     L->xn_q = take(T * H);
     L->xn_d = take(T * H / 32 * 4);
@@ -443,7 +431,6 @@ int luce_decode_step(const luce_model* m, const luce_slot* slots, const int32_t*
     REQUIRE(ws_bytes >= L.total, LUCE_ENOSPACE, "%s: workspace %zu bytes < %zu needed", who, ws_bytes, L.total);
 
     char* wsb = (char*)ws;
-    int* tickets = (int*)(wsb + L.tickets);
     float* xn = (float*)(wsb + L.xn);
     int8_t* xn_q = (int8_t*)(wsb + L.xn_q);
     float* xn_d = (float*)(wsb + L.xn_d);
@@ -476,9 +463,7 @@ int luce_decode_step(const luce_model* m, const luce_slot* slots, const int32_t*
             }
     }
     const RopeFreq freq = rope_freq(m->rope_theta);
-    // attention tickets start at zero; every launch leaves them zero again
-    cudaError_t e = cudaMemsetAsync(tickets, 0, (size_t)T * Hkv * sizeof(int), st);
-    if (e != cudaSuccess) return cuda_status(e, who);
+    cudaError_t e = cudaSuccess;
 
     const float scale = (float)(1.0 / sqrt((double)D));
     const int64_t qkv_rows = (int64_t)(Hq + 2 * Hkv) * D;
@@ -515,7 +500,7 @@ int luce_decode_step(const luce_model* m, const luce_slot* slots, const int32_t*
                                nullptr, 0, st)))
             break;
         if ((e = launch_rope_kv(qkv, T, Hq, Hkv, pos, freq, q_rot, kv, st))) break;
-        if ((e = launch_attention(q_rot, (int64_t)Hq * D, ar, Hq, Hkv, scale, part, tickets, attn, (int64_t)Hq * D,
+        if ((e = launch_attention(q_rot, (int64_t)Hq * D, ar, Hq, Hkv, scale, part, attn, (int64_t)Hq * D,
                                   attn_q, attn_d, st)))
             break;
         if ((e = launch_matvec(w.wo_q, (const __half*)w.wo_d, H, Hq * D, attn_q, attn_d, T, x1, H, x, H, st)))

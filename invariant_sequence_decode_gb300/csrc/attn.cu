@@ -7,25 +7,37 @@
 //
 // A row's keys are cut into chunks of CH keys, CH = attn_chunk_keys(row's key
 // count) (128 up to 16,384 keys, else 256: small contexts get smaller chunks
-// so the GPU has enough independent work).  One CTA of 256 threads per (row, chunk, KV
-// head g) serves all Hq/Hkv query heads of g, so each K/V byte is read once:
-//   scores   P = 512/CH threads per key pair (j, j + CH/2); thread part p
-//            covers dims [p*128/P, (p+1)*128/P) of both keys: fma over its
-//            dims ascending, then the P partial dots of a key are summed by an
-//            xor butterfly (1, 2, ...); s_h = scale * dot;
-//   softmax  warp h owns head h: m = max_j s_h, p_j = exp(s_h - m),
-//            l = sum p_j (lane-serial over j = lane + 32i, then butterfly);
-//   values   warp w owns keys w, w+8, ... and lane l dims 4l..4l+3:
-//            o_h += p_hj * v_j (fma, keys ascending); the 8 warp partials are
-//            added in warp order.
+// so the GPU has enough independent work).  One CTA of 256 threads (8 warps)
+// per (row, chunk, KV head g) serves all GQ = Hq/Hkv query heads of g, so each
+// K/V byte is read once.  Both contractions run on the tensor cores (mma
+// m16n8k16: f16 operands, fp32 accumulation).  f16 holds K and V exactly; q
+// and the probabilities are fp32, so each is split into two f16 parts,
+// x = hi + lo with hi = f16(x) and lo = f16(x - hi), and both parts are
+// multiplied in.  Keys are taken 128 at a time (a tile):
+//   scores   warp w owns keys 16w..16w+15 of the tile and loads their K rows
+//            straight into its A fragments: lane quarter t holds dims
+//            32t..32t+31, and step s = 0..7 contracts dims 32t+4s..32t+4s+3
+//            of every quarter t (q is laid out the same way); per step the
+//            q_hi, then the q_lo product is accumulated; s_h = scale * dot;
+//   softmax  warp h owns head h: m = max_j s_hj, p_hj = exp(s_hj - m),
+//            l = sum p_hj (lane-serial over j = lane + 32i, then butterfly);
+//   values   the tile's V rows are staged in shared memory by cp.async
+//            (16-byte pieces, piece c of key j at c ^ (j & 7), so ldmatrix
+//            reads them without bank conflicts) while the scores and the
+//            softmax run; warp w owns dims 16w..16w+15 and, for each step of
+//            16 keys in key order, accumulates p_hi.V, then p_lo.V.
 //   -> scratch (o_h[128], m_h, l_h) for the chunk.
-// The CTA that finishes last for its (row, g) (an atomic ticket; nobody
-// waits) merges the row's chunks in chunk order:
+// A second kernel, launched behind the first with programmatic dependent
+// launch (its wait returns once every chunk is written), merges each (row,
+// query head) over the row's chunks, one CTA per pair and one thread per dim:
 //   M = max_c m_c, w_c = e^(m_c - M), L = sum_c l_c w_c, O = sum_c o_c w_c,
-//   out = O / L  (the sums sequential over c),
+//   out = O / L  (O sequential over c; L lane-serial over c = lane + 32i,
+//   then a butterfly),
 // and optionally quantizes out to q8_0 blocks (the Wo projection's input).
 // Every chunking and reduction order depends only on the row's own key
 // count, never on the other rows, on which CTA merges or on the grid.
+// The split of q assumes |q| < 65504 (the f16 range); larger entries make
+// the row's scores non-finite.
 #include <math.h>
 
 #include "common.cuh"
@@ -34,176 +46,84 @@
 namespace luce {
 
 constexpr int kPartStride = 132;  // o[128], m, l, 2 pad floats per (chunk, head)
+constexpr int kAttnThreads = 256;
+constexpr int kTileKeys = 128;    // keys staged in shared memory at a time
+// Row stride of the probabilities: 264 = 8 (mod 32) words, so the value loads
+// of 4 heads x 4 key pairs in one half-warp hit 16 distinct bank pairs.
+constexpr int kPStride = kAttnChunk + 8;
 
 size_t attn_part_floats(int total_chunks, int Hq) { return (size_t)total_chunks * Hq * kPartStride; }
 
 int attn_chunk_keys(int len) { return len <= 16384 ? 128 : 256; }
 
-// q row of head h in shared memory: dim d at qpad(d) = d + 4*(d/32), so the
-// up-to-4 threads of a key (dims 32 apart) hit different banks and four
-// consecutive dims are one aligned 16-byte load.
-constexpr int kQStride = kHeadDim + 16;
-__device__ __forceinline__ int qpad(int d) { return d + 4 * (d >> 5); }
-
 template <int GQ>
 struct AttnSmem {
-    float q[GQ][kQStride];
-    float p[GQ][kAttnChunk];
-    float red[8][GQ][kHeadDim];  // also the merge's scratch
-    int last;
+    __half vt[kTileKeys * kHeadDim];  // staged V tile (32 KB)
+    uint4 qf[8][32];                  // q as B fragments per step and lane: hi b0, hi b1, lo b0, lo b1
+    float p[GQ][kPStride];            // scores, then probabilities, of the chunk
 };
 
-// Scores, softmax statistics and p.V of one chunk of CH keys.
-template <int GQ, int CH>
-__device__ __forceinline__ void attn_chunk(AttnSmem<GQ>& sm, const __half* kbase, const __half* vbase,
-                                           int64_t tok_stride, int nvalid, float scale, float* pout)
+// Offset (in halves) of 16-byte piece c (8 dims) of key j in a staged tile.
+__device__ __forceinline__ int tile_off(int j, int c) { return j * kHeadDim + ((c ^ (j & 7)) << 3); }
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes)
 {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
-    // ---- scores: each thread computes 2 keys (j, j + CH/2) over DPT dims, so
-    // every q load from shared memory serves 8 fma
-    {
-        constexpr int PARTS = 512 / CH;       // threads per key pair
-        constexpr int DPT2 = kHeadDim / PARTS;
-        const int j = tid / PARTS, part = tid % PARTS;
-        float dot0[GQ], dot1[GQ];
+// Stage keys [j0, j0 + 128) of a chunk (rows tok_stride halves apart from
+// src) in a tile; keys at or past nvalid are zero-filled without a read.
+__device__ __forceinline__ void stage_tile(__half* dst, const __half* src, int64_t tok_stride, int j0, int nvalid)
+{
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
 #pragma unroll
-        for (int h = 0; h < GQ; ++h) dot0[h] = dot1[h] = 0.0f;
-        const bool v0 = j < nvalid, v1 = j + CH / 2 < nvalid;
-        const int4* kp0 = reinterpret_cast<const int4*>(kbase + (int64_t)j * tok_stride + part * DPT2);
-        const int4* kp1 = reinterpret_cast<const int4*>(kbase + (int64_t)(j + CH / 2) * tok_stride + part * DPT2);
-        int4 ka[DPT2 / 8], kc[DPT2 / 8];
-#pragma unroll
-        for (int i = 0; i < DPT2 / 8; ++i) {
-            ka[i] = v0 ? __ldg(kp0 + i) : make_int4(0, 0, 0, 0);
-            kc[i] = v1 ? __ldg(kp1 + i) : make_int4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int i = 0; i < DPT2 / 8; ++i) {
-            const __half2* ha = reinterpret_cast<const __half2*>(&ka[i]);
-            const __half2* hc = reinterpret_cast<const __half2*>(&kc[i]);
-#pragma unroll
-            for (int e = 0; e < 4; e += 2) {
-                const float2 a01 = __half22float2(ha[e]), a23 = __half22float2(ha[e + 1]);
-                const float2 c01 = __half22float2(hc[e]), c23 = __half22float2(hc[e + 1]);
-                const int dq = qpad(part * DPT2 + i * 8 + e * 2);
-#pragma unroll
-                for (int h = 0; h < GQ; ++h) {
-                    const float4 qv = *reinterpret_cast<const float4*>(&sm.q[h][dq]);
-                    dot0[h] = __fmaf_rn(qv.x, a01.x, dot0[h]);
-                    dot0[h] = __fmaf_rn(qv.y, a01.y, dot0[h]);
-                    dot0[h] = __fmaf_rn(qv.z, a23.x, dot0[h]);
-                    dot0[h] = __fmaf_rn(qv.w, a23.y, dot0[h]);
-                    dot1[h] = __fmaf_rn(qv.x, c01.x, dot1[h]);
-                    dot1[h] = __fmaf_rn(qv.y, c01.y, dot1[h]);
-                    dot1[h] = __fmaf_rn(qv.z, c23.x, dot1[h]);
-                    dot1[h] = __fmaf_rn(qv.w, c23.y, dot1[h]);
-                }
-            }
-        }
-#pragma unroll
-        for (int h = 0; h < GQ; ++h) {
-#pragma unroll
-            for (int off = 1; off < PARTS; off <<= 1) {
-                dot0[h] = __fadd_rn(dot0[h], __shfl_xor_sync(0xffffffffu, dot0[h], off));
-                dot1[h] = __fadd_rn(dot1[h], __shfl_xor_sync(0xffffffffu, dot1[h], off));
-            }
-        }
-        if (part == 0) {
-#pragma unroll
-            for (int h = 0; h < GQ; ++h) {
-                sm.p[h][j] = v0 ? __fmul_rn(dot0[h], scale) : -INFINITY;
-                sm.p[h][j + CH / 2] = v1 ? __fmul_rn(dot1[h], scale) : -INFINITY;
-            }
-        }
-    }
-    __syncthreads();
-
-    // ---- chunk softmax statistics, warp h per head
-    for (int h = warp; h < GQ; h += 8) {
-        float sv[CH / 32];
-        float m = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < CH / 32; ++i) {
-            sv[i] = sm.p[h][lane + 32 * i];
-            m = fmaxf(m, sv[i]);
-        }
-        m = warp_max(m);
-        float l = 0.0f;
-#pragma unroll
-        for (int i = 0; i < CH / 32; ++i) {
-            const int j = lane + 32 * i;
-            const float p = (j < nvalid) ? expf(__fsub_rn(sv[i], m)) : 0.0f;
-            sm.p[h][j] = p;
-            l = __fadd_rn(l, p);
-        }
-        l = warp_sum_butterfly(l);
-        if (lane == 0) {
-            pout[(size_t)h * kPartStride + 128] = m;
-            pout[(size_t)h * kPartStride + 129] = l;
-        }
-    }
-    __syncthreads();
-
-    // ---- p . V  (keys w, w+8, ...; all of this warp's loads issued first)
-    {
-        float o[GQ][4];
-#pragma unroll
-        for (int h = 0; h < GQ; ++h)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) o[h][e] = 0.0f;
-        const __half* vl = vbase + lane * 4;
-        constexpr int KPW = CH / 8;  // keys per warp
-        constexpr int UB = KPW < 8 ? KPW : 8;
-#pragma unroll 1
-        for (int u0 = 0; u0 < KPW; u0 += UB) {
-            uint2 raw[UB];
-#pragma unroll
-            for (int u = 0; u < UB; ++u) {
-                const int j = warp + 8 * (u0 + u);
-                if (j < nvalid) raw[u] = __ldg(reinterpret_cast<const uint2*>(vl + (int64_t)j * tok_stride));
-            }
-#pragma unroll
-            for (int u = 0; u < UB; ++u) {
-                const int j = warp + 8 * (u0 + u);
-                if (j < nvalid) {
-                    const float2 v01 = __half22float2(*reinterpret_cast<const __half2*>(&raw[u].x));
-                    const float2 v23 = __half22float2(*reinterpret_cast<const __half2*>(&raw[u].y));
-#pragma unroll
-                    for (int h = 0; h < GQ; ++h) {
-                        const float p = sm.p[h][j];
-                        o[h][0] = __fmaf_rn(p, v01.x, o[h][0]);
-                        o[h][1] = __fmaf_rn(p, v01.y, o[h][1]);
-                        o[h][2] = __fmaf_rn(p, v23.x, o[h][2]);
-                        o[h][3] = __fmaf_rn(p, v23.y, o[h][3]);
-                    }
-                }
-            }
-        }
-#pragma unroll
-        for (int h = 0; h < GQ; ++h)
-            *reinterpret_cast<float4*>(&sm.red[warp][h][lane * 4]) = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
-    }
-    __syncthreads();
-    for (int i = tid; i < GQ * kHeadDim; i += 256) {
-        const int h = i / kHeadDim, d = i % kHeadDim;
-        float s = sm.red[0][h][d];
-#pragma unroll
-        for (int w = 1; w < 8; ++w) s = __fadd_rn(s, sm.red[w][h][d]);
-        pout[(size_t)h * kPartStride + d] = s;
+    for (int i = threadIdx.x; i < kTileKeys * 16; i += kAttnThreads) {
+        const int j = i >> 4, c = i & 15;
+        const bool ok = j0 + j < nvalid;
+        cp_async16(d + 2 * tile_off(j, c), ok ? src + (int64_t)(j0 + j) * tok_stride + c * 8 : src, ok ? 16 : 0);
     }
 }
 
-template <int GQ>
-__global__ void __launch_bounds__(256)
-attn_kernel(const float* __restrict__ q, int64_t ldq, AttnRows rows, int Hq, int Hkv, float scale,
-            float* __restrict__ part, int* __restrict__ tickets, float* __restrict__ out, int64_t ldo,
-            int8_t* __restrict__ out_q, float* __restrict__ out_d)
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t a, uint32_t (&r)[4])
 {
-    __shared__ __align__(16) AttnSmem<GQ> sm;  // q rows stay 16-byte aligned: kQStride % 4 == 0
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(a));
+}
+
+// c += A(16x16, row-major fragment) * B(16x8, column fragment b0, b1)
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%0,%1,%2,%3};"
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two fp32 values as f16 pairs: x = hi + lo, hi = f16(x), lo = f16(x - hi);
+// the first value in the low half of each word.
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo)
+{
+    const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
+    const __half l0 = __float2half_rn(__fsub_rn(x0, __half2float(h0)));
+    const __half l1 = __float2half_rn(__fsub_rn(x1, __half2float(h1)));
+    hi = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+    lo = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
+}
+
+template <int GQ>
+__global__ void __launch_bounds__(kAttnThreads)
+attn_kernel(const float* __restrict__ q, int64_t ldq, AttnRows rows, int Hq, int Hkv, float scale,
+            float* __restrict__ part)
+{
+    __shared__ __align__(128) AttnSmem<GQ> sm;
     pdl_trigger();
     const int chunk = blockIdx.x, g = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int gr = lane >> 2, tq = lane & 3;  // mma fragment: row group, thread in group
+    const int mi = lane >> 3, mr = lane & 7;  // ldmatrix: the matrix and row this lane addresses
 
     int r = 0;
 #pragma unroll 1
@@ -212,9 +132,9 @@ attn_kernel(const float* __restrict__ q, int64_t ldq, AttnRows rows, int Hq, int
     const AttnRow row = rows.row[r];
     const int CH = row.chunk;
     const int c = chunk - row.chunk0;
-    const int nch = (row.len + CH - 1) / CH;
     const int key0 = c * CH;
     const int nvalid = min(CH, row.len - key0);
+    const int ntile = (nvalid + kTileKeys - 1) / kTileKeys;  // tiles of this chunk: 1 or 2
     const int h0 = g * GQ;
     const __half* kbase = row.k + g * row.head_stride + (int64_t)key0 * row.tok_stride;
     const __half* vbase = row.v + g * row.head_stride + (int64_t)key0 * row.tok_stride;
@@ -226,95 +146,238 @@ attn_kernel(const float* __restrict__ q, int64_t ldq, AttnRows rows, int Hq, int
         prefetch_l2(vbase, span);
     }
     pdl_wait();
-    for (int i = tid; i < GQ * kHeadDim; i += 256)
-        sm.q[i / kHeadDim][qpad(i % kHeadDim)] = q[(size_t)r * ldq + (size_t)(h0 + i / kHeadDim) * kHeadDim + i % kHeadDim];
+    stage_tile(sm.vt, vbase, row.tok_stride, 0, nvalid);
+    cp_async_commit();
+
+    // K rows of keys j0 + 16w + gr (ka) and + 8 (kb): dims 32tq .. 32tq + 31,
+    // read once with L1 bypassed: whole 32-byte sectors per load when the
+    // row's rows start on 32-byte boundaries, else 16-byte loads
+    const bool k32 = ((reinterpret_cast<uintptr_t>(kbase) | (uintptr_t)(row.tok_stride * 2)) & 31) == 0;
+    uint32_t ka[16], kb[16];
+    auto load_row = [&](const __half* p, bool ok, uint32_t (&w)[16]) {
+        if (!ok) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) w[e] = 0u;
+        } else if (k32) {
+            ld_stream_v8(p, *reinterpret_cast<uint32_t(*)[8]>(&w[0]));
+            ld_stream_v8(p + 16, *reinterpret_cast<uint32_t(*)[8]>(&w[8]));
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int4 v = ld_stream_v4(p + 8 * i);
+                w[4 * i] = (uint32_t)v.x;
+                w[4 * i + 1] = (uint32_t)v.y;
+                w[4 * i + 2] = (uint32_t)v.z;
+                w[4 * i + 3] = (uint32_t)v.w;
+            }
+        }
+    };
+    auto load_k = [&](int j0) {
+        const int ja = j0 + 16 * warp + gr, jb = ja + 8;
+        load_row(kbase + (int64_t)ja * row.tok_stride + 32 * tq, ja < nvalid, ka);
+        load_row(kbase + (int64_t)jb * row.tok_stride + 32 * tq, jb < nvalid, kb);
+    };
+    load_k(0);
+
+    // q as B fragments: step s, lane (head n = lane / 4, t = lane % 4) holds
+    // q[n][32t + 4s .. 32t + 4s + 3]; heads past the group are zero
+    {
+        const int s = tid >> 5, n = lane >> 2, t = lane & 3;
+        float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (n < GQ)
+            v = *reinterpret_cast<const float4*>(q + (size_t)r * ldq + (size_t)(h0 + n) * kHeadDim + 32 * t + 4 * s);
+        uint4 f;
+        split2(v.x, v.y, f.x, f.z);
+        split2(v.z, v.w, f.y, f.w);
+        sm.qf[s][lane] = f;
+    }
     __syncthreads();
 
+    // ---- scores of keys j0 + 16w .. j0 + 16w + 15
+    auto scores = [&](int j0) {
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            const uint32_t a[4] = {ka[2 * s], kb[2 * s], ka[2 * s + 1], kb[2 * s + 1]};
+            const uint4 f = sm.qf[s][lane];
+            mma16816(acc, a, f.x, f.y);
+            mma16816(acc, a, f.z, f.w);
+        }
+        // acc: keys ja (c0, c1) and ja + 8 (c2, c3); heads 2tq (c0, c2) and 2tq + 1
+        const int ja = j0 + 16 * warp + gr, jb = ja + 8, h = 2 * tq;
+        if (h < GQ) {
+            sm.p[h][ja] = ja < nvalid ? __fmul_rn(acc[0], scale) : -INFINITY;
+            sm.p[h][jb] = jb < nvalid ? __fmul_rn(acc[2], scale) : -INFINITY;
+        }
+        if (h + 1 < GQ) {
+            sm.p[h + 1][ja] = ja < nvalid ? __fmul_rn(acc[1], scale) : -INFINITY;
+            sm.p[h + 1][jb] = jb < nvalid ? __fmul_rn(acc[3], scale) : -INFINITY;
+        }
+    };
+    scores(0);
+    if (ntile == 2) {
+        load_k(kTileKeys);
+        scores(kTileKeys);
+    }
+    __syncthreads();
+
+    // ---- chunk softmax statistics, warp h per head
     float* pout = part + ((size_t)chunk * Hq + h0) * kPartStride;
-    if (CH == 64)
-        attn_chunk<GQ, 64>(sm, kbase, vbase, row.tok_stride, nvalid, scale, pout);
-    else if (CH == 128)
-        attn_chunk<GQ, 128>(sm, kbase, vbase, row.tok_stride, nvalid, scale, pout);
-    else
-        attn_chunk<GQ, 256>(sm, kbase, vbase, row.tok_stride, nvalid, scale, pout);
-
-    // ---- the last CTA of (row, g) merges the row's chunks
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) sm.last = (atomicAdd(&tickets[r * Hkv + g], 1) == nch - 1);
-    __syncthreads();
-    if (!sm.last) return;
-    __threadfence();
-    const float* base = part + ((size_t)row.chunk0 * Hq + h0) * kPartStride;
-    const size_t cstride = (size_t)Hq * kPartStride;
-    // chunk weights w[h][c] = e^(m_c - M_h), the chunk sums l[h][c] and L_h,
-    // in the reduction scratch; every load of the chunk statistics is issued
-    // lane-parallel, only the sum over c is sequential (in chunk order).
-    float* wts = &sm.red[0][0][0];                // [GQ][nch]
-    float* lsum = &sm.red[0][0][0] + GQ * nch;    // [GQ][nch]
-    float* Ls = &sm.red[0][0][0] + 2 * GQ * nch;  // [GQ]
     for (int h = warp; h < GQ; h += 8) {
-        const float* bh = base + (size_t)h * kPartStride;
+        float sv[kAttnChunk / 32];
+        float m = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < kAttnChunk / 32; ++i) {
+            const int j = lane + 32 * i;
+            sv[i] = (32 * i < CH && j < nvalid) ? sm.p[h][j] : -INFINITY;
+            m = fmaxf(m, sv[i]);
+        }
+        m = warp_max(m);
+        float l = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kAttnChunk / 32; ++i) {
+            const int j = lane + 32 * i;
+            if (32 * i < CH) {
+                const float p = j < nvalid ? expf(__fsub_rn(sv[i], m)) : 0.0f;
+                sm.p[h][j] = p;
+                l = __fadd_rn(l, p);
+            }
+        }
+        l = warp_sum_butterfly(l);
+        if (lane == 0) {
+            pout[(size_t)h * kPartStride + 128] = m;
+            pout[(size_t)h * kPartStride + 129] = l;
+        }
+    }
+    cp_async_wait_all();
+    __syncthreads();
+
+    // ---- p . V for dims 16w .. 16w + 15, 16 keys per step
+    float o[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
+    const uint32_t vt = (uint32_t)__cvta_generic_to_shared(sm.vt);
+    auto values = [&](int j0) {
+#pragma unroll 2
+        for (int ks = 0; ks < kTileKeys / 16; ++ks) {
+            float2 x = make_float2(0.0f, 0.0f), y = make_float2(0.0f, 0.0f);
+            if (gr < GQ) {
+                x = *reinterpret_cast<const float2*>(&sm.p[gr][j0 + 16 * ks + 2 * tq]);
+                y = *reinterpret_cast<const float2*>(&sm.p[gr][j0 + 16 * ks + 2 * tq + 8]);
+            }
+            uint32_t ah[4], al[4];
+            split2(x.x, x.y, ah[0], al[0]);
+            split2(y.x, y.y, ah[2], al[2]);
+            ah[1] = ah[3] = al[1] = al[3] = 0u;  // rows 8..15 of A: no heads
+            uint32_t b[4];
+            ldsm_x4_trans(vt + 2 * tile_off(16 * ks + 8 * (mi & 1) + mr, 2 * warp + (mi >> 1)), b);
+            mma16816(o[0], ah, b[0], b[1]);
+            mma16816(o[0], al, b[0], b[1]);
+            mma16816(o[1], ah, b[2], b[3]);
+            mma16816(o[1], al, b[2], b[3]);
+        }
+    };
+    values(0);
+    if (ntile == 2) {
+        __syncthreads();  // every warp is done with the first V tile
+        stage_tile(sm.vt, vbase, row.tok_stride, kTileKeys, nvalid);
+        cp_async_commit();
+        cp_async_wait_all();
+        __syncthreads();
+        values(kTileKeys);
+    }
+    if (gr < GQ) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+            *reinterpret_cast<float2*>(pout + (size_t)gr * kPartStride + 16 * warp + 8 * nt + 2 * tq) =
+                make_float2(o[nt][0], o[nt][1]);
+    }
+}
+
+// Merge of one (row, query head h) over the row's chunks, one thread per dim
+// d (CTA of 128), after the chunk kernel has completed:
+//   M = max_c m_c, w_c = e^(m_c - M), L = sum_c l_c w_c, O_d = sum_c o_c,d w_c,
+//   out_d = O_d / L;  L lane-serial over c = lane + 32i then a butterfly, O_d
+//   sequential over c; optionally q8_0 blocks of out (one warp per block).
+__global__ void __launch_bounds__(kHeadDim)
+attn_merge_kernel(AttnRows rows, int Hq, const float* __restrict__ part, float* __restrict__ out, int64_t ldo,
+                  int8_t* __restrict__ out_q, float* __restrict__ out_d)
+{
+    __shared__ float wts[kAttnMaxChunksPerRow];
+    __shared__ float lsum[kAttnMaxChunksPerRow];
+    __shared__ float Lsh;
+    pdl_trigger();
+    const int h = blockIdx.x, r = blockIdx.y;
+    const int d = threadIdx.x, lane = d & 31;
+    const AttnRow row = rows.row[r];
+    const int nch = (row.len + row.chunk - 1) / row.chunk;
+    const size_t cstride = (size_t)Hq * kPartStride;
+    const float* bh = part + ((size_t)row.chunk0 * Hq + h) * kPartStride;
+    pdl_wait();
+    float ov[16];  // the first 16 chunk outputs, loaded while the statistics are gathered
+#pragma unroll
+    for (int u = 0; u < 16; ++u) ov[u] = u < nch ? __ldcg(bh + u * cstride + d) : 0.0f;
+    if (d < 32) {
         float M = -INFINITY;
         for (int cc = lane; cc < nch; cc += 32) {
             const float m = __ldcg(bh + cc * cstride + 128);
-            wts[h * nch + cc] = m;
-            lsum[h * nch + cc] = __ldcg(bh + cc * cstride + 129);
+            wts[cc] = m;
+            lsum[cc] = __ldcg(bh + cc * cstride + 129);
             M = fmaxf(M, m);
         }
         M = warp_max(M);
-        for (int cc = lane; cc < nch; cc += 32) wts[h * nch + cc] = expf(__fsub_rn(wts[h * nch + cc], M));
-        __syncwarp();
-        if (lane == 0) {
-            float L = 0.0f;
-            for (int cc = 0; cc < nch; ++cc) L = __fmaf_rn(lsum[h * nch + cc], wts[h * nch + cc], L);
-            Ls[h] = L;
+        float L = 0.0f;
+        for (int cc = lane; cc < nch; cc += 32) {
+            const float w = expf(__fsub_rn(wts[cc], M));
+            wts[cc] = w;
+            L = __fmaf_rn(lsum[cc], w, L);
         }
+        L = warp_sum_butterfly(L);
+        if (lane == 0) Lsh = L;
     }
     __syncthreads();
-    for (int blk = warp; blk < GQ * (kHeadDim / 32); blk += 8) {
-        const int h = blk / (kHeadDim / 32), d = (blk % (kHeadDim / 32)) * 32 + lane;
-        const float* bh = base + (size_t)h * kPartStride + d;
-        const float* wh = wts + h * nch;
-        float O = 0.0f;
-        int cc = 0;
-        for (; cc + 16 <= nch; cc += 16) {
-            float ov[16];
+    float O = 0.0f;
 #pragma unroll
-            for (int u = 0; u < 16; ++u) ov[u] = __ldcg(bh + (cc + u) * cstride);
+    for (int u = 0; u < 16; ++u)
+        if (u < nch) O = __fmaf_rn(ov[u], wts[u], O);
+    int cc = 16;
+    for (; cc + 16 <= nch; cc += 16) {
+        float ob[16];
 #pragma unroll
-            for (int u = 0; u < 16; ++u) O = __fmaf_rn(ov[u], wh[cc + u], O);
-        }
-        for (; cc < nch; ++cc) O = __fmaf_rn(__ldcg(bh + cc * cstride), wh[cc], O);
-        const float val = __fdiv_rn(O, Ls[h]);
-        const size_t oi = (size_t)r * ldo + (size_t)(h0 + h) * kHeadDim + d;
-        out[oi] = val;
-        if (out_q) {
-            float dd;
-            const int code = q8_quantize_lane(val, &dd);
-            out_q[oi] = (int8_t)code;
-            if (lane == 0) out_d[oi / 32] = dd;
-        }
+        for (int u = 0; u < 16; ++u) ob[u] = __ldcg(bh + (cc + u) * cstride + d);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) O = __fmaf_rn(ob[u], wts[cc + u], O);
     }
-    if (tid == 0) tickets[r * Hkv + g] = 0;  // ready for the next launch
+    for (; cc < nch; ++cc) O = __fmaf_rn(__ldcg(bh + cc * cstride + d), wts[cc], O);
+    const float val = __fdiv_rn(O, Lsh);
+    const size_t oi = (size_t)r * ldo + (size_t)h * kHeadDim + d;
+    out[oi] = val;
+    if (out_q) {
+        float dd;
+        const int code = q8_quantize_lane(val, &dd);
+        out_q[oi] = (int8_t)code;
+        if (lane == 0) out_d[oi / 32] = dd;
+    }
 }
 
 template <int GQ>
-static void launch_g(const float* q, int64_t ldq, const AttnRows& rows, int Hq, int Hkv, float scale, float* part,
-                     int* tickets, float* out, int64_t ldo, int8_t* out_q, float* out_d, cudaStream_t s)
+static cudaError_t launch_g(const float* q, int64_t ldq, const AttnRows& rows, int Hq, int Hkv, float scale,
+                            float* part, float* out, int64_t ldo, int8_t* out_q, float* out_d, cudaStream_t s)
 {
-    launch_pdl(attn_kernel<GQ>, dim3(rows.total_chunks, Hkv), dim3(256), s, q, ldq, rows, Hq, Hkv, scale, part, tickets,
-               out, ldo, out_q, out_d);
+    cudaError_t e = launch_pdl(attn_kernel<GQ>, dim3(rows.total_chunks, Hkv), dim3(kAttnThreads), s, q, ldq, rows,
+                               Hq, Hkv, scale, part);
     count_launches(1);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(attn_merge_kernel, dim3(Hq, rows.n_rows), dim3(kHeadDim), s, rows, Hq, (const float*)part, out,
+                   ldo, out_q, out_d);
+    count_launches(1);
+    return e;
 }
 
 cudaError_t launch_attention(const float* q, int64_t ldq, const AttnRows& rows, int Hq, int Hkv, float scale,
-                             float* part, int* tickets, float* out, int64_t ldo, int8_t* out_q, float* out_d,
-                             cudaStream_t s)
+                             float* part, float* out, int64_t ldo, int8_t* out_q, float* out_d, cudaStream_t s)
 {
     switch (Hq / Hkv) {
 #define LUCE_AT(G) \
-    case G: launch_g<G>(q, ldq, rows, Hq, Hkv, scale, part, tickets, out, ldo, out_q, out_d, s); break;
+    case G: return launch_g<G>(q, ldq, rows, Hq, Hkv, scale, part, out, ldo, out_q, out_d, s);
         LUCE_AT(1)
         LUCE_AT(2)
         LUCE_AT(3)
@@ -326,7 +389,6 @@ cudaError_t launch_attention(const float* q, int64_t ldq, const AttnRows& rows, 
 #undef LUCE_AT
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 }  // namespace luce

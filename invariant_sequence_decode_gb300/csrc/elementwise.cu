@@ -7,8 +7,12 @@
 // quantize, SwiGLU + quantize) call the very same per-lane routine as the
 // standalone quantizer, on the same fp32 value they also store, so their
 // codes equal a standalone quantization of their fp32 output bit for bit.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "kernels.h"
+
+namespace cg = cooperative_groups;
 
 namespace luce {
 
@@ -40,15 +44,20 @@ cudaError_t launch_quantize(const float* x, int T, int K, int64_t ldx, int8_t* q
     return e;
 }
 
-// RMSNorm of one row per CTA (512 threads), then q8_0 quantization of the
-// normalised row.  Warp w owns the 32-value blocks b = w, w + 16, ... and
-// lane l element 32b + l of each; the row and its gamma are read once (all
-// loads issued together) and kept in registers.  Sum of squares: each thread adds its
-// elements' squares with fma in ascending b; warp partials by butterfly;
-// thread 0 adds the 16 warp sums in warp order.  r = 1 / sqrt(ss / H + eps)
-// with IEEE division and square root.  The order depends on H only.
-constexpr int kNormThreads = 512;
-constexpr int kNormMaxPerThread = 16;  // H <= 512 * 16 = 8192 on the register path
+// RMSNorm of one row by a cluster of kNormCtas CTAs (128 threads each), then
+// q8_0 quantization of the normalised row.  CTA c of the row owns the
+// 32-value blocks [c*bpc, (c+1)*bpc), bpc = ceil((H/32) / kNormCtas); its warp
+// w the blocks c*bpc + w, c*bpc + w + 4, ... and lane l element 32b + l of
+// each, read once and kept in registers (gamma is read before the wait on the
+// previous kernel).  Sum of squares, in an order that depends on H only: each
+// thread adds its elements' squares with fma in ascending b; warp partials by
+// butterfly; thread 0 adds its CTA's 4 warp sums in warp order; every thread
+// then adds the kNormCtas CTA sums in rank order, read from the CTAs' shared
+// memory, so all CTAs of the row hold the same r = 1 / sqrt(ss / H + eps)
+// (IEEE division and square root).
+constexpr int kNormCtas = 8;
+constexpr int kNormThreads = 128;
+constexpr int kNormMaxPerThread = 16;  // blocks per warp on the register path: H <= 16384
 
 template <bool REG>
 __global__ void __launch_bounds__(kNormThreads)
@@ -57,27 +66,37 @@ rmsnorm_quant_kernel(const float* __restrict__ x, int H, const float* __restrict
 {
     constexpr int NW = kNormThreads / 32;
     __shared__ float red[NW];
-    __shared__ float rs;
+    __shared__ float part;
+    cg::cluster_group cluster = cg::this_cluster();
     pdl_trigger();
-    pdl_wait();
-    const int t = blockIdx.x;
+    const int c = (int)cluster.block_rank();
+    const int t = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const float* xr = x + (size_t)t * H;
     const int nb = H >> 5;
+    const int bpc = (nb + kNormCtas - 1) / kNormCtas;
+    const int b0 = c * bpc, b1 = min(nb, b0 + bpc);
+    const float* xr = x + (size_t)t * H;
     float v[kNormMaxPerThread], gv[kNormMaxPerThread];
+    if (REG) {
+#pragma unroll
+        for (int k = 0; k < kNormMaxPerThread; ++k) {
+            const int b = b0 + warp + NW * k;
+            gv[k] = b < b1 ? gamma[b * 32 + lane] : 0.0f;
+        }
+    }
+    pdl_wait();
     float ss = 0.0f;
     if (REG) {
 #pragma unroll
         for (int k = 0; k < kNormMaxPerThread; ++k) {
-            const int b = warp + NW * k;
-            v[k] = b < nb ? xr[b * 32 + lane] : 0.0f;
-            gv[k] = b < nb ? gamma[b * 32 + lane] : 0.0f;
+            const int b = b0 + warp + NW * k;
+            v[k] = b < b1 ? xr[b * 32 + lane] : 0.0f;
         }
 #pragma unroll
         for (int k = 0; k < kNormMaxPerThread; ++k)
-            if (warp + NW * k < nb) ss = __fmaf_rn(v[k], v[k], ss);
+            if (b0 + warp + NW * k < b1) ss = __fmaf_rn(v[k], v[k], ss);
     } else {
-        for (int b = warp; b < nb; b += NW) {
+        for (int b = b0 + warp; b < b1; b += NW) {
             const float e = xr[b * 32 + lane];
             ss = __fmaf_rn(e, e, ss);
         }
@@ -86,16 +105,17 @@ rmsnorm_quant_kernel(const float* __restrict__ x, int H, const float* __restrict
     if (lane == 0) red[warp] = ss;
     __syncthreads();
     if (tid == 0) {
-        float tot = red[0];
-        for (int w = 1; w < NW; ++w) tot = __fadd_rn(tot, red[w]);
-        const float mean = __fdiv_rn(tot, (float)H);
-        rs = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
+        float s = red[0];
+        for (int w = 1; w < NW; ++w) s = __fadd_rn(s, red[w]);
+        part = s;
     }
-    __syncthreads();
-    const float r = rs;
+    cluster.sync();  // every CTA's sum is in place
+    float tot = *cluster.map_shared_rank(&part, 0);
+    for (int cc = 1; cc < kNormCtas; ++cc) tot = __fadd_rn(tot, *cluster.map_shared_rank(&part, cc));
+    const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(tot, (float)H), eps)));
 #pragma unroll
     for (int k = 0; k < (REG ? kNormMaxPerThread : 1); ++k) {
-        for (int b = warp + NW * k; b < nb; b += (REG ? nb : NW)) {
+        for (int b = b0 + warp + NW * k; b < b1; b += (REG ? nb : NW)) {
             const int i = b * 32 + lane;
             const float e = REG ? v[k] : xr[i];
             const float vn = __fmul_rn(__fmul_rn(e, r), REG ? gv[k] : gamma[i]);
@@ -106,15 +126,20 @@ rmsnorm_quant_kernel(const float* __restrict__ x, int H, const float* __restrict
             if (lane == 0) d[(size_t)t * nb + b] = dd;
         }
     }
+    cluster.sync();  // no CTA leaves while another may still read its sum
 }
 
 cudaError_t launch_rmsnorm_quant(const float* x, int T, int H, const float* gamma, float eps,
                                  float* xn, int8_t* q, float* d, cudaStream_t s)
 {
+    const int bpc = ((H >> 5) + kNormCtas - 1) / kNormCtas;
+    const dim3 grid(kNormCtas, T);
     const cudaError_t e =
-        H <= kNormThreads * kNormMaxPerThread
-            ? launch_pdl(rmsnorm_quant_kernel<true>, dim3(T), dim3(kNormThreads), s, x, H, gamma, eps, xn, q, d)
-            : launch_pdl(rmsnorm_quant_kernel<false>, dim3(T), dim3(kNormThreads), s, x, H, gamma, eps, xn, q, d);
+        bpc <= (kNormThreads / 32) * kNormMaxPerThread
+            ? launch_pdl_cluster(rmsnorm_quant_kernel<true>, grid, dim3(kNormThreads), kNormCtas, s, x, H, gamma, eps,
+                                 xn, q, d)
+            : launch_pdl_cluster(rmsnorm_quant_kernel<false>, grid, dim3(kNormThreads), kNormCtas, s, x, H, gamma,
+                                 eps, xn, q, d);
     count_launches(1);
     return e;
 }

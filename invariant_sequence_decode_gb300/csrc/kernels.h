@@ -74,10 +74,11 @@ size_t attn_part_floats(int total_chunks, int Hq);
 int attn_chunk_keys(int len);
 constexpr int kAttnMaxChunksPerRow = 511;  // the merge keeps two floats per chunk in shared memory
 
-// tickets: n_rows * Hkv ints that are zero on entry (and zero again on exit).
+// part: attn_part_floats(total_chunks, Hq) floats of split-K scratch.
 // out_q / out_d (nullable): q8_0 codes and scales of out (requires ldo == Hq*128).
+// Two launches: the chunks, then their merge.
 cudaError_t launch_attention(const float* q, int64_t ldq, const AttnRows& rows, int Hq, int Hkv,
-                             float scale, float* part, int* tickets, float* out, int64_t ldo,
+                             float scale, float* part, float* out, int64_t ldo,
                              int8_t* out_q, float* out_d, cudaStream_t s);
 
 cudaError_t launch_rmsnorm_quant(const float* x, int T, int H, const float* gamma, float eps,

@@ -97,7 +97,7 @@ def test_attention_refusals(lib):
     assert lib.luce_decode_attn_multiseq(P, v, 1, 18, 2, 128, 0.1, P, P, ws, None) == luce.LUCE_EUNSUPPORTED
     assert lib.luce_decode_attn_multiseq(P, v, 1, 9, 2, 128, 0.1, P, P, ws, None) == luce.LUCE_EINVAL
     assert lib.luce_decode_attn_multiseq(P, v, 1, 8, 2, 128, 0.1, P, P, 16, None) == luce.LUCE_ENOSPACE
-    assert lib.luce_decode_attn_workspace_size(4, 8, 128, 1000) == 512 + 4 * 8 * 8 * 132 * 4
+    assert lib.luce_decode_attn_workspace_size(4, 8, 128, 1000) == 4 * 8 * 8 * 132 * 4
 
 
 def fake_model(n_layers=2, vocab=0, head_dim=128, hidden=256, hq=4, hkv=2, ffn=512):

@@ -227,6 +227,28 @@ def test_attention_long_context_parity():
     assert np.max(np.abs(got - ref)) <= 2e-3
 
 
+def test_attention_strided_unaligned_cache_bitwise():
+    """A cache whose rows start 16 (not 32) bytes into a padded row of 136
+    halves gives the same bits as a packed, aligned cache: only how K is
+    loaded differs."""
+    lens, nq, Hkv = [1030, 257, 2051, 130], [2, 1, 1, 3], 8
+    q, caches, views = attn_case(11, lens, nq, 40, Hkv)
+    packed = run_attn(q, caches, views, Hkv, 0.08838834764831845)
+    sv = []
+    for (k, v), (L, n, r0) in zip(caches, views):
+        cap = k.shape[1]
+        pads = []
+        for a in (k, v):
+            flat = torch.zeros(8 + Hkv * cap * 136, dtype=torch.float16, device="cuda")
+            t = flat[8:].view(Hkv, cap, 136)[:, :, :128]
+            t.copy_(torch.from_numpy(a))
+            pads.append(t)
+        assert pads[0].data_ptr() % 32 == 16 and pads[0].stride(1) == 136
+        sv.append(luce.SeqView(pads[0], pads[1], L, n, r0))
+    got = host(luce.luce_decode_attn_multiseq(cuda(q), sv, Hkv, 0.08838834764831845))
+    assert np.array_equal(got.view(np.uint32), packed.view(np.uint32))
+
+
 def test_attention_batched_equals_solo_bitwise():
     lens, nq = [1030, 1800, 2051, 700], [4, 3, 2, 1]
     q, caches, views = attn_case(7, lens, nq, 40, 8)
