@@ -140,6 +140,18 @@ __device__ __forceinline__ int block_dot8(const uint32_t (&w)[8], const uint32_t
     return s0 + s1;
 }
 
+// The same dot returned as a float, exactly: one dp4a chain seeded with the
+// bits of 1.5 * 2^23, so the int32 result is the float 1.5 * 2^23 + dot
+// (|dot| <= 516,128 < 2^22 keeps it inside that binade), and one exact
+// subtraction leaves (float)dot without an integer-to-float conversion.
+__device__ __forceinline__ float block_dot8_f(const uint32_t (&w)[8], const uint32_t (&a)[8])
+{
+    int s = __dp4a((int)w[0], (int)a[0], 0x4B400000);
+#pragma unroll
+    for (int i = 1; i < 8; ++i) s = __dp4a((int)w[i], (int)a[i], s);
+    return __fsub_rn(__int_as_float(s), 12582912.0f);
+}
+
 // Integer dot of one 32-value block held as two 16-byte vectors per side.
 __device__ __forceinline__ int block_dot(const int4 w0, const int4 w1, const int4 a0, const int4 a1)
 {

@@ -31,7 +31,7 @@
 
 namespace luce {
 
-template <int T, int KL, int G, bool PF>
+template <int T, int KL, int G, bool PF, bool BIAS>
 __global__ void __launch_bounds__(32 * (32 / KL))
 q8_matvec_kernel(const int8_t* __restrict__ wq, const __half* __restrict__ wd, int N, int K,
                  const int8_t* __restrict__ aq, const float* __restrict__ ad,
@@ -79,8 +79,8 @@ q8_matvec_kernel(const int8_t* __restrict__ wq, const __half* __restrict__ wd, i
             const float da = __ldg(ad + (size_t)t * nb + b);
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                const int s = block_dot8(wv[g], av);
-                acc[g][t] = __fmaf_rn(__fmul_rn(sv[g], da), (float)s, acc[g][t]);
+                const float s = BIAS ? block_dot8_f(wv[g], av) : (float)block_dot8(wv[g], av);
+                acc[g][t] = __fmaf_rn(__fmul_rn(sv[g], da), s, acc[g][t]);
             }
         }
     };
@@ -118,13 +118,13 @@ q8_matvec_kernel(const int8_t* __restrict__ wq, const __half* __restrict__ wd, i
     }
 }
 
-template <int T, int KL, int G, bool PF>
+template <int T, int KL, int G, bool PF, bool BIAS>
 static cudaError_t launch_t(const int8_t* wq, const __half* wd, int N, int K, const int8_t* aq,
                             const float* ad, float* y, int64_t ldy, const float* resid, int64_t ldr,
                             cudaStream_t s)
 {
     constexpr int RC = (32 / KL) * G;
-    const cudaError_t e = launch_pdl(q8_matvec_kernel<T, KL, G, PF>, dim3((N + RC - 1) / RC), dim3(32 * (32 / KL)), s,
+    const cudaError_t e = launch_pdl(q8_matvec_kernel<T, KL, G, PF, BIAS>, dim3((N + RC - 1) / RC), dim3(32 * (32 / KL)), s,
                                      wq, wd, N, K, aq, ad, y, ldy, resid, ldr);
     count_launches(1);
     return e;
@@ -134,27 +134,28 @@ cudaError_t launch_matvec(const int8_t* wq, const __half* wd, int N, int K, cons
                           const float* ad, int T, float* y, int64_t ldy, const float* resid,
                           int64_t ldr, cudaStream_t s)
 {
-    // KL (lanes per row), G (rows per lane) and the L2 prefetch only shape the
-    // memory pipeline; none of them changes any row's arithmetic.
+    // KL (lanes per row), G (rows per lane), the L2 prefetch and the form of
+    // the int-to-float step (conversion, or the exact biased chain) only shape
+    // the pipeline; none of them changes any row's arithmetic.
     switch (T) {
-#define LUCE_MV(TT, KK, GG, PP) \
-    case TT: return launch_t<TT, KK, GG, PP>(wq, wd, N, K, aq, ad, y, ldy, resid, ldr, s);
-        LUCE_MV(1, 8, 1, false)
-        LUCE_MV(2, 8, 2, false)
-        LUCE_MV(3, 8, 2, false)
-        LUCE_MV(4, 8, 4, false)
-        LUCE_MV(5, 8, 4, false)
-        LUCE_MV(6, 8, 4, false)
-        LUCE_MV(7, 8, 4, false)
-        LUCE_MV(8, 8, 4, false)
-        LUCE_MV(9, 8, 2, false)
-        LUCE_MV(10, 8, 2, false)
-        LUCE_MV(11, 8, 2, false)
-        LUCE_MV(12, 8, 2, false)
-        LUCE_MV(13, 8, 2, false)
-        LUCE_MV(14, 8, 2, false)
-        LUCE_MV(15, 8, 2, false)
-        LUCE_MV(16, 8, 2, false)
+#define LUCE_MV(TT, KK, GG, PP, BB) \
+    case TT: return launch_t<TT, KK, GG, PP, BB>(wq, wd, N, K, aq, ad, y, ldy, resid, ldr, s);
+        LUCE_MV(1, 8, 1, false, true)
+        LUCE_MV(2, 8, 2, false, false)
+        LUCE_MV(3, 8, 2, false, false)
+        LUCE_MV(4, 8, 4, false, false)
+        LUCE_MV(5, 8, 4, false, true)
+        LUCE_MV(6, 8, 4, false, true)
+        LUCE_MV(7, 8, 4, false, true)
+        LUCE_MV(8, 8, 4, false, true)
+        LUCE_MV(9, 8, 2, false, false)
+        LUCE_MV(10, 8, 2, false, false)
+        LUCE_MV(11, 8, 2, false, false)
+        LUCE_MV(12, 8, 3, false, false)
+        LUCE_MV(13, 8, 2, false, false)
+        LUCE_MV(14, 8, 2, false, false)
+        LUCE_MV(15, 8, 2, false, false)
+        LUCE_MV(16, 8, 2, false, false)
 #undef LUCE_MV
         default: return cudaErrorInvalidValue;
     }

@@ -91,6 +91,23 @@ def test_block_dots_extremes():
     assert got[0, 0].tolist() == [516128, 516128] and got[0, 1].tolist() == [-516128, -516128]
 
 
+@pytest.mark.parametrize("T", list(range(1, 17)))
+def test_matvec_full_scale_blocks_exact(T):
+    """Every block dot at its extreme, +-32*127*127 = +-516,128, in every launch
+    shape: with unit scales each output is 32 * 516,128 = 16,516,096 (< 2^24),
+    exact in fp32 whatever the form of the int-to-float step."""
+    N, K = 40, 1024
+    wq = np.full((N, K), 127, np.int8)
+    wq[1::2] = -127
+    aq = np.full((T, K), 127, np.int8)
+    aq[1::2] = -127
+    wd = np.ones((N, K // 32), np.float16)
+    ad = np.ones((T, K // 32), np.float32)
+    y = host(luce.luce_q8_matvec_batch(cuda(wq), cuda(wd), cuda(aq), cuda(ad)))
+    sign = np.where(np.arange(T)[:, None] % 2 == np.arange(N)[None, :] % 2, 1.0, -1.0)
+    assert np.array_equal(y, (sign * 32 * 516128).astype(np.float32))
+
+
 @pytest.mark.parametrize("N,K", MV_SHAPES)
 @pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 8, 12, 16])
 def test_matvec_parity(N, K, T):
