@@ -466,7 +466,6 @@ int luce_decode_step(const luce_model* m, const luce_slot* slots, const int32_t*
     cudaError_t e = cudaSuccess;
 
     const float scale = (float)(1.0 / sqrt((double)D));
-    const int64_t qkv_rows = (int64_t)(Hq + 2 * Hkv) * D;
     for (int l = 0; l < m->n_layers; ++l) {
         const luce_layer& w = m->layers[l];
         KvRows kv{};
@@ -496,10 +495,9 @@ int luce_decode_step(const luce_model* m, const luce_slot* slots, const int32_t*
         ar.total_chunks = c;
 
         if ((e = launch_rmsnorm_quant(x, T, H, w.attn_norm, m->rms_eps, xn, xn_q, xn_d, st))) break;
-        if ((e = launch_matvec(w.wqkv_q, (const __half*)w.wqkv_d, (int)qkv_rows, H, xn_q, xn_d, T, qkv, qkv_rows,
-                               nullptr, 0, st)))
+        if ((e = launch_qkv_rope(w.wqkv_q, (const __half*)w.wqkv_d, H, xn_q, xn_d, T, qkv, Hq, Hkv, pos, freq, q_rot,
+                                 kv, st)))
             break;
-        if ((e = launch_rope_kv(qkv, T, Hq, Hkv, pos, freq, q_rot, kv, st))) break;
         if ((e = launch_attention(q_rot, (int64_t)Hq * D, ar, Hq, Hkv, scale, part, attn, (int64_t)Hq * D,
                                   attn_q, attn_d, st)))
             break;

@@ -58,6 +58,13 @@ cudaError_t launch_matvec(const int8_t* wq, const __half* wd, int N, int K, cons
                           const float* ad, int T, float* y, int64_t ldy, const float* resid,
                           int64_t ldr, cudaStream_t s);
 
+// The step's q|k|v projection (N = (Hq + 2*Hkv) * 128 rows) with RoPE of the
+// q and k heads at each row's position, q heads to q_rot [T][Hq][128], k and v
+// heads appended as binary16 at rows' K/V destinations; qkv [T][N] also written.
+cudaError_t launch_qkv_rope(const int8_t* wq, const __half* wd, int K, const int8_t* aq, const float* ad, int T,
+                            float* qkv, int Hq, int Hkv, const RowPos& pos, const RopeFreq& f, float* q_rot,
+                            const KvRows& kv, cudaStream_t s);
+
 cudaError_t launch_block_dots(const int8_t* wq, int N, int K, const int8_t* aq, int T, int32_t* out,
                               cudaStream_t s);
 
@@ -86,9 +93,6 @@ cudaError_t launch_rmsnorm_quant(const float* x, int T, int H, const float* gamm
 
 cudaError_t launch_swiglu_quant(const float* gu, int T, int F, float* h, int8_t* q, float* d,
                                 cudaStream_t s);
-
-cudaError_t launch_rope_kv(const float* qkv, int T, int Hq, int Hkv, const RowPos& pos, const RopeFreq& f,
-                           float* q_rot, const KvRows& rows, cudaStream_t s);
 
 cudaError_t launch_argmax(const float* x, int T, int V, int32_t* out, cudaStream_t s);
 

@@ -31,33 +31,23 @@
 
 namespace luce {
 
-template <int T, int KL, int G, bool PF, bool BIAS>
-__global__ void __launch_bounds__(32 * (32 / KL))
-q8_matvec_kernel(const int8_t* __restrict__ wq, const __half* __restrict__ wd, int N, int K,
-                 const int8_t* __restrict__ aq, const float* __restrict__ ad,
-                 float* y, int64_t ldy, const float* resid, int64_t ldr)
+// The chains of lane (r, kb) of warp w (c = kb + KL*w) for the G weight rows
+// rows[g]: acc[g][t] = chain c of row rows[g] against token t.  The first
+// weight stage is loaded before the wait on the previous kernel.
+template <int T, int KL, int G, bool BIAS>
+__device__ __forceinline__ void q8_chains(const int8_t* __restrict__ wq, const __half* __restrict__ wd, int K,
+                                          const int (&rows)[G], int c, const int8_t* __restrict__ aq,
+                                          const float* __restrict__ ad, float (&acc)[G][T])
 {
-    constexpr int RW = 32 / KL;
-    constexpr int RC = RW * G;
-    __shared__ float part[RC][T][33];
-    pdl_trigger();
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int r = lane / KL, kb = lane - (lane / KL) * KL;
-    const int c = kb + KL * w;
-    const int row0 = blockIdx.x * RC;
     const int nb = K >> 5;
     const int8_t* wp[G];
     const __half* dp[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-        const int rowc = min(row0 + r + RW * g, N - 1);
-        wp[g] = wq + (size_t)rowc * K + (size_t)c * 32;
-        dp[g] = wd + (size_t)rowc * nb + c;
+        wp[g] = wq + (size_t)rows[g] * K + (size_t)c * 32;
+        dp[g] = wd + (size_t)rows[g] * nb + c;
     }
-    if (PF && threadIdx.x == 0) prefetch_l2(wq + (size_t)row0 * K, (uint32_t)(min(RC, N - row0) * K));
     const int nj = (nb - c + 31) >> 5;  // blocks of this chain (>= 0)
-
-    float acc[G][T];
 #pragma unroll
     for (int g = 0; g < G; ++g)
 #pragma unroll
@@ -94,7 +84,42 @@ q8_matvec_kernel(const int8_t* __restrict__ wq, const __half* __restrict__ wd, i
         if (j + 2 < nj) load(wa, sa, j + 2);
         if (j + 1 < nj) compute(wb, sb, j + 1);
     }
+}
 
+// The 32 chain values of one (row, token), combined by the xor butterfly's
+// pairings: v[i] += v[i + off] for off = 16, 8, 4, 2, 1.
+__device__ __forceinline__ float q8_butterfly(const float* __restrict__ part)
+{
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = part[i];
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1)
+#pragma unroll
+        for (int i = 0; i < off; ++i) v[i] = __fadd_rn(v[i], v[i + off]);
+    return v[0];
+}
+
+template <int T, int KL, int G, bool PF, bool BIAS>
+__global__ void __launch_bounds__(32 * (32 / KL))
+q8_matvec_kernel(const int8_t* __restrict__ wq, const __half* __restrict__ wd, int N, int K,
+                 const int8_t* __restrict__ aq, const float* __restrict__ ad,
+                 float* y, int64_t ldy, const float* resid, int64_t ldr)
+{
+    constexpr int RW = 32 / KL;
+    constexpr int RC = RW * G;
+    __shared__ float part[RC][T][33];
+    pdl_trigger();
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int r = lane / KL, kb = lane - (lane / KL) * KL;
+    const int c = kb + KL * w;
+    const int row0 = blockIdx.x * RC;
+    int rows[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) rows[g] = min(row0 + r + RW * g, N - 1);
+    if (PF && threadIdx.x == 0) prefetch_l2(wq + (size_t)row0 * K, (uint32_t)(min(RC, N - row0) * K));
+    float acc[G][T];
+    q8_chains<T, KL, G, BIAS>(wq, wd, K, rows, c, aq, ad, acc);
 #pragma unroll
     for (int g = 0; g < G; ++g)
 #pragma unroll
@@ -102,16 +127,9 @@ q8_matvec_kernel(const int8_t* __restrict__ wq, const __half* __restrict__ wd, i
     __syncthreads();
     for (int idx = threadIdx.x; idx < RC * T; idx += blockDim.x) {
         const int rr = idx / T, t = idx - (idx / T) * T;
-        float v[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = part[rr][t][i];
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1)
-#pragma unroll
-            for (int i = 0; i < off; ++i) v[i] = __fadd_rn(v[i], v[i + off]);
         const int n = row0 + rr;
         if (n < N) {
-            float out = v[0];
+            float out = q8_butterfly(part[rr][t]);
             if (resid) out = __fadd_rn(resid[(size_t)t * ldr + n], out);
             y[(size_t)t * ldy + n] = out;
         }
@@ -124,8 +142,8 @@ static cudaError_t launch_t(const int8_t* wq, const __half* wd, int N, int K, co
                             cudaStream_t s)
 {
     constexpr int RC = (32 / KL) * G;
-    const cudaError_t e = launch_pdl(q8_matvec_kernel<T, KL, G, PF, BIAS>, dim3((N + RC - 1) / RC), dim3(32 * (32 / KL)), s,
-                                     wq, wd, N, K, aq, ad, y, ldy, resid, ldr);
+    const cudaError_t e = launch_pdl(q8_matvec_kernel<T, KL, G, PF, BIAS>, dim3((N + RC - 1) / RC),
+                                     dim3(32 * (32 / KL)), s, wq, wd, N, K, aq, ad, y, ldy, resid, ldr);
     count_launches(1);
     return e;
 }
@@ -157,6 +175,113 @@ cudaError_t launch_matvec(const int8_t* wq, const __half* wd, int N, int K, cons
         LUCE_MV(15, 8, 2, false, false)
         LUCE_MV(16, 8, 2, false, false)
 #undef LUCE_MV
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+// ------------------------------------------------------------ q|k|v + RoPE + K/V append
+//
+// The decode step's q|k|v projection with the RoPE rotation and the K/V
+// append done by the CTA that computes the rows ("antirez/ds4 pull 604",
+// Commit walkthrough: RoPE per row at the row's position, K/V appended per
+// sequence).  The CTA's RC = 8G weight rows are P = RC/2 rotation pairs of one
+// head: CTA b serves head h = b / (64/P), pair group q = b % (64/P), and local
+// row s is dim q*P + s (s < P) or 64 + q*P + (s - P) of the head.  Each row's
+// value is the same chain-and-butterfly result as the plain kernel's; the
+// pair then takes exactly the rotation and conversion of the standalone RoPE
+// and append kernels (rope_cs, rope_rotate, round-to-nearest binary16), and
+// the unrotated q|k|v row is written too.
+template <int T, int G, bool BIAS>
+__global__ void __launch_bounds__(128)
+q8_qkv_rope_kernel(const int8_t* __restrict__ wq, const __half* __restrict__ wd, int K,
+                   const int8_t* __restrict__ aq, const float* __restrict__ ad, float* __restrict__ qkv, int Hq,
+                   int Hkv, RowPos pos, RopeFreq f, float* __restrict__ q_rot, KvRows kv)
+{
+    constexpr int KL = 8, RW = 4, RC = RW * G, P = RC / 2, GROUPS = (kHeadDim / 2) / P;
+    static_assert((kHeadDim / 2) % P == 0, "rotation pairs must tile the half head");
+    __shared__ float part[RC][T][33];
+    pdl_trigger();
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int r = lane / KL, kb = lane - (lane / KL) * KL;
+    const int c = kb + KL * w;
+    const int h = blockIdx.x / GROUPS, q0 = (blockIdx.x % GROUPS) * P;
+    auto dim_of = [&](int s) { return s < P ? q0 + s : kHeadDim / 2 + q0 + (s - P); };
+    static_assert(P * T <= 128, "one (pair, token) per thread");
+    int rows[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) rows[g] = h * kHeadDim + dim_of(r + RW * g);
+    // thread idx < P*T finishes pair p = idx / T of token t = idx % T; its
+    // cos/sin depend only on the position, so they are formed first
+    const int idx = threadIdx.x;
+    const int p = idx / T, t = idx - (idx / T) * T;
+    const int i = q0 + p;
+    const bool fin = idx < P * T;
+    const float2 cs = (fin && h < Hq + Hkv) ? rope_cs(pos.pos[t], f.inv[i]) : make_float2(1.0f, 0.0f);
+    float acc[G][T];
+    q8_chains<T, KL, G, BIAS>(wq, wd, K, rows, c, aq, ad, acc);
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int tt = 0; tt < T; ++tt) part[r + RW * g][tt][c] = acc[g][tt];
+    __syncthreads();
+    const int ldq = (Hq + 2 * Hkv) * kHeadDim;
+    if (fin) {
+        float x0 = q8_butterfly(part[p][t]);
+        float x1 = q8_butterfly(part[p + P][t]);
+        float* yr = qkv + (size_t)t * ldq + (size_t)h * kHeadDim;
+        yr[i] = x0;
+        yr[i + kHeadDim / 2] = x1;
+        const KvRow kr = kv.row[t];
+        if (h < Hq + Hkv) rope_rotate(x0, x1, cs.x, cs.y);
+        if (h < Hq) {
+            float* dst = q_rot + (size_t)t * Hq * kHeadDim + (size_t)h * kHeadDim;
+            dst[i] = x0;
+            dst[i + kHeadDim / 2] = x1;
+        } else {
+            __half* dst = (h < Hq + Hkv ? kr.k + (h - Hq) * kr.head_stride : kr.v + (h - Hq - Hkv) * kr.head_stride);
+            dst[i] = __float2half_rn(x0);
+            dst[i + kHeadDim / 2] = __float2half_rn(x1);
+        }
+    }
+}
+
+template <int T, int G, bool BIAS>
+static cudaError_t launch_qkv_t(const int8_t* wq, const __half* wd, int K, const int8_t* aq, const float* ad,
+                                float* qkv, int Hq, int Hkv, const RowPos& pos, const RopeFreq& f, float* q_rot,
+                                const KvRows& kv, cudaStream_t s)
+{
+    constexpr int P = 4 * G / 2;
+    const cudaError_t e = launch_pdl(q8_qkv_rope_kernel<T, G, BIAS>, dim3((Hq + 2 * Hkv) * ((kHeadDim / 2) / P)),
+                                     dim3(128), s, wq, wd, K, aq, ad, qkv, Hq, Hkv, pos, f, q_rot, kv);
+    count_launches(1);
+    return e;
+}
+
+cudaError_t launch_qkv_rope(const int8_t* wq, const __half* wd, int K, const int8_t* aq, const float* ad, int T,
+                            float* qkv, int Hq, int Hkv, const RowPos& pos, const RopeFreq& f, float* q_rot,
+                            const KvRows& kv, cudaStream_t s)
+{
+    // the plain kernel's launch shapes, except G = 4 at T = 12 (P must divide 64)
+    switch (T) {
+#define LUCE_QKV(TT, GG, BB) \
+    case TT: return launch_qkv_t<TT, GG, BB>(wq, wd, K, aq, ad, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
+        LUCE_QKV(1, 1, true)
+        LUCE_QKV(2, 2, false)
+        LUCE_QKV(3, 2, false)
+        LUCE_QKV(4, 4, false)
+        LUCE_QKV(5, 4, true)
+        LUCE_QKV(6, 4, true)
+        LUCE_QKV(7, 4, true)
+        LUCE_QKV(8, 4, true)
+        LUCE_QKV(9, 2, false)
+        LUCE_QKV(10, 2, false)
+        LUCE_QKV(11, 2, false)
+        LUCE_QKV(12, 4, false)
+        LUCE_QKV(13, 2, false)
+        LUCE_QKV(14, 2, false)
+        LUCE_QKV(15, 2, false)
+        LUCE_QKV(16, 2, false)
+#undef LUCE_QKV
         default: return cudaErrorInvalidValue;
     }
 }

@@ -10,7 +10,8 @@
 // reduced in double on the device and only the reduced angle goes through
 // fp32 sincosf (see rope_cs), so even position 32767 carries no fp32 angle
 // error.  The rotation is fp32 with explicit rounding.  One CTA of 64 threads
-// per (row, head): thread i owns pair i.
+// per (row, head): thread i owns pair i.  The decode step applies the same
+// rotation and append in the epilogue of its q|k|v projection (matvec.cu).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -57,48 +58,6 @@ cudaError_t launch_kv_append(const float* k, const float* v, int64_t ld, int Hkv
                              cudaStream_t s)
 {
     const cudaError_t e = launch_pdl(kv_append_kernel, dim3(rows.n_rows), dim3(256), s, k, v, ld, Hkv, rows);
-    count_launches(1);
-    return e;
-}
-
-// Decode-step glue, one CTA per (row, head of the fused q|k|v projection):
-// q heads are rotated into q_rot, k heads rotated and appended to the row's
-// cache position as binary16, v heads appended.  Same rotation and
-// conversion as the standalone kernels above.
-__global__ void __launch_bounds__(64)
-rope_kv_kernel(const float* __restrict__ qkv, int Hq, int Hkv, RowPos pos, RopeFreq f,
-               float* __restrict__ q_rot, KvRows rows)
-{
-    pdl_trigger();
-    const int t = blockIdx.x, h = blockIdx.y, i = threadIdx.x;
-    const float2 cs = h < Hq + Hkv ? rope_cs(pos.pos[t], f.inv[i]) : make_float2(1.0f, 0.0f);
-    pdl_wait();
-    const float* src = qkv + (size_t)t * (Hq + 2 * Hkv) * kHeadDim + (size_t)h * kHeadDim;
-    const KvRow r = rows.row[t];
-    if (h < Hq + Hkv) {
-        float x0 = src[i], x1 = src[i + 64];
-        rope_rotate(x0, x1, cs.x, cs.y);
-        if (h < Hq) {
-            float* dst = q_rot + (size_t)t * Hq * kHeadDim + (size_t)h * kHeadDim;
-            dst[i] = x0;
-            dst[i + 64] = x1;
-        } else {
-            __half* dst = r.k + (h - Hq) * r.head_stride;
-            dst[i] = __float2half_rn(x0);
-            dst[i + 64] = __float2half_rn(x1);
-        }
-    } else {
-        __half* dst = r.v + (h - Hq - Hkv) * r.head_stride;
-        dst[i] = __float2half_rn(src[i]);
-        dst[i + 64] = __float2half_rn(src[i + 64]);
-    }
-}
-
-cudaError_t launch_rope_kv(const float* qkv, int T, int Hq, int Hkv, const RowPos& pos, const RopeFreq& f,
-                           float* q_rot, const KvRows& rows, cudaStream_t s)
-{
-    const cudaError_t e = launch_pdl(rope_kv_kernel, dim3(T, Hq + 2 * Hkv), dim3(64), s, qkv, Hq, Hkv, pos, f, q_rot,
-                                     rows);
     count_launches(1);
     return e;
 }
