@@ -312,9 +312,10 @@ attn_merge_kernel(AttnRows rows, int Hq, const float* __restrict__ part, float* 
     const size_t cstride = (size_t)Hq * kPartStride;
     const float* bh = part + ((size_t)row.chunk0 * Hq + h) * kPartStride;
     pdl_wait();
-    float ov[16];  // the first 16 chunk outputs, loaded while the statistics are gathered
+    constexpr int kPre = 32;  // chunk outputs loaded while the statistics are gathered
+    float ov[kPre];
 #pragma unroll
-    for (int u = 0; u < 16; ++u) ov[u] = u < nch ? __ldcg(bh + u * cstride + d) : 0.0f;
+    for (int u = 0; u < kPre; ++u) ov[u] = u < nch ? __ldcg(bh + u * cstride + d) : 0.0f;
     if (d < 32) {
         float M = -INFINITY;
         for (int cc = lane; cc < nch; cc += 32) {
@@ -336,9 +337,9 @@ attn_merge_kernel(AttnRows rows, int Hq, const float* __restrict__ part, float* 
     __syncthreads();
     float O = 0.0f;
 #pragma unroll
-    for (int u = 0; u < 16; ++u)
+    for (int u = 0; u < kPre; ++u)
         if (u < nch) O = __fmaf_rn(ov[u], wts[u], O);
-    int cc = 16;
+    int cc = kPre;
     for (; cc + 16 <= nch; cc += 16) {
         float ob[16];
 #pragma unroll
