@@ -181,6 +181,35 @@ int luce_decode_attn_multiseq(const float* q, const luce_seqview* views, int n_s
 size_t luce_decode_attn_workspace_size(int n_rows, int Hq, int D, int max_len);
 
 /*
+ * A sequence's K/V for one layer held in fixed pages of LUCE_PAGE_KEYS keys
+ * [the per-sequence fallback beyond a flat cache: the pages' attention keeps
+ * its per-sequence views, here each view names its pages].  Page p of a pool
+ * is binary16 [Hkv][LUCE_PAGE_KEYS][D]; key j of the sequence is in pool page
+ * table[j / LUCE_PAGE_KEYS] at row j % LUCE_PAGE_KEYS, so element (g, j, d) of
+ * K is k_pool[(table[j / 128] * Hkv + g) * 128 * 128 + (j % 128) * 128 + d].
+ * The page size equals the attention's key tile, so chunking and every sum
+ * are those of the flat cache: a paged sequence gives the flat sequence's
+ * bits.  table (device) holds ceil(len / 128) entries in [0, n_pages).
+ */
+#define LUCE_PAGE_KEYS 128
+typedef struct luce_pagedview {
+    const uint16_t* k_pool;  /* (device) [n_pages][Hkv][128][128], 16-byte aligned */
+    const uint16_t* v_pool;  /* (device) same layout */
+    const int32_t* table;    /* (device) page of each 128-key span */
+    int32_t len;             /* keys including this step's n_q rows */
+    int32_t n_q;             /* 1..LUCE_MAX_ROWS_PER_SEQ */
+    int32_t row0;
+} luce_pagedview;
+
+/*
+ * luce_decode_attn_multiseq over paged views (same rows, outputs, workspace
+ * size and errors).  The table entries are device data the call cannot see:
+ * the caller guarantees they lie in [0, n_pages) of their pool.
+ */
+int luce_decode_attn_paged(const float* q, const luce_pagedview* views, int n_seq, int Hq, int Hkv, int D,
+                           float scale, float* out, void* ws, size_t ws_bytes, void* stream);
+
+/*
  * luce_decode_attn_multiseq without a caller workspace.  The pages have no
  * counterpart: this entry point exists for callers that cannot allocate
  * device memory themselves (a serving loop that must not call cudaMalloc
@@ -272,6 +301,35 @@ int luce_decode_step_layout(const luce_model* m, int n_rows, int max_ctx, luce_s
 int luce_decode_step(const luce_model* m, const luce_slot* slots, const int32_t* rows_per_slot,
                      int n_seq, float* x, float* logits, int32_t* argmax,
                      void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * A slot whose K/V lives in pages of LUCE_PAGE_KEYS tokens: pool page p holds
+ * binary16 [n_layers][n_kv_heads][128][head_dim], so token j's K in layer l,
+ * KV head g is k_pool[((table[j / 128] * n_layers + l) * n_kv_heads + g)
+ * * 128 * 128 + (j % 128) * 128 + d].  The table is given twice, identical:
+ * on the device (read by attention) and on the host (where the step's rows
+ * are appended).  n_table >= ceil((len + rows) / 128) entries, each in
+ * [0, n_pages); the pages that receive this step's rows are referenced by no
+ * other slot of the call.
+ */
+typedef struct luce_paged_slot {
+    uint16_t* k_pool;              /* (device) [n_pages][n_layers][Hkv][128][128] */
+    uint16_t* v_pool;              /* (device) */
+    const int32_t* table;          /* (device) [n_table] */
+    const int32_t* table_host;     /* (host)   [n_table], equal to table */
+    int32_t n_table;
+    int32_t n_pages;
+    int32_t len;                   /* tokens already cached before this step */
+} luce_paged_slot;
+
+/*
+ * luce_decode_step over paged slots: the same rows, outputs and bits as the
+ * flat step over caches holding the same tokens.  ws is sized by
+ * luce_decode_step_layout with max_ctx >= every len + rows.
+ */
+int luce_decode_step_paged(const luce_model* m, const luce_paged_slot* slots, const int32_t* rows_per_slot,
+                           int n_seq, float* x, float* logits, int32_t* argmax,
+                           void* ws, size_t ws_bytes, void* stream);
 
 #ifdef __cplusplus
 }

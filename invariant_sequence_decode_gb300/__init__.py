@@ -57,6 +57,17 @@ class SlotC(ctypes.Structure):
     _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("len", ctypes.c_int32), ("cap", ctypes.c_int32)]
 
 
+class PagedViewC(ctypes.Structure):
+    _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p), ("table", ctypes.c_void_p),
+                ("len", ctypes.c_int32), ("n_q", ctypes.c_int32), ("row0", ctypes.c_int32)]
+
+
+class PagedSlotC(ctypes.Structure):
+    _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p), ("table", ctypes.c_void_p),
+                ("table_host", ctypes.POINTER(ctypes.c_int32)), ("n_table", ctypes.c_int32),
+                ("n_pages", ctypes.c_int32), ("len", ctypes.c_int32)]
+
+
 _LAYOUT_FIELDS = ("xn", "xn_q", "xn_d", "qkv", "q_rot", "part", "attn", "attn_q", "attn_d", "x1",
                   "xn2", "xn2_q", "xn2_d", "gu", "h", "h_q", "h_d", "xf", "xf_q", "xf_d", "total")
 
@@ -68,7 +79,8 @@ class StepLayoutC(ctypes.Structure):
 EXPORTS = ("luce_last_error", "luce_version", "luce_launch_count", "luce_q8_quantize_act", "luce_q8_matvec_batch",
            "luce_q8_block_dots", "luce_rope_posvec", "luce_kv_append", "luce_decode_attn_multiseq",
            "luce_decode_attn_workspace_size", "luce_decode_step_layout", "luce_decode_step",
-           "luce_decode_attn_multiseq_noalloc", "luce_decode_attn_noalloc_max_bytes")
+           "luce_decode_attn_multiseq_noalloc", "luce_decode_attn_noalloc_max_bytes", "luce_decode_attn_paged",
+           "luce_decode_step_paged")
 
 _lib = None
 
@@ -101,6 +113,9 @@ def load_library(path: str = LIB_PATH):
                                      i32, vp, vp, vp, vp, sz, vp]
     lib.luce_decode_attn_multiseq_noalloc.argtypes = [vp, ctypes.POINTER(SeqViewC), i32, i32, i32, i32, f32, vp, vp]
     lib.luce_decode_attn_noalloc_max_bytes.argtypes = []
+    lib.luce_decode_attn_paged.argtypes = [vp, ctypes.POINTER(PagedViewC), i32, i32, i32, i32, f32, vp, vp, sz, vp]
+    lib.luce_decode_step_paged.argtypes = [ctypes.POINTER(ModelC), ctypes.POINTER(PagedSlotC),
+                                           ctypes.POINTER(ctypes.c_int32), i32, vp, vp, vp, vp, sz, vp]
     lib.luce_decode_attn_noalloc_max_bytes.restype = sz
     for name in EXPORTS:
         if name not in ("luce_last_error", "luce_version", "luce_launch_count", "luce_decode_attn_workspace_size",
@@ -240,6 +255,39 @@ def luce_decode_attn_multiseq(q, views: Sequence[SeqView], n_kv_heads: int, scal
     return out
 
 
+PAGE_KEYS = 128
+
+
+@dataclass
+class PagedView:
+    """A sequence's K/V for one layer in pages: pools fp16 [n_pages][Hkv][128][128],
+    ``table`` (device int32) the pool page of each 128-key span; ``len`` keys
+    including this step's ``n_q`` rows, which are rows row0.. of q/out."""
+    k_pool: object
+    v_pool: object
+    table: object
+    len: int
+    n_q: int = 1
+    row0: int = 0
+
+
+def luce_decode_attn_paged(q, views: Sequence[PagedView], n_kv_heads: int, scale: float, out=None, ws=None,
+                           stream=None):
+    """luce_decode_attn_multiseq over paged caches (the same bits as a flat cache)."""
+    import torch
+    _need(q, torch.float32, "q")
+    T, Hq, D = q.shape
+    out = torch.empty_like(q) if out is None else out
+    if ws is None:
+        max_len = max(v.len for v in views)
+        ws = torch.empty(luce_decode_attn_workspace_size(T, Hq, D, max_len), dtype=torch.uint8, device=q.device)
+    vc = (PagedViewC * len(views))(*[PagedViewC(v.k_pool.data_ptr(), v.v_pool.data_ptr(), v.table.data_ptr(), v.len,
+                                                v.n_q, v.row0) for v in views])
+    _check(load_library().luce_decode_attn_paged(q.data_ptr(), vc, len(views), Hq, n_kv_heads, D, float(scale),
+                                                 out.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream)))
+    return out
+
+
 def luce_decode_attn_multiseq_noalloc(q, views: Sequence[SeqView], n_kv_heads: int, scale: float, out=None,
                                       stream=None):
     """luce_decode_attn_multiseq using the library's fixed scratch array instead
@@ -308,6 +356,40 @@ class Slot:
     @property
     def cap(self) -> int:
         return self.k.shape[2]
+
+
+@dataclass
+class PagedSlot:
+    """A slot in pages of 128 tokens: pools fp16 [n_pages][n_layers][Hkv][128][128];
+    ``table`` lists the pool page of each 128-token span (kept as a host int32
+    array and mirrored on the device)."""
+    k_pool: object
+    v_pool: object
+    table: object  # numpy int32
+    len: int
+
+    def __post_init__(self):
+        import numpy as np
+        import torch
+        self.table = np.ascontiguousarray(self.table, dtype=np.int32)
+        self.table_dev = torch.from_numpy(self.table).to(self.k_pool.device)
+
+
+def luce_decode_step_paged(model: "Model", slots: Sequence[PagedSlot], rows_per_slot: Sequence[int], x, ws,
+                           logits=None, argmax=None, stream=None):
+    """luce_decode_step over paged slots (the same bits as flat caches)."""
+    import torch
+    _need(x, torch.float32, "x")
+    n = len(slots)
+    sc = (PagedSlotC * max(1, n))()
+    for i, s in enumerate(slots):
+        sc[i] = PagedSlotC(s.k_pool.data_ptr(), s.v_pool.data_ptr(), s.table_dev.data_ptr(),
+                           s.table.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), len(s.table),
+                           s.k_pool.shape[0], s.len)
+    rows = (ctypes.c_int32 * max(1, n))(*rows_per_slot)
+    _check(load_library().luce_decode_step_paged(ctypes.byref(model.c), sc, rows, n, x.data_ptr(), _ptr(logits),
+                                                 _ptr(argmax), ws.data_ptr(), ws.numel(), _stream(stream)))
+    return x
 
 
 def luce_decode_step(model: Model, slots: Sequence[Slot], rows_per_slot: Sequence[int], x, ws,

@@ -64,6 +64,8 @@ bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+constexpr int kPageKeys = LUCE_PAGE_KEYS;
+
 int chunks_of(int len)
 {
     const int ch = attn_chunk_keys(len);
@@ -252,6 +254,63 @@ int luce_decode_attn_multiseq(const float* q, const luce_seqview* views, int n_s
                        "decode_attn");
 }
 
+int luce_decode_attn_paged(const float* q, const luce_pagedview* views, int n_seq, int Hq, int Hkv, int D,
+                           float scale, float* out, void* ws, size_t ws_bytes, void* stream)
+{
+    const char* who = "decode_attn_paged";
+    REQUIRE(q && out && ws && views, LUCE_EINVAL, "%s: null q/out/ws/views", who);
+    REQUIRE(Hkv >= 1 && Hq >= Hkv && Hq % Hkv == 0, LUCE_EINVAL, "%s: Hq=%d must be a multiple of Hkv=%d", who, Hq,
+            Hkv);
+    REQUIRE(Hq / Hkv <= 8, LUCE_EUNSUPPORTED, "%s: group size %d > 8", who, Hq / Hkv);
+    REQUIRE(D == LUCE_HEAD_DIM, LUCE_EUNSUPPORTED, "%s: head_dim %d (only %d)", who, D, LUCE_HEAD_DIM);
+    REQUIRE(isfinite(scale), LUCE_EINVAL, "%s: scale must be finite", who);
+    REQUIRE(aligned(q, 16) && aligned(out, 4) && aligned(ws, 16), LUCE_EINVAL, "%s: misaligned q/out/ws", who);
+    REQUIRE(n_seq >= 1 && n_seq <= LUCE_MAX_SEQ, LUCE_EINVAL,
+            "%s: n_seq=%d outside 1..%d (more than %d sequences are refused)", who, n_seq, LUCE_MAX_SEQ,
+            LUCE_MAX_SEQ);
+    int covered[LUCE_MAX_ROWS] = {0};
+    int T = 0;
+    AttnRows rows{};
+    for (int s = 0; s < n_seq; ++s) {
+        const luce_pagedview& v = views[s];
+        REQUIRE(v.k_pool && v.v_pool && aligned(v.k_pool, 16) && aligned(v.v_pool, 16), LUCE_EINVAL,
+                "%s: view %d pool null or not 16-byte aligned", who, s);
+        REQUIRE(v.table && aligned(v.table, 4), LUCE_EINVAL, "%s: view %d table null", who, s);
+        REQUIRE(v.n_q >= 1 && v.n_q <= LUCE_MAX_ROWS_PER_SEQ, LUCE_EINVAL, "%s: view %d n_q=%d outside 1..%d", who,
+                s, v.n_q, LUCE_MAX_ROWS_PER_SEQ);
+        REQUIRE(v.len >= v.n_q, LUCE_EINVAL, "%s: view %d len=%d < n_q", who, s, v.len);
+        REQUIRE(v.len <= kMaxKeys, LUCE_EUNSUPPORTED, "%s: view %d has %d keys (at most %d)", who, s, v.len, kMaxKeys);
+        REQUIRE(v.row0 >= 0 && v.row0 + v.n_q <= LUCE_MAX_ROWS, LUCE_EINVAL, "%s: view %d rows out of range", who, s);
+        for (int j = 0; j < v.n_q; ++j) {
+            REQUIRE(!covered[v.row0 + j], LUCE_EINVAL, "%s: row %d claimed twice", who, v.row0 + j);
+            covered[v.row0 + j] = 1;
+            AttnRow& r = rows.row[v.row0 + j];
+            r.k = reinterpret_cast<const __half*>(v.k_pool);
+            r.v = reinterpret_cast<const __half*>(v.v_pool);
+            r.head_stride = (int64_t)kPageKeys * D;
+            r.tok_stride = D;
+            r.len = v.len - v.n_q + 1 + j;
+            r.chunk = attn_chunk_keys(r.len);
+            r.pages = v.table;
+            r.page_stride = (int64_t)Hkv * kPageKeys * D;
+        }
+        T = std::max(T, v.row0 + v.n_q);
+    }
+    for (int r = 0; r < T; ++r) REQUIRE(covered[r], LUCE_EINVAL, "%s: row %d belongs to no view", who, r);
+    rows.n_rows = T;
+    int c = 0;
+    for (int r = 0; r < T; ++r) {
+        rows.row[r].chunk0 = c;
+        c += chunks_of(rows.row[r].len);
+    }
+    rows.total_chunks = c;
+    const size_t need = attn_part_floats(rows.total_chunks, Hq) * sizeof(float);
+    REQUIRE(ws_bytes >= need, LUCE_ENOSPACE, "%s: workspace %zu bytes < %zu needed", who, ws_bytes, need);
+    return cuda_status(launch_attention(q, (int64_t)Hq * D, rows, Hq, Hkv, scale, (float*)ws, out, (int64_t)Hq * D,
+                                        nullptr, nullptr, (cudaStream_t)stream),
+                       who);
+}
+
 // ------------------------------------------------------------ attention, no allocation
 //
 // For callers that cannot allocate device memory themselves (a real-time
@@ -383,15 +442,23 @@ int luce_decode_step_layout(const luce_model* m, int n_rows, int max_ctx, luce_s
     return ok();
 }
 
-int luce_decode_step(const luce_model* m, const luce_slot* slots, const int32_t* rows_per_slot, int n_seq,
-                     float* x, float* logits, int32_t* argmax, void* ws, size_t ws_bytes, void* stream)
+// A slot as the step addresses it: a flat cache [n_layers][Hkv][cap][D], or
+// pages of kPageKeys tokens [n_pages][n_layers][Hkv][kPageKeys][D] named by
+// a table (device copy for attention, host copy for the appends).
+struct StepSlot {
+    __half* k;
+    __half* v;
+    int len;
+    int cap;
+    const int32_t* table;       // nullptr for a flat cache
+    const int32_t* table_host;
+};
+
+static int decode_step_impl(const luce_model* m, const StepSlot* slots, const int32_t* rows_per_slot, int n_seq,
+                            float* x, float* logits, int32_t* argmax, void* ws, size_t ws_bytes, void* stream,
+                            const char* who)
 {
-    const char* who = "decode_step";
-    int rc = check_model(m, who);
-    if (rc) return rc;
-    REQUIRE(slots && rows_per_slot && x && ws, LUCE_EINVAL, "%s: null slots/rows/x/ws", who);
-    REQUIRE(n_seq >= 1 && n_seq <= LUCE_MAX_SEQ, LUCE_EINVAL,
-            "%s: n_seq=%d outside 1..%d (more than %d slots are refused)", who, n_seq, LUCE_MAX_SEQ, LUCE_MAX_SEQ);
+    REQUIRE(x && ws, LUCE_EINVAL, "%s: null x/ws", who);
     REQUIRE(aligned(x, 16) && aligned(ws, 256), LUCE_EINVAL, "%s: x must be 16-byte and ws 256-byte aligned", who);
     REQUIRE(!(logits || argmax) || (m->vocab > 0 && m->final_norm && m->head_q && m->head_d), LUCE_EINVAL,
             "%s: logits/argmax need vocab > 0 and the head weights", who);
@@ -399,21 +466,8 @@ int luce_decode_step(const luce_model* m, const luce_slot* slots, const int32_t*
     const int H = m->hidden, Hq = m->n_q_heads, Hkv = m->n_kv_heads, D = m->head_dim, F = m->ffn;
     int T = 0, max_len = 1;
     for (int s = 0; s < n_seq; ++s) {
-        const luce_slot& sl = slots[s];
-        const int n = rows_per_slot[s];
-        REQUIRE(n >= 1 && n <= LUCE_MAX_ROWS_PER_SEQ, LUCE_EINVAL, "%s: slot %d has %d rows (1..%d)", who, s, n,
-                LUCE_MAX_ROWS_PER_SEQ);
-        REQUIRE(sl.k && sl.v && aligned(sl.k, 16) && aligned(sl.v, 16), LUCE_EINVAL,
-                "%s: slot %d cache null or not 16-byte aligned", who, s);
-        REQUIRE(sl.len >= 0 && sl.cap >= 1 && (int64_t)sl.len + n <= sl.cap, LUCE_EINVAL,
-                "%s: slot %d len=%d + rows=%d exceeds cap=%d", who, s, sl.len, n, sl.cap);
-        REQUIRE(sl.len + n <= kMaxKeys, LUCE_EUNSUPPORTED, "%s: slot %d would hold %d keys (at most %d)", who, s,
-                sl.len + n, kMaxKeys);
-        for (int p = 0; p < s; ++p)
-            REQUIRE(slots[p].k != sl.k && slots[p].v != sl.v, LUCE_EINVAL, "%s: slots %d and %d share a cache", who,
-                    p, s);
-        T += n;
-        max_len = std::max(max_len, sl.len + n);
+        T += rows_per_slot[s];
+        max_len = std::max(max_len, slots[s].len + rows_per_slot[s]);
     }
     REQUIRE(T <= LUCE_MAX_ROWS, LUCE_EINVAL, "%s: %d rows > %d", who, T, LUCE_MAX_ROWS);
     for (int l = 0; l < m->n_layers; ++l) {
@@ -466,25 +520,43 @@ int luce_decode_step(const luce_model* m, const luce_slot* slots, const int32_t*
     cudaError_t e = cudaSuccess;
 
     const float scale = (float)(1.0 / sqrt((double)D));
+    const int64_t page_elems = (int64_t)Hkv * kPageKeys * D;   // one layer of one page
+    const int64_t page_stride = (int64_t)m->n_layers * page_elems;
     for (int l = 0; l < m->n_layers; ++l) {
         const luce_layer& w = m->layers[l];
         KvRows kv{};
         AttnRows ar{};
         kv.n_rows = ar.n_rows = T;
         for (int r = 0; r < T; ++r) {
-            const luce_slot& sl = slots[slot_of[r]];
-            const int64_t head_stride = (int64_t)sl.cap * D;
-            const int64_t layer_off = (int64_t)l * Hkv * head_stride;
-            __half* kb = reinterpret_cast<__half*>(sl.k) + layer_off;
-            __half* vb = reinterpret_cast<__half*>(sl.v) + layer_off;
-            kv.row[r].k = kb + (int64_t)pos.pos[r] * D;
-            kv.row[r].v = vb + (int64_t)pos.pos[r] * D;
-            kv.row[r].head_stride = head_stride;
-            ar.row[r].k = kb;
-            ar.row[r].v = vb;
-            ar.row[r].head_stride = head_stride;
+            const StepSlot& sl = slots[slot_of[r]];
+            const int p = pos.pos[r];
+            if (sl.table) {
+                const int64_t at = (int64_t)sl.table_host[p / kPageKeys] * page_stride + (int64_t)l * page_elems +
+                                   (int64_t)(p % kPageKeys) * D;
+                kv.row[r].k = sl.k + at;
+                kv.row[r].v = sl.v + at;
+                kv.row[r].head_stride = (int64_t)kPageKeys * D;
+                ar.row[r].k = sl.k + (int64_t)l * page_elems;
+                ar.row[r].v = sl.v + (int64_t)l * page_elems;
+                ar.row[r].head_stride = (int64_t)kPageKeys * D;
+                ar.row[r].pages = sl.table;
+                ar.row[r].page_stride = page_stride;
+            } else {
+                const int64_t head_stride = (int64_t)sl.cap * D;
+                const int64_t layer_off = (int64_t)l * Hkv * head_stride;
+                __half* kb = sl.k + layer_off;
+                __half* vb = sl.v + layer_off;
+                kv.row[r].k = kb + (int64_t)p * D;
+                kv.row[r].v = vb + (int64_t)p * D;
+                kv.row[r].head_stride = head_stride;
+                ar.row[r].k = kb;
+                ar.row[r].v = vb;
+                ar.row[r].head_stride = head_stride;
+                ar.row[r].pages = nullptr;
+                ar.row[r].page_stride = 0;
+            }
             ar.row[r].tok_stride = D;
-            ar.row[r].len = pos.pos[r] + 1;
+            ar.row[r].len = p + 1;
             ar.row[r].chunk = attn_chunk_keys(ar.row[r].len);
         }
         int c = 0;
@@ -524,6 +596,90 @@ int luce_decode_step(const luce_model* m, const luce_slot* slots, const int32_t*
         if (argmax && (e = launch_argmax(logits, T, m->vocab, argmax, st))) return cuda_status(e, who);
     }
     return ok();
+}
+
+static int check_rows(const int32_t* rows_per_slot, int s, const char* who)
+{
+    const int n = rows_per_slot[s];
+    REQUIRE(n >= 1 && n <= LUCE_MAX_ROWS_PER_SEQ, LUCE_EINVAL, "%s: slot %d has %d rows (1..%d)", who, s, n,
+            LUCE_MAX_ROWS_PER_SEQ);
+    return LUCE_OK;
+}
+
+int luce_decode_step(const luce_model* m, const luce_slot* slots, const int32_t* rows_per_slot, int n_seq,
+                     float* x, float* logits, int32_t* argmax, void* ws, size_t ws_bytes, void* stream)
+{
+    const char* who = "decode_step";
+    int rc = check_model(m, who);
+    if (rc) return rc;
+    REQUIRE(slots && rows_per_slot, LUCE_EINVAL, "%s: null slots/rows", who);
+    REQUIRE(n_seq >= 1 && n_seq <= LUCE_MAX_SEQ, LUCE_EINVAL,
+            "%s: n_seq=%d outside 1..%d (more than %d slots are refused)", who, n_seq, LUCE_MAX_SEQ, LUCE_MAX_SEQ);
+    StepSlot ss[LUCE_MAX_SEQ];
+    for (int s = 0; s < n_seq; ++s) {
+        const luce_slot& sl = slots[s];
+        if ((rc = check_rows(rows_per_slot, s, who))) return rc;
+        const int n = rows_per_slot[s];
+        REQUIRE(sl.k && sl.v && aligned(sl.k, 16) && aligned(sl.v, 16), LUCE_EINVAL,
+                "%s: slot %d cache null or not 16-byte aligned", who, s);
+        REQUIRE(sl.len >= 0 && sl.cap >= 1 && (int64_t)sl.len + n <= sl.cap, LUCE_EINVAL,
+                "%s: slot %d len=%d + rows=%d exceeds cap=%d", who, s, sl.len, n, sl.cap);
+        REQUIRE(sl.len + n <= kMaxKeys, LUCE_EUNSUPPORTED, "%s: slot %d would hold %d keys (at most %d)", who, s,
+                sl.len + n, kMaxKeys);
+        for (int p = 0; p < s; ++p)
+            REQUIRE(slots[p].k != sl.k && slots[p].v != sl.v, LUCE_EINVAL, "%s: slots %d and %d share a cache", who,
+                    p, s);
+        ss[s] = StepSlot{reinterpret_cast<__half*>(sl.k), reinterpret_cast<__half*>(sl.v), sl.len, sl.cap, nullptr,
+                         nullptr};
+    }
+    return decode_step_impl(m, ss, rows_per_slot, n_seq, x, logits, argmax, ws, ws_bytes, stream, who);
+}
+
+int luce_decode_step_paged(const luce_model* m, const luce_paged_slot* slots, const int32_t* rows_per_slot,
+                           int n_seq, float* x, float* logits, int32_t* argmax, void* ws, size_t ws_bytes,
+                           void* stream)
+{
+    const char* who = "decode_step_paged";
+    int rc = check_model(m, who);
+    if (rc) return rc;
+    REQUIRE(slots && rows_per_slot, LUCE_EINVAL, "%s: null slots/rows", who);
+    REQUIRE(n_seq >= 1 && n_seq <= LUCE_MAX_SEQ, LUCE_EINVAL,
+            "%s: n_seq=%d outside 1..%d (more than %d slots are refused)", who, n_seq, LUCE_MAX_SEQ, LUCE_MAX_SEQ);
+    StepSlot ss[LUCE_MAX_SEQ];
+    for (int s = 0; s < n_seq; ++s) {
+        const luce_paged_slot& sl = slots[s];
+        if ((rc = check_rows(rows_per_slot, s, who))) return rc;
+        const int n = rows_per_slot[s];
+        REQUIRE(sl.k_pool && sl.v_pool && aligned(sl.k_pool, 16) && aligned(sl.v_pool, 16), LUCE_EINVAL,
+                "%s: slot %d pool null or not 16-byte aligned", who, s);
+        REQUIRE(sl.table && sl.table_host && aligned(sl.table, 4), LUCE_EINVAL, "%s: slot %d table null", who, s);
+        REQUIRE(sl.len >= 0 && sl.len + n <= kMaxKeys, LUCE_EINVAL, "%s: slot %d len=%d + rows=%d outside 0..%d",
+                who, s, sl.len, n, kMaxKeys);
+        const int need = (sl.len + n + kPageKeys - 1) / kPageKeys;
+        REQUIRE(sl.n_pages >= 1 && sl.n_table >= need, LUCE_EINVAL, "%s: slot %d table has %d entries, needs %d",
+                who, s, sl.n_table, need);
+        for (int i = 0; i < need; ++i)
+            REQUIRE(sl.table_host[i] >= 0 && sl.table_host[i] < sl.n_pages, LUCE_EINVAL,
+                    "%s: slot %d table[%d]=%d outside [0, %d)", who, s, i, sl.table_host[i], sl.n_pages);
+        ss[s] = StepSlot{reinterpret_cast<__half*>(sl.k_pool), reinterpret_cast<__half*>(sl.v_pool), sl.len,
+                         need * kPageKeys, sl.table, sl.table_host};
+    }
+    // pages written by this step belong to their slot alone within the call
+    for (int s = 0; s < n_seq; ++s) {
+        const luce_paged_slot& a = slots[s];
+        for (int pg = a.len / kPageKeys; pg <= (a.len + rows_per_slot[s] - 1) / kPageKeys; ++pg)
+            for (int o = 0; o < n_seq; ++o) {
+                const luce_paged_slot& b = slots[o];
+                if (b.k_pool != a.k_pool && b.v_pool != a.v_pool) continue;
+                const int nb = (b.len + rows_per_slot[o] + kPageKeys - 1) / kPageKeys;
+                for (int i = 0; i < nb; ++i)
+                    REQUIRE(o == s ? (i == pg || b.table_host[i] != a.table_host[pg])
+                                   : b.table_host[i] != a.table_host[pg],
+                            LUCE_EINVAL, "%s: page %d written for slot %d is also referenced by slot %d", who,
+                            a.table_host[pg], s, o);
+            }
+    }
+    return decode_step_impl(m, ss, rows_per_slot, n_seq, x, logits, argmax, ws, ws_bytes, stream, who);
 }
 
 }  // extern "C"

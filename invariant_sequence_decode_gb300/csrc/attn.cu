@@ -73,8 +73,9 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
-// Stage keys [j0, j0 + 128) of a chunk (rows tok_stride halves apart from
-// src) in a tile; keys at or past nvalid are zero-filled without a read.
+// Stage keys [j0, j0 + 128) of a chunk (their rows tok_stride halves apart
+// from src, the tile's first key) in a tile; keys at or past nvalid are
+// zero-filled without a read.
 __device__ __forceinline__ void stage_tile(__half* dst, const __half* src, int64_t tok_stride, int j0, int nvalid)
 {
     const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
@@ -82,7 +83,7 @@ __device__ __forceinline__ void stage_tile(__half* dst, const __half* src, int64
     for (int i = threadIdx.x; i < kTileKeys * 16; i += kAttnThreads) {
         const int j = i >> 4, c = i & 15;
         const bool ok = j0 + j < nvalid;
-        cp_async16(d + 2 * tile_off(j, c), ok ? src + (int64_t)(j0 + j) * tok_stride + c * 8 : src, ok ? 16 : 0);
+        cp_async16(d + 2 * tile_off(j, c), ok ? src + (int64_t)j * tok_stride + c * 8 : src, ok ? 16 : 0);
     }
 }
 
@@ -136,12 +137,19 @@ attn_kernel(const float* __restrict__ q, int64_t ldq, AttnRows rows, int Hq, int
     const int nvalid = min(CH, row.len - key0);
     const int ntile = (nvalid + kTileKeys - 1) / kTileKeys;  // tiles of this chunk: 1 or 2
     const int h0 = g * GQ;
-    const __half* kbase = row.k + g * row.head_stride + (int64_t)key0 * row.tok_stride;
-    const __half* vbase = row.v + g * row.head_stride + (int64_t)key0 * row.tok_stride;
+    // the first key of tile t (keys key0 + 128t ..) of KV head g: tiles
+    // never straddle a page, so within a tile keys are tok_stride apart
+    auto tile_base = [&](const __half* base, int t) -> const __half* {
+        const int key = key0 + kTileKeys * t;
+        return row.pages ? base + (int64_t)__ldg(row.pages + (key >> 7)) * row.page_stride + g * row.head_stride
+                         : base + g * row.head_stride + (int64_t)key * row.tok_stride;
+    };
+    const __half* kbase = tile_base(row.k, 0);
+    const __half* vbase = tile_base(row.v, 0);
     if (tid == 0) {
-        // stage the chunk's K and V rows in L2 while the previous kernel ends
-        // (a cache hint only: the rows it writes are read after pdl_wait)
-        const uint32_t span = (uint32_t)(((int64_t)(nvalid - 1) * row.tok_stride + kHeadDim) * 2);
+        // stage the first tile's K and V rows in L2 while the previous kernel
+        // ends (a cache hint only: the rows it writes are read after pdl_wait)
+        const uint32_t span = (uint32_t)(((int64_t)(min(nvalid, kTileKeys) - 1) * row.tok_stride + kHeadDim) * 2);
         prefetch_l2(kbase, span);
         prefetch_l2(vbase, span);
     }
@@ -172,12 +180,12 @@ attn_kernel(const float* __restrict__ q, int64_t ldq, AttnRows rows, int Hq, int
             }
         }
     };
-    auto load_k = [&](int j0) {
+    auto load_k = [&](const __half* kt, int j0) {
         const int ja = j0 + 16 * warp + gr, jb = ja + 8;
-        load_row(kbase + (int64_t)ja * row.tok_stride + 32 * tq, ja < nvalid, ka);
-        load_row(kbase + (int64_t)jb * row.tok_stride + 32 * tq, jb < nvalid, kb);
+        load_row(kt + (int64_t)(ja - j0) * row.tok_stride + 32 * tq, ja < nvalid, ka);
+        load_row(kt + (int64_t)(jb - j0) * row.tok_stride + 32 * tq, jb < nvalid, kb);
     };
-    load_k(0);
+    load_k(kbase, 0);
 
     // q as B fragments: step s, lane (head n = lane / 4, t = lane % 4) holds
     // q[n][32t + 4s .. 32t + 4s + 3]; heads past the group are zero
@@ -216,7 +224,7 @@ attn_kernel(const float* __restrict__ q, int64_t ldq, AttnRows rows, int Hq, int
     };
     scores(0);
     if (ntile == 2) {
-        load_k(kTileKeys);
+        load_k(tile_base(row.k, 1), kTileKeys);
         scores(kTileKeys);
     }
     __syncthreads();
@@ -278,7 +286,7 @@ attn_kernel(const float* __restrict__ q, int64_t ldq, AttnRows rows, int Hq, int
     values(0);
     if (ntile == 2) {
         __syncthreads();  // every warp is done with the first V tile
-        stage_tile(sm.vt, vbase, row.tok_stride, kTileKeys, nvalid);
+        stage_tile(sm.vt, tile_base(row.v, 1), row.tok_stride, kTileKeys, nvalid);
         cp_async_commit();
         cp_async_wait_all();
         __syncthreads();

@@ -22,8 +22,11 @@ struct KvRows {
     int n_rows;
 };
 
-// One query row of decode attention: its keys are k/v[g*head_stride + j*tok_stride + d]
-// for j < len; chunk0 is the index of its first split-K chunk in the scratch.
+// One query row of decode attention over keys j < len; chunk0 is the index
+// of its first split-K chunk in the scratch.  Flat cache (pages == nullptr):
+// element d of key j of KV head g is k[g*head_stride + j*tok_stride + d].
+// Paged cache: key j lives in page pages[j / 128] at
+// k[pages[j / 128]*page_stride + g*head_stride + (j % 128)*tok_stride + d].
 struct AttnRow {
     const __half* k;
     const __half* v;
@@ -32,6 +35,8 @@ struct AttnRow {
     int len;
     int chunk0;
     int chunk;  // keys per split-K chunk of this row: attn_chunk_keys(len)
+    const int32_t* pages;  // device page table (128 keys per page) or nullptr
+    int64_t page_stride;
 };
 struct AttnRows {
     AttnRow row[16];

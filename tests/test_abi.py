@@ -150,3 +150,54 @@ def test_step_layout_is_monotone_and_part_is_last(lib):
     assert lib.luce_decode_step_layout(ctypes.byref(m), 4, 32768, ctypes.byref(lay2)) == 0
     assert lay2.total > lay.total and lay2.xf_d == lay.xf_d and lay.part >= lay.xf_d
     assert all(getattr(lay, n) % 256 == 0 for n, _ in luce.StepLayoutC._fields_)
+
+
+def paged_slots(specs):
+    """specs: (len, table list, n_pages, pool id); keeps the tables alive."""
+    arr = (luce.PagedSlotC * len(specs))()
+    keep = []
+    for i, (ln, table, n_pages, pool) in enumerate(specs):
+        t = (ctypes.c_int32 * max(1, len(table)))(*table)
+        keep.append(t)
+        arr[i] = luce.PagedSlotC(P + pool * 0x1000000, P + pool * 0x1000000 + 0x800000, P + 0x40000 * (i + 1),
+                                 t, len(table), n_pages, ln)
+    return arr, keep
+
+
+def test_decode_step_paged_refusals(lib):
+    m, _keep = fake_model()
+    big = 1 << 40
+    step = lib.luce_decode_step_paged
+    ok, k1 = paged_slots([(100, [3, 1], 4, 0), (5, [0], 4, 1)])
+    # a table entry outside the pool
+    bad, k2 = paged_slots([(200, [3, 9], 4, 0)])
+    assert step(ctypes.byref(m), bad, rows([1]), 1, P, None, None, P, big, None) == luce.LUCE_EINVAL
+    assert "outside" in status_msg(lib)
+    # too few table entries for len + rows (130 keys need 2 pages)
+    short, k3 = paged_slots([(127, [2], 4, 0)])
+    assert step(ctypes.byref(m), short, rows([3]), 1, P, None, None, P, big, None) == luce.LUCE_EINVAL
+    # two slots of one pool writing / reading the same page
+    clash, k4 = paged_slots([(10, [2], 4, 0), (20, [2], 4, 0)])
+    assert step(ctypes.byref(m), clash, rows([1, 1]), 2, P, None, None, P, big, None) == luce.LUCE_EINVAL
+    assert "also referenced" in status_msg(lib)
+    # more than four slots, too many rows, workspace too small
+    five, k5 = paged_slots([(3, [i], 8, i) for i in range(5)])
+    assert step(ctypes.byref(m), five, rows([1] * 5), 5, P, None, None, P, big, None) == luce.LUCE_EINVAL
+    assert step(ctypes.byref(m), ok, rows([1, 5]), 2, P, None, None, P, big, None) == luce.LUCE_EINVAL
+    assert step(ctypes.byref(m), ok, rows([1, 1]), 2, P, None, None, P, 1024, None) == luce.LUCE_ENOSPACE
+
+
+def test_decode_attn_paged_refusals(lib):
+    ws = 1 << 30
+    def pv(specs):
+        arr = (luce.PagedViewC * len(specs))()
+        for i, (ln, nq, r0) in enumerate(specs):
+            arr[i] = luce.PagedViewC(P, P + 0x800000, P + 0x100000, ln, nq, r0)
+        return arr
+    f = lib.luce_decode_attn_paged
+    assert f(P, pv([(10, 1, 0)] * 5), 5, 8, 2, 128, 0.1, P, P, ws, None) == luce.LUCE_EINVAL
+    assert f(P, pv([(10, 1, 1)]), 1, 8, 2, 128, 0.1, P, P, ws, None) == luce.LUCE_EINVAL   # row 0 uncovered
+    assert f(P, pv([(2, 3, 0)]), 1, 8, 2, 128, 0.1, P, P, ws, None) == luce.LUCE_EINVAL    # len < n_q
+    assert f(P, pv([(10, 1, 0)]), 1, 8, 2, 64, 0.1, P, P, ws, None) == luce.LUCE_EUNSUPPORTED
+    assert f(P, pv([(10, 1, 0)]), 1, 8, 2, 128, 0.1, P, P, 16, None) == luce.LUCE_ENOSPACE
+    assert f(P, pv([(200000, 1, 0)]), 1, 8, 2, 128, 0.1, P, P, ws, None) == luce.LUCE_EUNSUPPORTED
