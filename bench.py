@@ -22,6 +22,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -206,6 +207,36 @@ def matvec_roofline(torch, luce, wl, L: Layer27B, T: int, reps: int) -> dict:
     return out
 
 
+def attention_detail(torch, luce, wl, flush, steps: int, peak_gbs: float) -> dict:
+    """Decode attention alone (chunk kernel + merge kernel, CUDA events on the
+    launching stream, L2 flushed): the 27B layer's 4 x 2,051 keys at 40/8
+    heads and the long-context workload, 4 sequences with key counts uniform
+    on [16384, 32768] at 32/8 heads.  Algorithmic bytes = every K and V row
+    once (f16) + q and out."""
+    cu = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    out = {}
+    for name, seed, lens, hq, hkv in (("27b_layer_4x2051", 1, [2051] * 4, 40, 8),
+                                      ("long_4x16k_32k", 3, wl.lens(3, 4, 16384, 32768), 32, 8)):
+        d = wl.Dims(0, hq, hkv, 128, 0)
+        views = []
+        for s, L in enumerate(lens):
+            k, v = wl.cache_host(seed, s, 0, d, L, L)
+            views.append(luce.SeqView(cu(k), cu(v), L, 1, s))
+        q = cu(wl.qvec(seed, len(lens), hq))
+        o = torch.empty_like(q)
+        ws = torch.empty(luce.luce_decode_attn_workspace_size(len(lens), hq, 128, max(lens)), dtype=torch.uint8,
+                         device="cuda")
+        fn = lambda: luce.luce_decode_attn_multiseq(q, views, hkv, 1.0 / math.sqrt(128), o, ws)
+        for _ in range(3):
+            fn()
+        ms = statistics.median(time_steps(torch, fn, flush, steps))
+        b = sum(lens) * hkv * 128 * 2 * 2 + 2 * q.numel() * 4
+        out[name] = {"lens": lens, "heads": f"{hq}/{hkv}", "us": round(ms * 1e3, 2),
+                     "gbps": round(b / (ms / 1e3) / 1e9, 1), "frac": round(b / (ms / 1e3) / 1e9 / peak_gbs, 4)}
+        del views, q, o, ws
+    return out
+
+
 def verify64_detail(torch, luce, wl, flush, steps: int) -> dict:
     """Wide speculative verify: 4 slots x 2/3/4 rows through 64 distinct layers
     plus the 151,936 x 5120 q8_0 head (logits and argmax), cache lengths
@@ -328,10 +359,12 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     detail["matvec_gbps_by_ntok"] = {T: round(v["all"]["gbps"], 1) for T, v in mv.items()}
     detail["matvec_by_proj_ntok4"] = {k: {"gbps": round(v["gbps"], 1), "us": round(v["ms"] * 1e3, 2)}
                                       for k, v in mv["4"].items() if k != "all"}
+    detail["attention"] = attention_detail(torch, luce, wl, L.flush_l2, max(5, args.steps), peaks()["hbm_gbs"])
     detail["verify64"] = verify64_detail(torch, luce, wl, L.flush_l2, steps=5)
     detail["layer_weight_bytes"] = layer_bytes(L.d)
     detail["step_bytes_algorithmic"] = layer_bytes(L.d) + n_seq * 2 * L.d.n_kv_heads * KV_TOKENS * 128 * 2
     detail["step_gbps"] = detail["step_bytes_algorithmic"] / (ms_per_step / 1e3) / 1e9
+    detail["step_frac"] = round(detail["step_gbps"] / peaks()["hbm_gbs"], 4)
 
     pk = peaks()
     a = mv["4"]["all"]["gbps"]
