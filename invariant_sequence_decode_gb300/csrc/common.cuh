@@ -72,10 +72,7 @@ static inline cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
-constexpr int kQK = 32;
 constexpr int kHeadDim = 128;
-constexpr int kMaxRows = 16;
-constexpr int kMaxSeq = 4;
 constexpr int kAttnChunk = 256;  // largest split-K chunk (keys)
 
 // ---------------------------------------------------------------- loads
@@ -150,20 +147,6 @@ __device__ __forceinline__ float block_dot8_f(const uint32_t (&w)[8], const uint
 #pragma unroll
     for (int i = 1; i < 8; ++i) s = __dp4a((int)w[i], (int)a[i], s);
     return __fsub_rn(__int_as_float(s), 12582912.0f);
-}
-
-// Integer dot of one 32-value block held as two 16-byte vectors per side.
-__device__ __forceinline__ int block_dot(const int4 w0, const int4 w1, const int4 a0, const int4 a1)
-{
-    int s = __dp4a(w0.x, a0.x, 0);
-    s = __dp4a(w0.y, a0.y, s);
-    s = __dp4a(w0.z, a0.z, s);
-    s = __dp4a(w0.w, a0.w, s);
-    s = __dp4a(w1.x, a1.x, s);
-    s = __dp4a(w1.y, a1.y, s);
-    s = __dp4a(w1.z, a1.z, s);
-    s = __dp4a(w1.w, a1.w, s);
-    return s;
 }
 
 // One quantization code: q = round-half-away(x / d) clamped to [-127, 127];

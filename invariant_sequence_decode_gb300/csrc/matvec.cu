@@ -20,12 +20,15 @@
 // instruction reads KL consecutive 32-byte blocks of each of 32/KL rows
 // (KL*32 contiguous bytes per row, one 32-byte load per lane, L1 bypassed).
 // Each activation block is loaded once per lane and reused for its G rows,
-// and is one address shared by the 32/KL lanes of a kb column; this keeps the
-// L1-to-register traffic per weight block at (G*32 + T*36)/G bytes, the
-// quantity that bounds this kernel at T >= 2.  A lane keeps the next block of
-// its G rows in flight while it computes the current one.  The chain values
-// meet in shared memory, where one thread per (row, token) applies the
-// butterfly's pairings in the same order.
+// and is one address shared by the 32/KL lanes of a kb column, which keeps
+// the L1-to-register traffic per weight block at (G*32 + T*36)/G bytes (the
+// limit of a first version with one row per warp).  A lane keeps the next
+// stage of its G rows in flight while it computes the current one; the
+// chain values meet in shared memory, where one thread per (row, token)
+// applies the butterfly's pairings in the same order.  The int32 block dot
+// reaches fp32 either by conversion or through an exact biased dp4a chain;
+// the two give the same value.  The decode step's q|k|v projection uses the
+// same chains with a RoPE / K/V-append epilogue (q8_qkv_rope_kernel).
 #include "common.cuh"
 #include "kernels.h"
 
