@@ -36,6 +36,9 @@
 // and optionally quantizes out to q8_0 blocks (the Wo projection's input).
 // Every chunking and reduction order depends only on the row's own key
 // count, never on the other rows, on which CTA merges or on the grid.
+// A row's cache is flat or paged: pages hold 128 keys, one tile, so only the
+// address of a tile's first key comes from the page table and a paged cache
+// gives the flat cache's bits.
 // The split of q assumes |q| < 65504 (the f16 range); larger entries make
 // the row's scores non-finite.
 #include <math.h>
