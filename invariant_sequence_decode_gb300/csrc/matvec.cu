@@ -163,7 +163,7 @@ cudaError_t launch_matvec(const int8_t* wq, const __half* wd, int N, int K, cons
     case TT: return launch_t<TT, KK, GG, PP, BB>(wq, wd, N, K, aq, ad, y, ldy, resid, ldr, s);
         LUCE_MV(1, 8, 1, false, true)
         LUCE_MV(2, 8, 2, false, false)
-        LUCE_MV(3, 8, 2, false, false)
+        LUCE_MV(3, 8, 3, false, false)
         LUCE_MV(4, 8, 4, false, false)
         LUCE_MV(5, 8, 4, false, true)
         LUCE_MV(6, 8, 4, false, true)
@@ -264,13 +264,14 @@ cudaError_t launch_qkv_rope(const int8_t* wq, const __half* wd, int K, const int
                             float* qkv, int Hq, int Hkv, const RowPos& pos, const RopeFreq& f, float* q_rot,
                             const KvRows& kv, cudaStream_t s)
 {
-    // the plain kernel's launch shapes, except G = 4 at T = 12 (P must divide 64)
+    // the plain kernel's launch shapes, except G = 4 where the plain kernel
+    // takes G = 3 (T = 3, 12): the rotation pairs P = 2G must tile 64
     switch (T) {
 #define LUCE_QKV(TT, GG, BB) \
     case TT: return launch_qkv_t<TT, GG, BB>(wq, wd, K, aq, ad, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
         LUCE_QKV(1, 1, true)
         LUCE_QKV(2, 2, false)
-        LUCE_QKV(3, 2, false)
+        LUCE_QKV(3, 4, false)
         LUCE_QKV(4, 4, false)
         LUCE_QKV(5, 4, true)
         LUCE_QKV(6, 4, true)
