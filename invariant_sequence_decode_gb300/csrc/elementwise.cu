@@ -112,6 +112,8 @@ rmsnorm_quant_kernel(const float* __restrict__ x, int H, const float* __restrict
     cluster.sync();  // every CTA's sum is in place
     float tot = *cluster.map_shared_rank(&part, 0);
     for (int cc = 1; cc < kNormCtas; ++cc) tot = __fadd_rn(tot, *cluster.map_shared_rank(&part, cc));
+    // done reading the other CTAs' sums: arrive now, wait only before leaving
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(tot, (float)H), eps)));
 #pragma unroll
     for (int k = 0; k < (REG ? kNormMaxPerThread : 1); ++k) {
@@ -126,7 +128,7 @@ rmsnorm_quant_kernel(const float* __restrict__ x, int H, const float* __restrict
             if (lane == 0) d[(size_t)t * nb + b] = dd;
         }
     }
-    cluster.sync();  // no CTA leaves while another may still read its sum
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");  // no CTA leaves while another may still read its sum
 }
 
 cudaError_t launch_rmsnorm_quant(const float* x, int T, int H, const float* gamma, float eps,
