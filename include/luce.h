@@ -69,6 +69,19 @@ int luce_version(void);
 uint64_t luce_launch_count(void);
 
 /*
+ * Bounded waits that expired on the current device.  The TMA-ring matvec
+ * (1..4 rows, K a multiple of 256) waits on shared-memory barriers for its
+ * weight copies; every such wait gives up after about one second, adds one to
+ * this device counter and leaves the outputs of the rows still pending
+ * unwritten, so a stalled copy engine surfaces as an error here instead of a
+ * hung stream.  A healthy run reads 0.
+ *   count (host) receives the counter; reset != 0 clears it afterwards.
+ * Synchronises the device (it copies from device memory).  Returns LUCE_OK,
+ * LUCE_EINVAL (null count) or LUCE_ECUDA.
+ */
+int luce_wait_timeouts(uint32_t* count, int reset);
+
+/*
  * Activation quantization to q8_0 blocks [qfuse, item 2: the consumer's
  * division and rounding convention; ds4-604, Commit walkthrough].
  * For each row t and block b of 32 values: amax = max|x| (NaN skipped),

@@ -80,7 +80,7 @@ EXPORTS = ("luce_last_error", "luce_version", "luce_launch_count", "luce_q8_quan
            "luce_q8_block_dots", "luce_rope_posvec", "luce_kv_append", "luce_decode_attn_multiseq",
            "luce_decode_attn_workspace_size", "luce_decode_step_layout", "luce_decode_step",
            "luce_decode_attn_multiseq_noalloc", "luce_decode_attn_noalloc_max_bytes", "luce_decode_attn_paged",
-           "luce_decode_step_paged")
+           "luce_decode_step_paged", "luce_wait_timeouts")
 
 _lib = None
 
@@ -117,6 +117,7 @@ def load_library(path: str = LIB_PATH):
     lib.luce_decode_step_paged.argtypes = [ctypes.POINTER(ModelC), ctypes.POINTER(PagedSlotC),
                                            ctypes.POINTER(ctypes.c_int32), i32, vp, vp, vp, vp, sz, vp]
     lib.luce_decode_attn_noalloc_max_bytes.restype = sz
+    lib.luce_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
     for name in EXPORTS:
         if name not in ("luce_last_error", "luce_version", "luce_launch_count", "luce_decode_attn_workspace_size",
                         "luce_decode_attn_noalloc_max_bytes"):
@@ -128,6 +129,13 @@ def load_library(path: str = LIB_PATH):
 def launch_count() -> int:
     """Kernel launches the library has enqueued so far (all threads)."""
     return int(load_library().luce_launch_count())
+
+
+def wait_timeouts(reset: bool = False) -> int:
+    """Bounded device waits that expired on the current device (0 on a healthy run)."""
+    n = ctypes.c_uint32(0)
+    _check(load_library().luce_wait_timeouts(ctypes.byref(n), 1 if reset else 0))
+    return int(n.value)
 
 
 def _check(rc: int):

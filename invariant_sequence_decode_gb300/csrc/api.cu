@@ -92,6 +92,12 @@ int luce_version(void) { return 10000; }
 
 uint64_t luce_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+int luce_wait_timeouts(uint32_t* count, int reset)
+{
+    REQUIRE(count, LUCE_EINVAL, "wait_timeouts: null count");
+    return cuda_status(read_wait_timeouts(count, reset != 0), "wait_timeouts");
+}
+
 int luce_q8_quantize_act(const float* x, int T, int K, int64_t ldx, int8_t* q, float* d, void* stream)
 {
     REQUIRE(x && q && d, LUCE_EINVAL, "quantize_act: null pointer");

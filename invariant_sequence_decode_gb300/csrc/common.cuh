@@ -191,6 +191,20 @@ __device__ __forceinline__ float warp_max(float v)
     return v;
 }
 
+// The 32 chain values of one (row, token), combined by the xor butterfly's
+// pairings: v[i] += v[i + off] for off = 16, 8, 4, 2, 1.
+__device__ __forceinline__ float q8_butterfly(const float* __restrict__ part)
+{
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = part[i];
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1)
+#pragma unroll
+        for (int i = 0; i < off; ++i) v[i] = __fadd_rn(v[i], v[i + off]);
+    return v[0];
+}
+
 // ---------------------------------------------------------------- RoPE
 
 // Rotation of one (x0, x1) pair by (c, s) in fp32, no contraction.

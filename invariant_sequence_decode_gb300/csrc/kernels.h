@@ -63,6 +63,16 @@ cudaError_t launch_matvec(const int8_t* wq, const __half* wd, int N, int K, cons
                           const float* ad, int T, float* y, int64_t ldy, const float* resid,
                           int64_t ldr, cudaStream_t s);
 
+// The TMA-ring matvec (1..4 rows): cudaErrorNotSupported, with nothing
+// launched, when K % 256 != 0, an operand is not 16-byte aligned or the
+// tensor-map encoder is unavailable.
+cudaError_t launch_matvec_tma(const int8_t* wq, const __half* wd, int N, int K, const int8_t* aq, const float* ad,
+                              int T, float* y, int64_t ldy, const float* resid, int64_t ldr, cudaStream_t s);
+
+// Bounded waits of the TMA-ring kernels that expired on the current device
+// (synchronous); reset clears the counter.
+cudaError_t read_wait_timeouts(uint32_t* count, bool reset);
+
 // The step's q|k|v projection (N = (Hq + 2*Hkv) * 128 rows) with RoPE of the
 // q and k heads at each row's position, q heads to q_rot [T][Hq][128], k and v
 // heads appended as binary16 at rows' K/V destinations; qkv [T][N] also written.

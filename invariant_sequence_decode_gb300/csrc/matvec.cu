@@ -89,20 +89,6 @@ __device__ __forceinline__ void q8_chains(const int8_t* __restrict__ wq, const _
     }
 }
 
-// The 32 chain values of one (row, token), combined by the xor butterfly's
-// pairings: v[i] += v[i + off] for off = 16, 8, 4, 2, 1.
-__device__ __forceinline__ float q8_butterfly(const float* __restrict__ part)
-{
-    float v[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = part[i];
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1)
-#pragma unroll
-        for (int i = 0; i < off; ++i) v[i] = __fadd_rn(v[i], v[i + off]);
-    return v[0];
-}
-
 template <int T, int KL, int G, bool PF, bool BIAS>
 __global__ void __launch_bounds__(32 * (32 / KL))
 q8_matvec_kernel(const int8_t* __restrict__ wq, const __half* __restrict__ wd, int N, int K,
@@ -155,9 +141,16 @@ cudaError_t launch_matvec(const int8_t* wq, const __half* wd, int N, int K, cons
                           const float* ad, int T, float* y, int64_t ldy, const float* resid,
                           int64_t ldr, cudaStream_t s)
 {
-    // KL (lanes per row), G (rows per lane), the L2 prefetch and the form of
-    // the int-to-float step (conversion, or the exact biased chain) only shape
-    // the pipeline; none of them changes any row's arithmetic.
+    // Up to 4 rows with K a multiple of 256 and 16-byte aligned operands, the
+    // weights stream through the TMA ring (matvec_tma.cu); otherwise the
+    // register-pipelined kernel below.  KL (lanes per row), G (rows per lane),
+    // the L2 prefetch and the form of the int-to-float step (conversion, or the
+    // exact biased chain) only shape the pipeline; none of them, and neither
+    // kernel choice, changes any row's arithmetic.
+    if (T <= 4) {
+        const cudaError_t e = launch_matvec_tma(wq, wd, N, K, aq, ad, T, y, ldy, resid, ldr, s);
+        if (e != cudaErrorNotSupported) return e;
+    }
     switch (T) {
 #define LUCE_MV(TT, KK, GG, PP, BB) \
     case TT: return launch_t<TT, KK, GG, PP, BB>(wq, wd, N, K, aq, ad, y, ldy, resid, ldr, s);

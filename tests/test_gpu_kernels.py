@@ -67,7 +67,11 @@ def test_quantize_bit_exact(T, K):
 
 # ------------------------------------------------------------ block dots / matvec
 
-MV_SHAPES = [(1024, 1024), (1000, 1056), (33, 96), (7, 32), (301, 5120), (64, 17408)]
+# K % 256 == 0 with T <= 4 runs the TMA-ring kernel: (37, 1280) has a partial
+# last kilobyte stage and a partial quad of rows, (100, 256) a K shorter than
+# one stage, (2049, 768) stages of 24 blocks over many CTAs
+MV_SHAPES = [(1024, 1024), (1000, 1056), (33, 96), (7, 32), (301, 5120), (64, 17408), (37, 1280), (100, 256),
+             (2049, 768)]
 
 
 def mv_inputs(N, K, T, seed=0):
@@ -130,6 +134,24 @@ def test_matvec_batched_equals_solo_bitwise(N, K):
     yp = host(luce.luce_q8_matvec_batch(W, D, cuda(aq[perm]), cuda(ad[perm])))
     for i, t in enumerate(perm):
         assert np.array_equal(yp[i].view(np.uint32), solo[t].view(np.uint32))
+
+
+@pytest.mark.parametrize("N,K", [(301, 5120), (37, 1280), (100, 256), (64, 17408)])
+def test_matvec_tma_and_register_kernels_agree_bitwise(N, K):
+    """Scales stored 2 bytes past a 16-byte boundary send 1..4-row launches to
+    the register-pipelined kernel instead of the TMA ring; the bits match."""
+    wq, wd, aq, ad = mv_inputs(N, K, 4, seed=5)
+    W, D = cuda(wq), cuda(wd)
+    buf = torch.zeros(wd.size + 8, dtype=torch.float16, device="cuda")
+    buf[1:1 + wd.size] = D.flatten()
+    D_odd = buf[1:1 + wd.size].view(wd.shape)
+    assert D_odd.data_ptr() % 16 == 2
+    for T in range(1, 5):
+        A, Ad = cuda(aq[:T]), cuda(ad[:T])
+        ring = host(luce.luce_q8_matvec_batch(W, D, A, Ad))
+        reg = host(luce.luce_q8_matvec_batch(W, D_odd, A, Ad))
+        assert np.array_equal(ring.view(np.uint32), reg.view(np.uint32)), T
+    assert luce.wait_timeouts() == 0
 
 
 def test_matvec_writes_only_its_outputs():
