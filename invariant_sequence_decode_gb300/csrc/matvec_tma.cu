@@ -35,6 +35,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <string.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -169,22 +171,146 @@ __device__ __forceinline__ float block_dot_halves(uint4 x, uint4 y, uint4 ax, ui
 
 }  // namespace
 
+namespace {
+
+// Shared-memory carve-up of a ring CTA: 128-aligned slots, the chain values,
+// the slot barriers.
+template <int T>
+struct RingSmem {
+    uint8_t* slots;
+    float* part;
+    uint64_t* full;   // slot filled: the producer's arrival + the copies' bytes
+    uint64_t* empty;  // slot released: one arrival per consumer warp
+    __device__ explicit RingSmem(uint8_t* raw)
+    {
+        using L = RingLayout<T>;
+        slots = raw + ((128u - (smem_addr(raw) & 127u)) & 127u);  // tensor copies land 128-aligned
+        part = reinterpret_cast<float*>(slots + kRingSlots * L::STAGE);
+        full = reinterpret_cast<uint64_t*>(slots + kRingSlots * L::STAGE + L::PART);
+        empty = full + kRingSlots;
+    }
+    __device__ void init() const
+    {
+        for (int s = 0; s < kRingSlots; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 4);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+};
+
+// The producer thread: stage it (group it / nj, K-kilobyte it % nj) of
+// `total` goes to slot it % S.  load_weights(it, slot, bar) issues the
+// group's weight and scale boxes, weight_bytes(it) counts them; the
+// activation boxes of the kilobyte follow.  The first S stages' weights go
+// before the wait on the previous kernel, which the activations need.
+template <int T, typename LoadW, typename BytesW>
+__device__ __forceinline__ void ring_produce(const RingSmem<T>& R, int total, int nj, const CUtensorMap* ma,
+                                             const CUtensorMap* mad, LoadW load_weights, BytesW weight_bytes)
+{
+    using L = RingLayout<T>;
+    constexpr int S = kRingSlots;
+    auto load_acts = [&](int it) {
+        uint8_t* slot = R.slots + (it % S) * L::STAGE;
+        const int j = it % nj;
+        tma_load_3d(slot + L::W + L::D, ma, 0, 4 * j, 0, &R.full[it % S]);
+        tma_load_2d(slot + L::W + L::D + L::A, mad, 32 * j, 0, &R.full[it % S]);
+    };
+    const int pre = min(S, total);
+    for (int it = 0; it < pre; ++it) {
+        mbar_expect_tx(&R.full[it], (uint32_t)(weight_bytes(it) + L::A + L::AD));
+        load_weights(it, R.slots + it * L::STAGE, &R.full[it]);
+    }
+    pdl_wait();
+    for (int it = 0; it < pre; ++it) load_acts(it);
+    for (int it = pre; it < total; ++it) {
+        const int s = it % S;
+        if (!mbar_wait(&R.empty[s], ((it / S) - 1) & 1)) break;
+        mbar_expect_tx(&R.full[s], (uint32_t)(weight_bytes(it) + L::A + L::AD));
+        load_weights(it, R.slots + s * L::STAGE, &R.full[s]);
+        load_acts(it);
+    }
+}
+
+// A consumer lane's chains for one group: stages it .. it + nj - 1 (it
+// advances), lane (r, kb) of warp w, chain c = kb + 8w, rows r + 4g of the
+// group.  acc[g][t] = chain c of row r + 4g against token t.  ok turns false
+// when a wait expires; from then on the lane waits for nothing more and the
+// caller writes nothing.
+template <int T, bool BIAS>
+__device__ __forceinline__ void ring_chains(const RingSmem<T>& R, int& it, int nj, int nb, int r, int c, int lane,
+                                            float (&acc)[kRingG][T], bool& ok)
+{
+    using L = RingLayout<T>;
+    constexpr int G = kRingG, S = kRingSlots;
+    const int h0 = ((lane & 7) >> 2) & 1;  // which 16-byte half first: a phase's 8 lanes hit 8 distinct bank quads
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int t = 0; t < T; ++t) acc[g][t] = 0.0f;
+    for (int j = 0; j < nj; ++j, ++it) {
+        const int s = it % S;
+        if (ok && !mbar_wait(&R.full[s], (it / S) & 1)) ok = false;
+        if (!ok) continue;
+        const uint8_t* slot = R.slots + s * L::STAGE;
+        const bool has = 32 * j + c < nb;
+        uint4 wx[G], wy[G], ax[T], ay[T];
+        float sw[G], sa[T];
+        if (has) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const uint8_t* p = slot + (r + 4 * g) * 1024 + c * 32;
+                wx[g] = lds128(p + 16 * h0);
+                wy[g] = lds128(p + 16 * (h0 ^ 1));
+                sw[g] = __half2float(*reinterpret_cast<const __half*>(slot + L::W + (r + 4 * g) * 64 + c * 2));
+            }
+#pragma unroll
+            for (int t = 0; t < T; ++t) {
+                const uint8_t* p = slot + L::W + L::D + t * 1024 + c * 32;
+                ax[t] = lds128(p + 16 * h0);
+                ay[t] = lds128(p + 16 * (h0 ^ 1));
+                sa[t] = *reinterpret_cast<const float*>(slot + L::W + L::D + L::A + t * 128 + c * 4);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&R.empty[s]);  // operands are in registers: the slot may refill
+        if (has) {
+#pragma unroll
+            for (int t = 0; t < T; ++t)
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float sd = block_dot_halves<BIAS>(wx[g], wy[g], ax[t], ay[t]);
+                    acc[g][t] = __fmaf_rn(__fmul_rn(sw[g], sa[t]), sd, acc[g][t]);
+                }
+        }
+    }
+}
+
+// Chain values of local row rr = r + 4g, token t, chain c into a [16][T][33] buffer.
+template <int T>
+__device__ __forceinline__ void store_chains(float* pp, int r, int c, const float (&acc)[kRingG][T])
+{
+#pragma unroll
+    for (int g = 0; g < kRingG; ++g)
+#pragma unroll
+        for (int t = 0; t < T; ++t) pp[((r + 4 * g) * T + t) * 33 + c] = acc[g][t];
+}
+
+}  // namespace
+
 // mw: W as uint8 [N][K/256][256], box {256, 4, 4};  md: scales fp16 [N][K/32],
 // box {32, 16};  ma: activations uint8 [T][K/256][256], box {256, 4, T};
-// mad: activation scales fp32 [T][K/32], box {32, T}.
+// mad: activation scales fp32 [T][K/32], box {32, T}.  Persistent: CTA b owns
+// quads [b*nq/grid, (b+1)*nq/grid) of the nq = ceil(N/4) quads, in groups of 4.
 template <int T, bool BIAS>
 __global__ void __launch_bounds__(kRingThreads)
 q8_matvec_tma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap md,
                      const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mad, int N, int K,
                      float* y, int64_t ldy, const float* resid, int64_t ldr)
 {
-    using L = RingLayout<T>;
-    constexpr int G = kRingG, S = kRingSlots;
+    constexpr int G = kRingG;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);  // tensor copies land 128-aligned
-    float* part = reinterpret_cast<float*>(sm + S * L::STAGE);
-    uint64_t* full = reinterpret_cast<uint64_t*>(sm + S * L::STAGE + L::PART);
-    uint64_t* empty = full + S;
+    const RingSmem<T> R(smem_raw);
     pdl_trigger();
     const int nb = K >> 5, nj = (nb + 31) >> 5;
     const int nq = (N + 3) >> 2;
@@ -192,114 +318,120 @@ q8_matvec_tma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_consta
     const int q1 = (int)((int64_t)(blockIdx.x + 1) * nq / gridDim.x);
     const int ngrp = (q1 - q0 + G - 1) / G;
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-    if (tid == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(&full[s], 1);   // the producer's arrival + the copies' bytes
-            mbar_init(&empty[s], 4);  // one arrival per consumer warp
-        }
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
+    if (tid == 0) R.init();
     __syncthreads();
 
     if (w == 4) {
-        // producer: stage it = (group it / nj, K-kilobyte it % nj) goes to slot it % S
         if (lane != 0) return;
-        const int total = ngrp * nj;
-        auto quads_of = [&](int it) { return min(G, q1 - (q0 + (it / nj) * G)); };
-        auto bytes_of = [&](int it) { return (uint32_t)(quads_of(it) * 4096 + L::D + L::A + L::AD); };
-        auto load_weights = [&](int it) {
-            const int s = it % S, j = it % nj, qa = q0 + (it / nj) * G, nqv = quads_of(it);
-            uint8_t* slot = sm + s * L::STAGE;
-            for (int qq = 0; qq < nqv; ++qq) tma_load_3d(slot + qq * 4096, &mw, 0, 4 * j, 4 * (qa + qq), &full[s]);
-            tma_load_2d(slot + L::W, &md, 32 * j, 4 * qa, &full[s]);
-        };
-        auto load_acts = [&](int it) {
-            const int s = it % S, j = it % nj;
-            uint8_t* slot = sm + s * L::STAGE;
-            tma_load_3d(slot + L::W + L::D, &ma, 0, 4 * j, 0, &full[s]);
-            tma_load_2d(slot + L::W + L::D + L::A, &mad, 32 * j, 0, &full[s]);
-        };
-        const int pre = min(S, total);
-        for (int it = 0; it < pre; ++it) {  // weights do not depend on the previous kernel
-            mbar_expect_tx(&full[it], bytes_of(it));
-            load_weights(it);
-        }
-        pdl_wait();  // the activations do
-        for (int it = 0; it < pre; ++it) load_acts(it);
-        for (int it = pre; it < total; ++it) {
-            const int s = it % S;
-            if (!mbar_wait(&empty[s], ((it / S) - 1) & 1)) break;
-            mbar_expect_tx(&full[s], bytes_of(it));
-            load_weights(it);
-            load_acts(it);
-        }
+        auto quads = [&](int it) { return min(G, q1 - (q0 + (it / nj) * G)); };
+        ring_produce<T>(
+            R, ngrp * nj, nj, &ma, &mad,
+            [&](int it, uint8_t* slot, uint64_t* bar) {
+                const int j = it % nj, qa = q0 + (it / nj) * G, nqv = quads(it);
+                for (int qq = 0; qq < nqv; ++qq) tma_load_3d(slot + qq * 4096, &mw, 0, 4 * j, 4 * (qa + qq), bar);
+                tma_load_2d(slot + RingLayout<T>::W, &md, 32 * j, 4 * qa, bar);
+            },
+            [&](int it) { return quads(it) * 4096 + RingLayout<T>::D; });
         return;
     }
 
     pdl_wait();  // the residual and y may be touched by earlier kernels
-    const int r = lane >> 3, kb = lane & 7, c = kb + 8 * w;
-    const int h0 = (kb >> 2) & 1;  // which 16-byte half first: 8 lanes of a phase hit 8 distinct bank quads
-    bool bad = false;
+    const int r = lane >> 3, c = (lane & 7) + 8 * w;
+    bool ok = true;
     int it = 0;
     for (int gi = 0; gi < ngrp; ++gi) {
         const int gr0 = 4 * (q0 + gi * G), gr1 = min(4 * q1, N);
         float acc[G][T];
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-#pragma unroll
-            for (int t = 0; t < T; ++t) acc[g][t] = 0.0f;
-        for (int j = 0; j < nj; ++j, ++it) {
-            const int s = it % S;
-            if (!bad && !mbar_wait(&full[s], (it / S) & 1)) bad = true;
-            if (bad) continue;
-            const uint8_t* slot = sm + s * L::STAGE;
-            const bool has = 32 * j + c < nb;
-            uint4 wx[G], wy[G], ax[T], ay[T];
-            float sw[G], sa[T];
-            if (has) {
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const uint8_t* p = slot + (r + 4 * g) * 1024 + c * 32;
-                    wx[g] = lds128(p + 16 * h0);
-                    wy[g] = lds128(p + 16 * (h0 ^ 1));
-                    sw[g] = __half2float(*reinterpret_cast<const __half*>(slot + L::W + (r + 4 * g) * 64 + c * 2));
-                }
-#pragma unroll
-                for (int t = 0; t < T; ++t) {
-                    const uint8_t* p = slot + L::W + L::D + t * 1024 + c * 32;
-                    ax[t] = lds128(p + 16 * h0);
-                    ay[t] = lds128(p + 16 * (h0 ^ 1));
-                    sa[t] = *reinterpret_cast<const float*>(slot + L::W + L::D + L::A + t * 128 + c * 4);
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);  // operands are in registers: the slot may refill
-            if (has) {
-#pragma unroll
-                for (int t = 0; t < T; ++t)
-#pragma unroll
-                    for (int g = 0; g < G; ++g) {
-                        const float sd = block_dot_halves<BIAS>(wx[g], wy[g], ax[t], ay[t]);
-                        acc[g][t] = __fmaf_rn(__fmul_rn(sw[g], sa[t]), sd, acc[g][t]);
-                    }
-            }
-        }
-        // the 32 chains of each (row, token) meet in shared memory; two
-        // buffers, so one barrier per group separates writers and readers
-        float* pp = part + (gi & 1) * (kRingRows * T * 33);
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-#pragma unroll
-            for (int t = 0; t < T; ++t) pp[((r + 4 * g) * T + t) * 33 + c] = acc[g][t];
+        ring_chains<T, BIAS>(R, it, nj, nb, r, c, lane, acc, ok);
+        // two chain buffers, so one barrier per group separates writers and readers
+        float* pp = R.part + (gi & 1) * (kRingRows * T * 33);
+        store_chains<T>(pp, r, c, acc);
         asm volatile("bar.sync 1, 128;" ::: "memory");
         for (int idx = tid; idx < kRingRows * T; idx += 128) {
             const int rr = idx / T, t = idx - (idx / T) * T;
             const int n = gr0 + rr;
-            if (n < gr1 && !bad) {
+            if (n < gr1 && ok) {
                 float out = q8_butterfly(pp + (rr * T + t) * 33);
                 if (resid) out = __fadd_rn(resid[(size_t)t * ldr + n], out);
                 y[(size_t)t * ldy + n] = out;
             }
+        }
+    }
+}
+
+// The decode step's q|k|v projection with the RoPE rotation and the K/V
+// append in the epilogue ("antirez/ds4 pull 604", Commit walkthrough): the
+// same chains, one group per CTA, the group being the rotation pairs
+// (i, i + 64) for i in [q0, q0 + 8) of head h = b / 8, q0 = 8 (b % 8).  Quads
+// 0-1 are rows h*128 + q0 + [0, 8), quads 2-3 rows h*128 + 64 + q0 + [0, 8);
+// md8 is the scale map with an 8-row box.  Thread idx < 8T finishes pair
+// p = idx / T of token t = idx % T exactly as q8_qkv_rope_kernel does.
+template <int T, bool BIAS>
+__global__ void __launch_bounds__(kRingThreads)
+q8_qkv_rope_tma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap md8,
+                       const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mad, int K,
+                       float* __restrict__ qkv, int Hq, int Hkv, RowPos pos, RopeFreq f, float* __restrict__ q_rot,
+                       KvRows kv)
+{
+    constexpr int G = kRingG, P = kRingRows / 2, GROUPS = (kHeadDim / 2) / P;
+    static_assert(P * T <= 128, "one (pair, token) per consumer thread");
+    extern __shared__ uint8_t smem_raw[];
+    const RingSmem<T> R(smem_raw);
+    pdl_trigger();
+    const int nb = K >> 5, nj = (nb + 31) >> 5;
+    const int h = blockIdx.x / GROUPS, q0 = (blockIdx.x % GROUPS) * P;
+    const int row0 = h * kHeadDim + q0, row1 = h * kHeadDim + kHeadDim / 2 + q0;
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+    if (tid == 0) R.init();
+    __syncthreads();
+
+    if (w == 4) {
+        if (lane != 0) return;
+        ring_produce<T>(
+            R, nj, nj, &ma, &mad,
+            [&](int it, uint8_t* slot, uint64_t* bar) {
+                const int j = it % nj;
+#pragma unroll
+                for (int qq = 0; qq < G; ++qq)
+                    tma_load_3d(slot + qq * 4096, &mw, 0, 4 * j, (qq < 2 ? row0 : row1) + 4 * (qq & 1), bar);
+                tma_load_2d(slot + RingLayout<T>::W, &md8, 32 * j, row0, bar);
+                tma_load_2d(slot + RingLayout<T>::W + P * 64, &md8, 32 * j, row1, bar);
+            },
+            [&](int) { return G * 4096 + RingLayout<T>::D; });
+        return;
+    }
+
+    // thread idx < P*T finishes pair p = idx / T of token t = idx % T; its
+    // cos/sin depend only on the position, so they are formed first
+    const int p = tid / T, t = tid - (tid / T) * T;
+    const int i = q0 + p;
+    const bool fin = tid < P * T;
+    const float2 cs = (fin && h < Hq + Hkv) ? rope_cs(pos.pos[t], f.inv[i]) : make_float2(1.0f, 0.0f);
+    pdl_wait();  // the K/V caches and outputs may be touched by earlier kernels
+    const int r = lane >> 3, c = (lane & 7) + 8 * w;
+    int it = 0;
+    float acc[G][T];
+    bool ok = true;
+    ring_chains<T, BIAS>(R, it, nj, nb, r, c, lane, acc, ok);
+    store_chains<T>(R.part, r, c, acc);
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    if (fin && ok) {
+        float x0 = q8_butterfly(R.part + (p * T + t) * 33);
+        float x1 = q8_butterfly(R.part + ((p + P) * T + t) * 33);
+        const int ldq = (Hq + 2 * Hkv) * kHeadDim;
+        float* yr = qkv + (size_t)t * ldq + (size_t)h * kHeadDim;
+        yr[i] = x0;
+        yr[i + kHeadDim / 2] = x1;
+        const KvRow kr = kv.row[t];
+        if (h < Hq + Hkv) rope_rotate(x0, x1, cs.x, cs.y);
+        if (h < Hq) {
+            float* dst = q_rot + (size_t)t * Hq * kHeadDim + (size_t)h * kHeadDim;
+            dst[i] = x0;
+            dst[i + kHeadDim / 2] = x1;
+        } else {
+            __half* dst = (h < Hq + Hkv ? kr.k + (h - Hq) * kr.head_stride : kr.v + (h - Hq - Hkv) * kr.head_stride);
+            dst[i] = __float2half_rn(x0);
+            dst[i + kHeadDim / 2] = __float2half_rn(x1);
         }
     }
 }
@@ -320,17 +452,67 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
     return fn;
 }
 
+// The inputs of one tiled tensor map; a map is a pure function of them, so
+// maps are kept in a small table and encoded once per distinct key (the
+// step's weights and workspace give the same keys every call).
+struct MapKey {
+    uint64_t base, dims[3], strides[2];
+    uint32_t box[3], dt, rank;
+    bool operator==(const MapKey& o) const { return memcmp(this, &o, sizeof(MapKey)) == 0; }
+};
+
+struct MapCache {
+    static constexpr int kSlots = 512;
+    std::mutex mu;
+    MapKey key[kSlots];
+    CUtensorMap map[kSlots];
+    bool used[kSlots] = {};
+};
+
+MapCache& map_cache()
+{
+    static MapCache c;
+    return c;
+}
+
 // A tiled tensor map of `rank` dims (dims[0] innermost, strides in bytes for
 // dims 1..rank-1), no swizzle, zero fill outside the tensor.
 bool encode_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const cuuint64_t* dims,
                 const cuuint64_t* strides, const cuuint32_t* box)
 {
+    MapKey k;
+    memset(&k, 0, sizeof k);
+    k.base = (uint64_t)(uintptr_t)base;
+    k.dt = (uint32_t)dt;
+    k.rank = (uint32_t)rank;
+    for (int i = 0; i < rank; ++i) {
+        k.dims[i] = dims[i];
+        k.box[i] = box[i];
+        if (i + 1 < rank) k.strides[i] = strides[i];
+    }
+    uint64_t h = 1469598103934665603ull;  // FNV-1a over the key's bytes
+    for (size_t i = 0; i < sizeof k; ++i) h = (h ^ reinterpret_cast<const uint8_t*>(&k)[i]) * 1099511628211ull;
+    MapCache& c = map_cache();
+    const int slot = (int)(h % MapCache::kSlots);
+    {
+        std::lock_guard<std::mutex> lock(c.mu);
+        if (c.used[slot] && c.key[slot] == k) {
+            *m = c.map[slot];
+            return true;
+        }
+    }
     const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return false;
     const cuuint32_t es[3] = {1, 1, 1};
-    return enc(m, dt, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    if (enc(m, dt, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    std::lock_guard<std::mutex> lock(c.mu);
+    c.key[slot] = k;
+    c.map[slot] = *m;
+    c.used[slot] = true;
+    return true;
 }
 
 int sm_count()
@@ -346,6 +528,13 @@ int sm_count()
     return counts[dev];
 }
 
+template <typename Kern>
+cudaError_t set_smem_once(Kern kernel, int bytes, std::once_flag& once, cudaError_t& status)
+{
+    std::call_once(once, [&] { status = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes); });
+    return status;
+}
+
 template <int T, bool BIAS>
 cudaError_t launch_tma_t(const CUtensorMap& mw, const CUtensorMap& md, const CUtensorMap& ma, const CUtensorMap& mad,
                          int N, int K, float* y, int64_t ldy, const float* resid, int64_t ldr, int sms,
@@ -354,11 +543,7 @@ cudaError_t launch_tma_t(const CUtensorMap& mw, const CUtensorMap& md, const CUt
     using L = RingLayout<T>;
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(q8_matvec_tma_kernel<T, BIAS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    L::SMEM);
-    });
-    if (attr != cudaSuccess) return attr;
+    if (set_smem_once(q8_matvec_tma_kernel<T, BIAS>, L::SMEM, once, attr) != cudaSuccess) return attr;
     const int nq = (N + 3) / 4;
     const int grid = min(kRingCtasPerSm * sms, (nq + kRingG - 1) / kRingG);
     const cudaError_t e = launch_pdl_smem(q8_matvec_tma_kernel<T, BIAS>, dim3(grid), dim3(kRingThreads), L::SMEM, s,
@@ -367,36 +552,72 @@ cudaError_t launch_tma_t(const CUtensorMap& mw, const CUtensorMap& md, const CUt
     return e;
 }
 
+template <int T, bool BIAS>
+cudaError_t launch_qkv_tma_t(const CUtensorMap& mw, const CUtensorMap& md8, const CUtensorMap& ma,
+                             const CUtensorMap& mad, int K, float* qkv, int Hq, int Hkv, const RowPos& pos,
+                             const RopeFreq& f, float* q_rot, const KvRows& kv, cudaStream_t s)
+{
+    using L = RingLayout<T>;
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    if (set_smem_once(q8_qkv_rope_tma_kernel<T, BIAS>, L::SMEM, once, attr) != cudaSuccess) return attr;
+    const int groups = (Hq + 2 * Hkv) * ((kHeadDim / 2) / (kRingRows / 2));
+    const cudaError_t e = launch_pdl_smem(q8_qkv_rope_tma_kernel<T, BIAS>, dim3(groups), dim3(kRingThreads), L::SMEM,
+                                          s, mw, md8, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv);
+    count_launches(1);
+    return e;
+}
+
+// The four maps of a ring launch; false when the shapes or alignments do not
+// allow one (the caller then takes the register-pipelined kernels).
+bool ring_maps(const int8_t* wq, const __half* wd, int N, int K, const int8_t* aq, const float* ad, int T,
+               int scale_box_rows, CUtensorMap* mw, CUtensorMap* md, CUtensorMap* ma, CUtensorMap* mad)
+{
+    auto al16 = [](const void* p) { return ((uintptr_t)p & 15) == 0; };
+    if (T < 1 || T > 4 || K % 256 != 0 || !al16(wq) || !al16(wd) || !al16(aq) || !al16(ad)) return false;
+    const cuuint64_t nb = (cuuint64_t)K / 32;
+    const cuuint64_t wdim[3] = {256, (cuuint64_t)K / 256, (cuuint64_t)N}, wstr[2] = {256, (cuuint64_t)K};
+    const cuuint32_t wbox[3] = {256, 4, 4};
+    const cuuint64_t ddim[2] = {nb, (cuuint64_t)N}, dstr[1] = {nb * 2};
+    const cuuint32_t dbox[2] = {32, (cuuint32_t)scale_box_rows};
+    const cuuint64_t adim[3] = {256, (cuuint64_t)K / 256, (cuuint64_t)T}, astr[2] = {256, (cuuint64_t)K};
+    const cuuint32_t abox[3] = {256, 4, (cuuint32_t)T};
+    const cuuint64_t addim[2] = {nb, (cuuint64_t)T}, adstr[1] = {nb * 4};
+    const cuuint32_t adbox[2] = {32, (cuuint32_t)T};
+    return encode_map(mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, wq, wdim, wstr, wbox) &&
+           encode_map(md, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, wd, ddim, dstr, dbox) &&
+           encode_map(ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, aq, adim, astr, abox) &&
+           encode_map(mad, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ad, addim, adstr, adbox);
+}
+
 }  // namespace
 
 cudaError_t launch_matvec_tma(const int8_t* wq, const __half* wd, int N, int K, const int8_t* aq, const float* ad,
                               int T, float* y, int64_t ldy, const float* resid, int64_t ldr, cudaStream_t s)
 {
-    auto al16 = [](const void* p) { return ((uintptr_t)p & 15) == 0; };
-    if (T < 1 || T > 4 || K % 256 != 0 || !al16(wq) || !al16(wd) || !al16(aq) || !al16(ad))
-        return cudaErrorNotSupported;
     const int sms = sm_count();
-    if (sms <= 0) return cudaErrorNotSupported;
-    const cuuint64_t nb = (cuuint64_t)K / 32;
-    const cuuint64_t wdim[3] = {256, (cuuint64_t)K / 256, (cuuint64_t)N}, wstr[2] = {256, (cuuint64_t)K};
-    const cuuint32_t wbox[3] = {256, 4, 4};
-    const cuuint64_t ddim[2] = {nb, (cuuint64_t)N}, dstr[1] = {nb * 2};
-    const cuuint32_t dbox[2] = {32, (cuuint32_t)kRingRows};
-    const cuuint64_t adim[3] = {256, (cuuint64_t)K / 256, (cuuint64_t)T}, astr[2] = {256, (cuuint64_t)K};
-    const cuuint32_t abox[3] = {256, 4, (cuuint32_t)T};
-    const cuuint64_t addim[2] = {nb, (cuuint64_t)T}, adstr[1] = {nb * 4};
-    const cuuint32_t adbox[2] = {32, (cuuint32_t)T};
     CUtensorMap mw, md, ma, mad;
-    if (!encode_map(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, wq, wdim, wstr, wbox) ||
-        !encode_map(&md, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, wd, ddim, dstr, dbox) ||
-        !encode_map(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, aq, adim, astr, abox) ||
-        !encode_map(&mad, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ad, addim, adstr, adbox))
-        return cudaErrorNotSupported;
+    if (sms <= 0 || !ring_maps(wq, wd, N, K, aq, ad, T, kRingRows, &mw, &md, &ma, &mad)) return cudaErrorNotSupported;
     switch (T) {
         case 1: return launch_tma_t<1, true>(mw, md, ma, mad, N, K, y, ldy, resid, ldr, sms, s);
         case 2: return launch_tma_t<2, false>(mw, md, ma, mad, N, K, y, ldy, resid, ldr, sms, s);
         case 3: return launch_tma_t<3, false>(mw, md, ma, mad, N, K, y, ldy, resid, ldr, sms, s);
         default: return launch_tma_t<4, false>(mw, md, ma, mad, N, K, y, ldy, resid, ldr, sms, s);
+    }
+}
+
+cudaError_t launch_qkv_rope_tma(const int8_t* wq, const __half* wd, int K, const int8_t* aq, const float* ad, int T,
+                                float* qkv, int Hq, int Hkv, const RowPos& pos, const RopeFreq& f, float* q_rot,
+                                const KvRows& kv, cudaStream_t s)
+{
+    const int N = (Hq + 2 * Hkv) * kHeadDim;
+    CUtensorMap mw, md8, ma, mad;
+    if (!ring_maps(wq, wd, N, K, aq, ad, T, kRingRows / 2, &mw, &md8, &ma, &mad)) return cudaErrorNotSupported;
+    switch (T) {
+        case 1: return launch_qkv_tma_t<1, true>(mw, md8, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
+        case 2: return launch_qkv_tma_t<2, false>(mw, md8, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
+        case 3: return launch_qkv_tma_t<3, false>(mw, md8, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
+        default: return launch_qkv_tma_t<4, false>(mw, md8, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
     }
 }
 
