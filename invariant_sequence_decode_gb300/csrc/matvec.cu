@@ -141,13 +141,13 @@ cudaError_t launch_matvec(const int8_t* wq, const __half* wd, int N, int K, cons
                           const float* ad, int T, float* y, int64_t ldy, const float* resid,
                           int64_t ldr, cudaStream_t s)
 {
-    // Up to 4 rows with K a multiple of 256 and 16-byte aligned operands, the
-    // weights stream through the TMA ring (matvec_tma.cu); otherwise the
-    // register-pipelined kernel below.  KL (lanes per row), G (rows per lane),
-    // the L2 prefetch and the form of the int-to-float step (conversion, or the
-    // exact biased chain) only shape the pipeline; none of them, and neither
-    // kernel choice, changes any row's arithmetic.
-    if (T <= 4) {
+    // 1..8 and 13..16 rows with K a multiple of 256 and 16-byte aligned
+    // operands: the weights stream through the TMA ring (matvec_tma.cu);
+    // otherwise the register-pipelined kernel below.  KL (lanes per row), G
+    // (rows per lane), the L2 prefetch and the form of the int-to-float step
+    // (conversion, or the exact biased chain) only shape the pipeline; none of
+    // them, and neither kernel choice, changes any row's arithmetic.
+    {
         const cudaError_t e = launch_matvec_tma(wq, wd, N, K, aq, ad, T, y, ldy, resid, ldr, s);
         if (e != cudaErrorNotSupported) return e;
     }

@@ -48,21 +48,23 @@ __device__ unsigned int g_wait_timeouts;
 
 namespace {
 
-constexpr int kRingG = 4;              // rows per lane (quads per group)
-constexpr int kRingRows = 4 * kRingG;  // rows per group
-constexpr int kRingSlots = 2;
-constexpr int kRingCtasPerSm = 3;
+constexpr int kRingCtasPerSm = 3;      // 1..4 rows
+constexpr int kRingCtasPerSmWide = 3;  // 5..8 rows (larger activation boxes)
+constexpr int kRingSlotsWide = 3;
 constexpr int kRingThreads = 160;  // 4 consumer warps + 1 producer warp
 
-template <int T>
+// Shape of a ring: T activation rows, G rows per lane (a group is G quads,
+// 4G rows), S slots.
+template <int T, int G, int S>
 struct RingLayout {
-    static constexpr int W = kRingRows * 1024;  // [16 rows][1024 B]
-    static constexpr int D = kRingRows * 64;    // [16 rows][32 fp16 scales]
+    static constexpr int ROWS = 4 * G;
+    static constexpr int W = ROWS * 1024;  // [4G rows][1024 B]
+    static constexpr int D = ROWS * 64;    // [4G rows][32 fp16 scales]
     static constexpr int A = T * 1024;          // [T][1024 B]
     static constexpr int AD = T * 128;          // [T][32 fp32 scales]
     static constexpr int STAGE = W + D + A + AD;  // a multiple of 128
-    static constexpr int PART = 2 * kRingRows * T * 33 * 4;
-    static constexpr int SMEM = 128 + kRingSlots * STAGE + PART + 2 * kRingSlots * 8;
+    static constexpr int PART = 2 * ROWS * T * 33 * 4;
+    static constexpr int SMEM = 128 + S * STAGE + PART + 2 * S * 8;
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -175,7 +177,7 @@ namespace {
 
 // Shared-memory carve-up of a ring CTA: 128-aligned slots, the chain values,
 // the slot barriers.
-template <int T>
+template <int T, int G, int S>
 struct RingSmem {
     uint8_t* slots;
     float* part;
@@ -183,15 +185,15 @@ struct RingSmem {
     uint64_t* empty;  // slot released: one arrival per consumer warp
     __device__ explicit RingSmem(uint8_t* raw)
     {
-        using L = RingLayout<T>;
+        using L = RingLayout<T, G, S>;
         slots = raw + ((128u - (smem_addr(raw) & 127u)) & 127u);  // tensor copies land 128-aligned
-        part = reinterpret_cast<float*>(slots + kRingSlots * L::STAGE);
-        full = reinterpret_cast<uint64_t*>(slots + kRingSlots * L::STAGE + L::PART);
-        empty = full + kRingSlots;
+        part = reinterpret_cast<float*>(slots + S * L::STAGE);
+        full = reinterpret_cast<uint64_t*>(slots + S * L::STAGE + L::PART);
+        empty = full + S;
     }
     __device__ void init() const
     {
-        for (int s = 0; s < kRingSlots; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 4);
         }
@@ -204,12 +206,11 @@ struct RingSmem {
 // group's weight and scale boxes, weight_bytes(it) counts them; the
 // activation boxes of the kilobyte follow.  The first S stages' weights go
 // before the wait on the previous kernel, which the activations need.
-template <int T, typename LoadW, typename BytesW>
-__device__ __forceinline__ void ring_produce(const RingSmem<T>& R, int total, int nj, const CUtensorMap* ma,
+template <int T, int G, int S, typename LoadW, typename BytesW>
+__device__ __forceinline__ void ring_produce(const RingSmem<T, G, S>& R, int total, int nj, const CUtensorMap* ma,
                                              const CUtensorMap* mad, LoadW load_weights, BytesW weight_bytes)
 {
-    using L = RingLayout<T>;
-    constexpr int S = kRingSlots;
+    using L = RingLayout<T, G, S>;
     auto load_acts = [&](int it) {
         uint8_t* slot = R.slots + (it % S) * L::STAGE;
         const int j = it % nj;
@@ -237,12 +238,11 @@ __device__ __forceinline__ void ring_produce(const RingSmem<T>& R, int total, in
 // group.  acc[g][t] = chain c of row r + 4g against token t.  ok turns false
 // when a wait expires; from then on the lane waits for nothing more and the
 // caller writes nothing.
-template <int T, bool BIAS>
-__device__ __forceinline__ void ring_chains(const RingSmem<T>& R, int& it, int nj, int nb, int r, int c, int lane,
-                                            float (&acc)[kRingG][T], bool& ok)
+template <int T, int G, int S, bool BIAS>
+__device__ __forceinline__ void ring_chains(const RingSmem<T, G, S>& R, int& it, int nj, int nb, int r, int c, int lane,
+                                            float (&acc)[G][T], bool& ok)
 {
-    using L = RingLayout<T>;
-    constexpr int G = kRingG, S = kRingSlots;
+    using L = RingLayout<T, G, S>;
     const int h0 = ((lane & 7) >> 2) & 1;  // which 16-byte half first: a phase's 8 lanes hit 8 distinct bank quads
 #pragma unroll
     for (int g = 0; g < G; ++g)
@@ -286,12 +286,12 @@ __device__ __forceinline__ void ring_chains(const RingSmem<T>& R, int& it, int n
     }
 }
 
-// Chain values of local row rr = r + 4g, token t, chain c into a [16][T][33] buffer.
-template <int T>
-__device__ __forceinline__ void store_chains(float* pp, int r, int c, const float (&acc)[kRingG][T])
+// Chain values of local row rr = r + 4g, token t, chain c into a [4G][T][33] buffer.
+template <int T, int G>
+__device__ __forceinline__ void store_chains(float* pp, int r, int c, const float (&acc)[G][T])
 {
 #pragma unroll
-    for (int g = 0; g < kRingG; ++g)
+    for (int g = 0; g < G; ++g)
 #pragma unroll
         for (int t = 0; t < T; ++t) pp[((r + 4 * g) * T + t) * 33 + c] = acc[g][t];
 }
@@ -301,16 +301,17 @@ __device__ __forceinline__ void store_chains(float* pp, int r, int c, const floa
 // mw: W as uint8 [N][K/256][256], box {256, 4, 4};  md: scales fp16 [N][K/32],
 // box {32, 16};  ma: activations uint8 [T][K/256][256], box {256, 4, T};
 // mad: activation scales fp32 [T][K/32], box {32, T}.  Persistent: CTA b owns
-// quads [b*nq/grid, (b+1)*nq/grid) of the nq = ceil(N/4) quads, in groups of 4.
-template <int T, bool BIAS>
+// quads [b*nq/grid, (b+1)*nq/grid) of the nq = ceil(N/4) quads, in groups of G
+// (md's box is 4G rows).
+template <int T, int G, int S, bool BIAS>
 __global__ void __launch_bounds__(kRingThreads)
 q8_matvec_tma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap md,
                      const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mad, int N, int K,
                      float* y, int64_t ldy, const float* resid, int64_t ldr)
 {
-    constexpr int G = kRingG;
+    using L = RingLayout<T, G, S>;
     extern __shared__ uint8_t smem_raw[];
-    const RingSmem<T> R(smem_raw);
+    const RingSmem<T, G, S> R(smem_raw);
     pdl_trigger();
     const int nb = K >> 5, nj = (nb + 31) >> 5;
     const int nq = (N + 3) >> 2;
@@ -324,14 +325,14 @@ q8_matvec_tma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_consta
     if (w == 4) {
         if (lane != 0) return;
         auto quads = [&](int it) { return min(G, q1 - (q0 + (it / nj) * G)); };
-        ring_produce<T>(
+        ring_produce<T, G, S>(
             R, ngrp * nj, nj, &ma, &mad,
             [&](int it, uint8_t* slot, uint64_t* bar) {
                 const int j = it % nj, qa = q0 + (it / nj) * G, nqv = quads(it);
                 for (int qq = 0; qq < nqv; ++qq) tma_load_3d(slot + qq * 4096, &mw, 0, 4 * j, 4 * (qa + qq), bar);
-                tma_load_2d(slot + RingLayout<T>::W, &md, 32 * j, 4 * qa, bar);
+                tma_load_2d(slot + L::W, &md, 32 * j, 4 * qa, bar);
             },
-            [&](int it) { return quads(it) * 4096 + RingLayout<T>::D; });
+            [&](int it) { return quads(it) * 4096 + L::D; });
         return;
     }
 
@@ -342,12 +343,12 @@ q8_matvec_tma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_consta
     for (int gi = 0; gi < ngrp; ++gi) {
         const int gr0 = 4 * (q0 + gi * G), gr1 = min(4 * q1, N);
         float acc[G][T];
-        ring_chains<T, BIAS>(R, it, nj, nb, r, c, lane, acc, ok);
+        ring_chains<T, G, S, BIAS>(R, it, nj, nb, r, c, lane, acc, ok);
         // two chain buffers, so one barrier per group separates writers and readers
-        float* pp = R.part + (gi & 1) * (kRingRows * T * 33);
-        store_chains<T>(pp, r, c, acc);
+        float* pp = R.part + (gi & 1) * (L::ROWS * T * 33);
+        store_chains<T, G>(pp, r, c, acc);
         asm volatile("bar.sync 1, 128;" ::: "memory");
-        for (int idx = tid; idx < kRingRows * T; idx += 128) {
+        for (int idx = tid; idx < L::ROWS * T; idx += 128) {
             const int rr = idx / T, t = idx - (idx / T) * T;
             const int n = gr0 + rr;
             if (n < gr1 && ok) {
@@ -370,13 +371,14 @@ template <int T, bool BIAS>
 __global__ void __launch_bounds__(kRingThreads)
 q8_qkv_rope_tma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap md8,
                        const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mad, int K,
-                       float* __restrict__ qkv, int Hq, int Hkv, RowPos pos, RopeFreq f, float* __restrict__ q_rot,
-                       KvRows kv)
+                       float* __restrict__ qkv, int Hq, int Hkv, const __grid_constant__ RowPos pos,
+                       const __grid_constant__ RopeFreq f, float* __restrict__ q_rot, const __grid_constant__ KvRows kv)
 {
-    constexpr int G = kRingG, P = kRingRows / 2, GROUPS = (kHeadDim / 2) / P;
+    constexpr int G = 4, S = 2, P = 2 * G, GROUPS = (kHeadDim / 2) / P;
+    using L = RingLayout<T, G, S>;
     static_assert(P * T <= 128, "one (pair, token) per consumer thread");
     extern __shared__ uint8_t smem_raw[];
-    const RingSmem<T> R(smem_raw);
+    const RingSmem<T, G, S> R(smem_raw);
     pdl_trigger();
     const int nb = K >> 5, nj = (nb + 31) >> 5;
     const int h = blockIdx.x / GROUPS, q0 = (blockIdx.x % GROUPS) * P;
@@ -387,17 +389,17 @@ q8_qkv_rope_tma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_cons
 
     if (w == 4) {
         if (lane != 0) return;
-        ring_produce<T>(
+        ring_produce<T, G, S>(
             R, nj, nj, &ma, &mad,
             [&](int it, uint8_t* slot, uint64_t* bar) {
                 const int j = it % nj;
 #pragma unroll
                 for (int qq = 0; qq < G; ++qq)
                     tma_load_3d(slot + qq * 4096, &mw, 0, 4 * j, (qq < 2 ? row0 : row1) + 4 * (qq & 1), bar);
-                tma_load_2d(slot + RingLayout<T>::W, &md8, 32 * j, row0, bar);
-                tma_load_2d(slot + RingLayout<T>::W + P * 64, &md8, 32 * j, row1, bar);
+                tma_load_2d(slot + L::W, &md8, 32 * j, row0, bar);
+                tma_load_2d(slot + L::W + P * 64, &md8, 32 * j, row1, bar);
             },
-            [&](int) { return G * 4096 + RingLayout<T>::D; });
+            [&](int) { return G * 4096 + L::D; });
         return;
     }
 
@@ -412,8 +414,8 @@ q8_qkv_rope_tma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_cons
     int it = 0;
     float acc[G][T];
     bool ok = true;
-    ring_chains<T, BIAS>(R, it, nj, nb, r, c, lane, acc, ok);
-    store_chains<T>(R.part, r, c, acc);
+    ring_chains<T, G, S, BIAS>(R, it, nj, nb, r, c, lane, acc, ok);
+    store_chains<T, G>(R.part, r, c, acc);
     asm volatile("bar.sync 1, 128;" ::: "memory");
     if (fin && ok) {
         float x0 = q8_butterfly(R.part + (p * T + t) * 33);
@@ -535,19 +537,19 @@ cudaError_t set_smem_once(Kern kernel, int bytes, std::once_flag& once, cudaErro
     return status;
 }
 
-template <int T, bool BIAS>
+template <int T, int G, int S, bool BIAS>
 cudaError_t launch_tma_t(const CUtensorMap& mw, const CUtensorMap& md, const CUtensorMap& ma, const CUtensorMap& mad,
-                         int N, int K, float* y, int64_t ldy, const float* resid, int64_t ldr, int sms,
+                         int N, int K, float* y, int64_t ldy, const float* resid, int64_t ldr, int ctas,
                          cudaStream_t s)
 {
-    using L = RingLayout<T>;
+    using L = RingLayout<T, G, S>;
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
-    if (set_smem_once(q8_matvec_tma_kernel<T, BIAS>, L::SMEM, once, attr) != cudaSuccess) return attr;
+    if (set_smem_once(q8_matvec_tma_kernel<T, G, S, BIAS>, L::SMEM, once, attr) != cudaSuccess) return attr;
     const int nq = (N + 3) / 4;
-    const int grid = min(kRingCtasPerSm * sms, (nq + kRingG - 1) / kRingG);
-    const cudaError_t e = launch_pdl_smem(q8_matvec_tma_kernel<T, BIAS>, dim3(grid), dim3(kRingThreads), L::SMEM, s,
-                                          mw, md, ma, mad, N, K, y, ldy, resid, ldr);
+    const int grid = min(ctas, (nq + G - 1) / G);
+    const cudaError_t e = launch_pdl_smem(q8_matvec_tma_kernel<T, G, S, BIAS>, dim3(grid), dim3(kRingThreads), L::SMEM,
+                                          s, mw, md, ma, mad, N, K, y, ldy, resid, ldr);
     count_launches(1);
     return e;
 }
@@ -557,11 +559,11 @@ cudaError_t launch_qkv_tma_t(const CUtensorMap& mw, const CUtensorMap& md8, cons
                              const CUtensorMap& mad, int K, float* qkv, int Hq, int Hkv, const RowPos& pos,
                              const RopeFreq& f, float* q_rot, const KvRows& kv, cudaStream_t s)
 {
-    using L = RingLayout<T>;
+    using L = RingLayout<T, 4, 2>;
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
     if (set_smem_once(q8_qkv_rope_tma_kernel<T, BIAS>, L::SMEM, once, attr) != cudaSuccess) return attr;
-    const int groups = (Hq + 2 * Hkv) * ((kHeadDim / 2) / (kRingRows / 2));
+    const int groups = (Hq + 2 * Hkv) * ((kHeadDim / 2) / 8);
     const cudaError_t e = launch_pdl_smem(q8_qkv_rope_tma_kernel<T, BIAS>, dim3(groups), dim3(kRingThreads), L::SMEM,
                                           s, mw, md8, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv);
     count_launches(1);
@@ -574,7 +576,7 @@ bool ring_maps(const int8_t* wq, const __half* wd, int N, int K, const int8_t* a
                int scale_box_rows, CUtensorMap* mw, CUtensorMap* md, CUtensorMap* ma, CUtensorMap* mad)
 {
     auto al16 = [](const void* p) { return ((uintptr_t)p & 15) == 0; };
-    if (T < 1 || T > 4 || K % 256 != 0 || !al16(wq) || !al16(wd) || !al16(aq) || !al16(ad)) return false;
+    if (T < 1 || T > 8 || K % 256 != 0 || !al16(wq) || !al16(wd) || !al16(aq) || !al16(ad)) return false;
     const cuuint64_t nb = (cuuint64_t)K / 32;
     const cuuint64_t wdim[3] = {256, (cuuint64_t)K / 256, (cuuint64_t)N}, wstr[2] = {256, (cuuint64_t)K};
     const cuuint32_t wbox[3] = {256, 4, 4};
@@ -592,18 +594,46 @@ bool ring_maps(const int8_t* wq, const __half* wd, int N, int K, const int8_t* a
 
 }  // namespace
 
+// One ring launch of T <= 8 rows: groups of 16 rows over two slots up to 4
+// rows, groups of 8 rows over three slots for 5..8 (shared memory for the
+// larger activation boxes).
+static cudaError_t launch_ring_rows(const int8_t* wq, const __half* wd, int N, int K, const int8_t* aq,
+                                    const float* ad, int T, float* y, int64_t ldy, const float* resid, int64_t ldr,
+                                    int sms, cudaStream_t s)
+{
+    CUtensorMap mw, md, ma, mad;
+    if (!ring_maps(wq, wd, N, K, aq, ad, T, T <= 4 ? 16 : 8, &mw, &md, &ma, &mad)) return cudaErrorNotSupported;
+    const int narrow = kRingCtasPerSm * sms, wide = kRingCtasPerSmWide * sms;
+    constexpr int SW = kRingSlotsWide;
+    switch (T) {
+        case 1: return launch_tma_t<1, 4, 2, true>(mw, md, ma, mad, N, K, y, ldy, resid, ldr, narrow, s);
+        case 2: return launch_tma_t<2, 4, 2, false>(mw, md, ma, mad, N, K, y, ldy, resid, ldr, narrow, s);
+        case 3: return launch_tma_t<3, 4, 2, false>(mw, md, ma, mad, N, K, y, ldy, resid, ldr, narrow, s);
+        case 4: return launch_tma_t<4, 4, 2, false>(mw, md, ma, mad, N, K, y, ldy, resid, ldr, narrow, s);
+        case 5: return launch_tma_t<5, 2, SW, false>(mw, md, ma, mad, N, K, y, ldy, resid, ldr, wide, s);
+        case 6: return launch_tma_t<6, 2, SW, false>(mw, md, ma, mad, N, K, y, ldy, resid, ldr, wide, s);
+        case 7: return launch_tma_t<7, 2, SW, false>(mw, md, ma, mad, N, K, y, ldy, resid, ldr, wide, s);
+        default: return launch_tma_t<8, 2, SW, false>(mw, md, ma, mad, N, K, y, ldy, resid, ldr, wide, s);
+    }
+}
+
 cudaError_t launch_matvec_tma(const int8_t* wq, const __half* wd, int N, int K, const int8_t* aq, const float* ad,
                               int T, float* y, int64_t ldy, const float* resid, int64_t ldr, cudaStream_t s)
 {
+    // 1..8 rows: one launch.  13..16 rows: rows 0..7, then rows 8..T-1 - the
+    // weights stream twice, which still beats the register kernel there;
+    // 9..12 rows stay on the register kernel (measured faster).
     const int sms = sm_count();
-    CUtensorMap mw, md, ma, mad;
-    if (sms <= 0 || !ring_maps(wq, wd, N, K, aq, ad, T, kRingRows, &mw, &md, &ma, &mad)) return cudaErrorNotSupported;
-    switch (T) {
-        case 1: return launch_tma_t<1, true>(mw, md, ma, mad, N, K, y, ldy, resid, ldr, sms, s);
-        case 2: return launch_tma_t<2, false>(mw, md, ma, mad, N, K, y, ldy, resid, ldr, sms, s);
-        case 3: return launch_tma_t<3, false>(mw, md, ma, mad, N, K, y, ldy, resid, ldr, sms, s);
-        default: return launch_tma_t<4, false>(mw, md, ma, mad, N, K, y, ldy, resid, ldr, sms, s);
-    }
+    if (sms <= 0 || T < 1 || (T > 8 && T < 13) || T > 16) return cudaErrorNotSupported;
+    if (T <= 8) return launch_ring_rows(wq, wd, N, K, aq, ad, T, y, ldy, resid, ldr, sms, s);
+    CUtensorMap probe[4];
+    if (!ring_maps(wq, wd, N, K, aq + (size_t)8 * K, ad + (size_t)8 * (K / 32), T - 8, 8, &probe[0], &probe[1],
+                   &probe[2], &probe[3]))
+        return cudaErrorNotSupported;  // both halves take the ring or neither does
+    cudaError_t e = launch_ring_rows(wq, wd, N, K, aq, ad, 8, y, ldy, resid, ldr, sms, s);
+    if (e != cudaSuccess) return e;
+    return launch_ring_rows(wq, wd, N, K, aq + (size_t)8 * K, ad + (size_t)8 * (K / 32), T - 8, y + 8 * ldy, ldy,
+                            resid ? resid + 8 * ldr : nullptr, ldr, sms, s);
 }
 
 cudaError_t launch_qkv_rope_tma(const int8_t* wq, const __half* wd, int K, const int8_t* aq, const float* ad, int T,
@@ -612,7 +642,7 @@ cudaError_t launch_qkv_rope_tma(const int8_t* wq, const __half* wd, int K, const
 {
     const int N = (Hq + 2 * Hkv) * kHeadDim;
     CUtensorMap mw, md8, ma, mad;
-    if (!ring_maps(wq, wd, N, K, aq, ad, T, kRingRows / 2, &mw, &md8, &ma, &mad)) return cudaErrorNotSupported;
+    if (T > 4 || !ring_maps(wq, wd, N, K, aq, ad, T, 8, &mw, &md8, &ma, &mad)) return cudaErrorNotSupported;
     switch (T) {
         case 1: return launch_qkv_tma_t<1, true>(mw, md8, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
         case 2: return launch_qkv_tma_t<2, false>(mw, md8, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv, s);

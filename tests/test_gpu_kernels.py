@@ -138,15 +138,16 @@ def test_matvec_batched_equals_solo_bitwise(N, K):
 
 @pytest.mark.parametrize("N,K", [(301, 5120), (37, 1280), (100, 256), (64, 17408)])
 def test_matvec_tma_and_register_kernels_agree_bitwise(N, K):
-    """Scales stored 2 bytes past a 16-byte boundary send 1..4-row launches to
-    the register-pipelined kernel instead of the TMA ring; the bits match."""
-    wq, wd, aq, ad = mv_inputs(N, K, 4, seed=5)
+    """Scales stored 2 bytes past a 16-byte boundary send every launch to the
+    register-pipelined kernel instead of the TMA ring (1..8 rows in one launch,
+    13..16 in two); the bits match at every row count."""
+    wq, wd, aq, ad = mv_inputs(N, K, 16, seed=5)
     W, D = cuda(wq), cuda(wd)
     buf = torch.zeros(wd.size + 8, dtype=torch.float16, device="cuda")
     buf[1:1 + wd.size] = D.flatten()
     D_odd = buf[1:1 + wd.size].view(wd.shape)
     assert D_odd.data_ptr() % 16 == 2
-    for T in range(1, 5):
+    for T in range(1, 17):
         A, Ad = cuda(aq[:T]), cuda(ad[:T])
         ring = host(luce.luce_q8_matvec_batch(W, D, A, Ad))
         reg = host(luce.luce_q8_matvec_batch(W, D_odd, A, Ad))
