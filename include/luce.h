@@ -316,6 +316,20 @@ int luce_decode_step(const luce_model* m, const luce_slot* slots, const int32_t*
                      void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * luce_decode_step with the rows' hidden states exchanged with the host, all
+ * on the stream and without waiting: x_in (host, fp32 [T][hidden]) is copied
+ * to x (device, the step's in/out rows), the step runs, then x is copied to
+ * x_out (host, nullable) and argmax to argmax_out (host, nullable; needs
+ * argmax).  Host buffers should be page-locked so the copies run
+ * asynchronously; the caller synchronises the stream before reading x_out.
+ * Validation is luce_decode_step's (plus a non-null x_in); a refused call
+ * enqueues nothing.
+ */
+int luce_decode_step_host(const luce_model* m, const luce_slot* slots, const int32_t* rows_per_slot, int n_seq,
+                          const float* x_in, float* x, float* x_out, float* logits, int32_t* argmax,
+                          int32_t* argmax_out, void* ws, size_t ws_bytes, void* stream);
+
+/*
  * A slot whose K/V lives in pages of LUCE_PAGE_KEYS tokens: pool page p holds
  * binary16 [n_layers][n_kv_heads][128][head_dim], so token j's K in layer l,
  * KV head g is k_pool[((table[j / 128] * n_layers + l) * n_kv_heads + g)

@@ -80,7 +80,7 @@ EXPORTS = ("luce_last_error", "luce_version", "luce_launch_count", "luce_q8_quan
            "luce_q8_block_dots", "luce_rope_posvec", "luce_kv_append", "luce_decode_attn_multiseq",
            "luce_decode_attn_workspace_size", "luce_decode_step_layout", "luce_decode_step",
            "luce_decode_attn_multiseq_noalloc", "luce_decode_attn_noalloc_max_bytes", "luce_decode_attn_paged",
-           "luce_decode_step_paged", "luce_wait_timeouts")
+           "luce_decode_step_paged", "luce_wait_timeouts", "luce_decode_step_host")
 
 _lib = None
 
@@ -118,6 +118,8 @@ def load_library(path: str = LIB_PATH):
                                            ctypes.POINTER(ctypes.c_int32), i32, vp, vp, vp, vp, sz, vp]
     lib.luce_decode_attn_noalloc_max_bytes.restype = sz
     lib.luce_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
+    lib.luce_decode_step_host.argtypes = [ctypes.POINTER(ModelC), ctypes.POINTER(SlotC), ctypes.POINTER(ctypes.c_int32),
+                                          i32, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     for name in EXPORTS:
         if name not in ("luce_last_error", "luce_version", "luce_launch_count", "luce_decode_attn_workspace_size",
                         "luce_decode_attn_noalloc_max_bytes"):
@@ -414,3 +416,26 @@ def luce_decode_step(model: Model, slots: Sequence[Slot], rows_per_slot: Sequenc
     _check(load_library().luce_decode_step(ctypes.byref(model.c), sc, rows, n, x.data_ptr(), _ptr(logits),
                                            _ptr(argmax), ws.data_ptr(), ws.numel(), _stream(stream)))
     return x
+
+
+def luce_decode_step_host(model: Model, slots: Sequence[Slot], rows_per_slot: Sequence[int], x_in, x, ws,
+                          x_out=None, logits=None, argmax=None, argmax_out=None, stream=None):
+    """luce_decode_step with host rows: x_in (CPU fp32 [T][hidden], ideally
+    pinned) is copied to x (device) on the stream, the step runs, and x (and
+    argmax) are copied back to x_out (and argmax_out) when given.  Nothing
+    waits: synchronise the stream before reading x_out."""
+    import torch
+    _need(x, torch.float32, "x")
+    if x_in.device.type != "cpu" or x_in.dtype != torch.float32 or not x_in.is_contiguous():
+        raise TypeError("x_in: expected a contiguous CPU float32 tensor")
+    if x_in.shape != x.shape or (x_out is not None and x_out.shape != x.shape):
+        raise ValueError("x_in, x and x_out must have the same shape")
+    n = len(slots)
+    sc = (SlotC * max(1, n))()
+    for i, s in enumerate(slots):
+        sc[i] = SlotC(s.k.data_ptr(), s.v.data_ptr(), s.len, s.cap)
+    rows = (ctypes.c_int32 * max(1, n))(*rows_per_slot)
+    _check(load_library().luce_decode_step_host(ctypes.byref(model.c), sc, rows, n, x_in.data_ptr(), x.data_ptr(),
+                                                _ptr(x_out), _ptr(logits), _ptr(argmax), _ptr(argmax_out),
+                                                ws.data_ptr(), ws.numel(), _stream(stream)))
+    return x_out

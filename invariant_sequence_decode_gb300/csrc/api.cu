@@ -460,15 +460,24 @@ struct StepSlot {
     const int32_t* table_host;
 };
 
+// Host buffers of luce_decode_step_host (all nullable): the step's input rows,
+// and where its output rows and argmax are copied back.
+struct HostIO {
+    const float* x_in;
+    float* x_out;
+    int32_t* argmax_out;
+};
+
 static int decode_step_impl(const luce_model* m, const StepSlot* slots, const int32_t* rows_per_slot, int n_seq,
                             float* x, float* logits, int32_t* argmax, void* ws, size_t ws_bytes, void* stream,
-                            const char* who)
+                            const char* who, const HostIO& io = HostIO{nullptr, nullptr, nullptr})
 {
     REQUIRE(x && ws, LUCE_EINVAL, "%s: null x/ws", who);
     REQUIRE(aligned(x, 16) && aligned(ws, 256), LUCE_EINVAL, "%s: x must be 16-byte and ws 256-byte aligned", who);
     REQUIRE(!(logits || argmax) || (m->vocab > 0 && m->final_norm && m->head_q && m->head_d), LUCE_EINVAL,
             "%s: logits/argmax need vocab > 0 and the head weights", who);
     REQUIRE(!argmax || logits, LUCE_EINVAL, "%s: argmax needs the logits buffer", who);
+    REQUIRE(!io.argmax_out || argmax, LUCE_EINVAL, "%s: argmax_out needs the argmax buffer", who);
     const int H = m->hidden, Hq = m->n_q_heads, Hkv = m->n_kv_heads, D = m->head_dim, F = m->ffn;
     int T = 0, max_len = 1;
     for (int s = 0; s < n_seq; ++s) {
@@ -522,8 +531,16 @@ static int decode_step_impl(const luce_model* m, const StepSlot* slots, const in
                 pos.pos[r] = slots[s].len + j;
             }
     }
-    const RopeFreq freq = rope_freq(m->rope_theta);
+    // the 64 inverse frequencies of the model's theta, formed once per thread and theta
+    thread_local double freq_theta = -1.0;
+    thread_local RopeFreq freq;
+    if (freq_theta != m->rope_theta) {
+        freq = rope_freq(m->rope_theta);
+        freq_theta = m->rope_theta;
+    }
     cudaError_t e = cudaSuccess;
+    if (io.x_in && (e = cudaMemcpyAsync(x, io.x_in, (size_t)T * H * sizeof(float), cudaMemcpyHostToDevice, st)))
+        return cuda_status(e, who);
 
     const float scale = (float)(1.0 / sqrt((double)D));
     const int64_t page_elems = (int64_t)Hkv * kPageKeys * D;   // one layer of one page
@@ -601,6 +618,11 @@ static int decode_step_impl(const luce_model* m, const StepSlot* slots, const in
             return cuda_status(e, who);
         if (argmax && (e = launch_argmax(logits, T, m->vocab, argmax, st))) return cuda_status(e, who);
     }
+    if (io.x_out && (e = cudaMemcpyAsync(io.x_out, x, (size_t)T * H * sizeof(float), cudaMemcpyDeviceToHost, st)))
+        return cuda_status(e, who);
+    if (io.argmax_out &&
+        (e = cudaMemcpyAsync(io.argmax_out, argmax, (size_t)T * sizeof(int32_t), cudaMemcpyDeviceToHost, st)))
+        return cuda_status(e, who);
     return ok();
 }
 
@@ -612,16 +634,15 @@ static int check_rows(const int32_t* rows_per_slot, int s, const char* who)
     return LUCE_OK;
 }
 
-int luce_decode_step(const luce_model* m, const luce_slot* slots, const int32_t* rows_per_slot, int n_seq,
-                     float* x, float* logits, int32_t* argmax, void* ws, size_t ws_bytes, void* stream)
+// Validates flat slots into ss; LUCE_OK or the refusal.
+static int flat_slots(const luce_model* m, const luce_slot* slots, const int32_t* rows_per_slot, int n_seq,
+                      StepSlot* ss, const char* who)
 {
-    const char* who = "decode_step";
     int rc = check_model(m, who);
     if (rc) return rc;
     REQUIRE(slots && rows_per_slot, LUCE_EINVAL, "%s: null slots/rows", who);
     REQUIRE(n_seq >= 1 && n_seq <= LUCE_MAX_SEQ, LUCE_EINVAL,
             "%s: n_seq=%d outside 1..%d (more than %d slots are refused)", who, n_seq, LUCE_MAX_SEQ, LUCE_MAX_SEQ);
-    StepSlot ss[LUCE_MAX_SEQ];
     for (int s = 0; s < n_seq; ++s) {
         const luce_slot& sl = slots[s];
         if ((rc = check_rows(rows_per_slot, s, who))) return rc;
@@ -638,7 +659,30 @@ int luce_decode_step(const luce_model* m, const luce_slot* slots, const int32_t*
         ss[s] = StepSlot{reinterpret_cast<__half*>(sl.k), reinterpret_cast<__half*>(sl.v), sl.len, sl.cap, nullptr,
                          nullptr};
     }
+    return LUCE_OK;
+}
+
+int luce_decode_step(const luce_model* m, const luce_slot* slots, const int32_t* rows_per_slot, int n_seq,
+                     float* x, float* logits, int32_t* argmax, void* ws, size_t ws_bytes, void* stream)
+{
+    const char* who = "decode_step";
+    StepSlot ss[LUCE_MAX_SEQ];
+    const int rc = flat_slots(m, slots, rows_per_slot, n_seq, ss, who);
+    if (rc) return rc;
     return decode_step_impl(m, ss, rows_per_slot, n_seq, x, logits, argmax, ws, ws_bytes, stream, who);
+}
+
+int luce_decode_step_host(const luce_model* m, const luce_slot* slots, const int32_t* rows_per_slot, int n_seq,
+                          const float* x_in, float* x, float* x_out, float* logits, int32_t* argmax,
+                          int32_t* argmax_out, void* ws, size_t ws_bytes, void* stream)
+{
+    const char* who = "decode_step_host";
+    REQUIRE(x_in, LUCE_EINVAL, "%s: null x_in", who);
+    StepSlot ss[LUCE_MAX_SEQ];
+    const int rc = flat_slots(m, slots, rows_per_slot, n_seq, ss, who);
+    if (rc) return rc;
+    return decode_step_impl(m, ss, rows_per_slot, n_seq, x, logits, argmax, ws, ws_bytes, stream, who,
+                            HostIO{x_in, x_out, argmax_out});
 }
 
 int luce_decode_step_paged(const luce_model* m, const luce_paged_slot* slots, const int32_t* rows_per_slot,

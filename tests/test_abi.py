@@ -142,6 +142,26 @@ def test_decode_step_refusals(lib):
     assert step(ctypes.byref(mh), s, rows([1, 1]), 2, P, None, None, P, big, None) == luce.LUCE_EINVAL
 
 
+def test_decode_step_host_refusals(lib):
+    """The host-buffer step validates like the device step, plus its own
+    buffers, and enqueues nothing (no copy either) when it refuses."""
+    m, _keep = fake_model()
+    big = 1 << 40
+    host = lib.luce_decode_step_host
+    s = slots([(3, 64), (3, 64)])
+    xin = (ctypes.c_float * 16)()
+    # null x_in
+    assert host(ctypes.byref(m), s, rows([1, 1]), 2, None, P, None, None, None, None, P, big, None) == luce.LUCE_EINVAL
+    # the device step's refusals apply: 5 slots, a row count above 4, too small a workspace
+    assert host(ctypes.byref(m), slots([(3, 64)] * 5), rows([1] * 5), 5, xin, P, None, None, None, None, P, big,
+                None) == luce.LUCE_EINVAL
+    assert host(ctypes.byref(m), s, rows([1, 5]), 2, xin, P, None, None, None, None, P, big, None) == luce.LUCE_EINVAL
+    assert host(ctypes.byref(m), s, rows([1, 1]), 2, xin, P, None, None, None, None, P, 1024, None) == luce.LUCE_ENOSPACE
+    # argmax_out without the argmax buffer
+    out = (ctypes.c_int32 * 2)()
+    assert host(ctypes.byref(m), s, rows([1, 1]), 2, xin, P, None, None, None, out, P, big, None) == luce.LUCE_EINVAL
+
+
 def test_step_layout_is_monotone_and_part_is_last(lib):
     m, _keep = fake_model()
     lay = luce.StepLayoutC()

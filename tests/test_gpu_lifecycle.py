@@ -151,3 +151,26 @@ def test_phase_soak_batched_equals_solo_and_identical_phases_stay_identical(mode
     for s in range(4):
         for a, b in zip(batched[s], solo[s]):
             assert np.array_equal(host(a)[:, :, :lens[s]].view(np.uint16), host(b)[:, :, :lens[s]].view(np.uint16))
+
+
+def test_host_buffer_step_equals_device_step_bitwise(model):
+    """luce_decode_step_host: pinned host rows in, the same step, rows and
+    argmax copied back on the stream - the same bits as the device-buffer step."""
+    L = 37
+    xr = rows(9, 3)
+    k1, v1 = cache(14, L)
+    hd, ld, ad = step(model, [(k1, v1, L)], [xr], [3])
+    k2, v2 = cache(14, L)
+    x_in = torch.from_numpy(np.ascontiguousarray(xr)).pin_memory()
+    x_out = torch.empty_like(x_in).pin_memory()
+    am_out = torch.empty(3, dtype=torch.int32).pin_memory()
+    x = torch.empty(x_in.shape, dtype=torch.float32, device="cuda")
+    logits = torch.empty((3, VOCAB), dtype=torch.float32, device="cuda")
+    am = torch.empty(3, dtype=torch.int32, device="cuda")
+    ws = model.workspace(3, CAP)
+    luce.luce_decode_step_host(model, [luce.Slot(k2, v2, L)], [3], x_in, x, ws, x_out=x_out, logits=logits,
+                               argmax=am, argmax_out=am_out)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(x_out.numpy()), bits(hd)) and np.array_equal(am_out.numpy(), ad)
+    assert np.array_equal(bits(host(logits)), bits(ld))
+    assert np.array_equal(host(k1).view(np.uint16), host(k2).view(np.uint16))
