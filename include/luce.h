@@ -82,6 +82,15 @@ uint64_t luce_launch_count(void);
 int luce_wait_timeouts(uint32_t* count, int reset);
 
 /*
+ * Test hook for the expiry path above: enqueues one kernel whose single
+ * bounded wait (limit_ns, 1 us .. 1 s) is on a shared-memory barrier that
+ * nothing completes, so the wait runs out, adds one to the counter and the
+ * kernel returns; the context stays usable.  Returns LUCE_OK, LUCE_EINVAL or
+ * LUCE_ECUDA.
+ */
+int luce_test_wait_expiry(int64_t limit_ns, void* stream);
+
+/*
  * Activation quantization to q8_0 blocks [qfuse, item 2: the consumer's
  * division and rounding convention; ds4-604, Commit walkthrough].
  * For each row t and block b of 32 values: amax = max|x| (NaN skipped),

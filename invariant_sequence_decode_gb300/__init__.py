@@ -80,7 +80,8 @@ EXPORTS = ("luce_last_error", "luce_version", "luce_launch_count", "luce_q8_quan
            "luce_q8_block_dots", "luce_rope_posvec", "luce_kv_append", "luce_decode_attn_multiseq",
            "luce_decode_attn_workspace_size", "luce_decode_step_layout", "luce_decode_step",
            "luce_decode_attn_multiseq_noalloc", "luce_decode_attn_noalloc_max_bytes", "luce_decode_attn_paged",
-           "luce_decode_step_paged", "luce_wait_timeouts", "luce_decode_step_host")
+           "luce_decode_step_paged", "luce_wait_timeouts", "luce_decode_step_host",
+           "luce_test_wait_expiry")
 
 _lib = None
 
@@ -118,6 +119,7 @@ def load_library(path: str = LIB_PATH):
                                            ctypes.POINTER(ctypes.c_int32), i32, vp, vp, vp, vp, sz, vp]
     lib.luce_decode_attn_noalloc_max_bytes.restype = sz
     lib.luce_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
+    lib.luce_test_wait_expiry.argtypes = [i64, vp]
     lib.luce_decode_step_host.argtypes = [ctypes.POINTER(ModelC), ctypes.POINTER(SlotC), ctypes.POINTER(ctypes.c_int32),
                                           i32, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     for name in EXPORTS:

@@ -98,6 +98,13 @@ int luce_wait_timeouts(uint32_t* count, int reset)
     return cuda_status(read_wait_timeouts(count, reset != 0), "wait_timeouts");
 }
 
+int luce_test_wait_expiry(int64_t limit_ns, void* stream)
+{
+    REQUIRE(limit_ns >= 1000 && limit_ns <= 1000000000, LUCE_EINVAL,
+            "test_wait_expiry: limit_ns=%lld outside 1 us .. 1 s", (long long)limit_ns);
+    return cuda_status(launch_wait_expiry((uint64_t)limit_ns, (cudaStream_t)stream), "test_wait_expiry");
+}
+
 int luce_q8_quantize_act(const float* x, int T, int K, int64_t ldx, int8_t* q, float* d, void* stream)
 {
     REQUIRE(x && q && d, LUCE_EINVAL, "quantize_act: null pointer");

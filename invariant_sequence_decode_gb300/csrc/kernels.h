@@ -79,6 +79,9 @@ cudaError_t launch_qkv_rope_tma(const int8_t* wq, const __half* wd, int K, const
 // (synchronous); reset clears the counter.
 cudaError_t read_wait_timeouts(uint32_t* count, bool reset);
 
+// One bounded wait that nothing completes (limit_ns), counted as expired.
+cudaError_t launch_wait_expiry(uint64_t limit_ns, cudaStream_t s);
+
 // The step's q|k|v projection (N = (Hq + 2*Hkv) * 128 rows) with RoPE of the
 // q and k heads at each row's position, q heads to q_rot [T][Hq][128], k and v
 // heads appended as binary16 at rows' K/V destinations; qkv [T][N] also written.

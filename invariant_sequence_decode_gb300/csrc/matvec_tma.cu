@@ -102,18 +102,33 @@ __device__ __forceinline__ uint64_t global_ns()
     return t;
 }
 
-// Wait for the phase of parity `parity` to complete, for about a second at
-// most; false (and one more timeout counted) if it did not.
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity)
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // about one second
+
+// Wait for the phase of parity `parity` to complete, for limit_ns at most
+// (and at most 2^26 polls, should the timer not advance); false (and one
+// more timeout counted) if it did not.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, uint64_t limit_ns = kWaitLimitNs)
 {
     if (mbar_try(b, parity)) return true;
     const uint64_t t0 = global_ns();
-    while (!mbar_try(b, parity))
-        if (global_ns() - t0 > 1000000000ull) {
+    for (uint32_t polls = 0; !mbar_try(b, parity); ++polls)
+        if (global_ns() - t0 > limit_ns || polls >= (1u << 26)) {
             atomicAdd(&g_wait_timeouts, 1u);
             return false;
         }
     return true;
+}
+
+// Exercises the expiry path: one thread waits, for limit_ns, on a barrier
+// that expects one arrival nobody makes (no copy is issued), so the wait
+// runs out, is counted, and the kernel returns normally.
+__global__ void wait_expiry_kernel(uint64_t limit_ns)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_wait(&bar, 0, limit_ns);
 }
 
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, int x, int y, int z, uint64_t* bar)
@@ -649,6 +664,13 @@ cudaError_t launch_qkv_rope_tma(const int8_t* wq, const __half* wd, int K, const
         case 3: return launch_qkv_tma_t<3, false>(mw, md8, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
         default: return launch_qkv_tma_t<4, false>(mw, md8, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
     }
+}
+
+cudaError_t launch_wait_expiry(uint64_t limit_ns, cudaStream_t s)
+{
+    wait_expiry_kernel<<<1, 32, 0, s>>>(limit_ns);
+    count_launches(1);
+    return cudaGetLastError();
 }
 
 cudaError_t read_wait_timeouts(uint32_t* count, bool reset)

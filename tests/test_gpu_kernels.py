@@ -308,3 +308,19 @@ def test_attention_batched_equals_solo_bitwise():
     for (L, n, newr0), s in zip(vv, order):
         old = views[s][2]
         assert np.array_equal(perm[newr0:newr0 + n].view(np.uint32), batched[old:old + n].view(np.uint32))
+
+
+def test_bounded_wait_expires_counts_and_leaves_the_context_usable():
+    """A wait on a barrier that nothing completes gives up after its limit,
+    is counted by luce_wait_timeouts, and the next launches run normally."""
+    lib = luce.load_library()
+    luce.wait_timeouts(reset=True)
+    assert lib.luce_test_wait_expiry(5_000_000, torch.cuda.current_stream().cuda_stream) == 0
+    torch.cuda.synchronize()
+    assert luce.wait_timeouts(reset=True) == 1
+    wq, wd, aq, ad = mv_inputs(301, 5120, 4, seed=8)
+    y = host(luce.luce_q8_matvec_batch(cuda(wq), cuda(wd), cuda(aq), cuda(ad)))
+    ref = oracle.matvec(wq, wd, aq, ad)
+    assert np.all(rel_row_err(y.astype(np.float64), ref) <= 1e-5)
+    assert luce.wait_timeouts() == 0
+    assert lib.luce_test_wait_expiry(10, None) == luce.LUCE_EINVAL
