@@ -441,3 +441,36 @@ def luce_decode_step_host(model: Model, slots: Sequence[Slot], rows_per_slot: Se
                                                 _ptr(x_out), _ptr(logits), _ptr(argmax), _ptr(argmax_out),
                                                 ws.data_ptr(), ws.numel(), _stream(stream)))
     return x_out
+
+
+class HostStep:
+    """luce_decode_step_host with its arguments marshalled once, for repeated
+    steps over the same slots and buffers: each call copies the slots' current
+    ``len`` into the prepared slot array and makes the C call (nothing else is
+    re-checked).  The stream is the one given, or the current stream at
+    construction.  Synchronise the stream before reading x_out."""
+
+    def __init__(self, model: Model, slots: Sequence[Slot], rows_per_slot: Sequence[int], x_in, x, ws,
+                 x_out=None, logits=None, argmax=None, argmax_out=None, stream=None):
+        import torch
+        _need(x, torch.float32, "x")
+        if x_in.device.type != "cpu" or x_in.dtype != torch.float32 or not x_in.is_contiguous():
+            raise TypeError("x_in: expected a contiguous CPU float32 tensor")
+        if x_in.shape != x.shape or (x_out is not None and x_out.shape != x.shape):
+            raise ValueError("x_in, x and x_out must have the same shape")
+        self.slots = list(slots)
+        n = len(self.slots)
+        self._sc = (SlotC * max(1, n))()
+        for i, s in enumerate(self.slots):
+            self._sc[i] = SlotC(s.k.data_ptr(), s.v.data_ptr(), s.len, s.cap)
+        self._rows = (ctypes.c_int32 * max(1, n))(*rows_per_slot)
+        self._keep = (model, x_in, x, ws, x_out, logits, argmax, argmax_out)
+        self._fn = load_library().luce_decode_step_host
+        self._args = (ctypes.byref(model.c), self._sc, self._rows, n, x_in.data_ptr(), x.data_ptr(), _ptr(x_out),
+                      _ptr(logits), _ptr(argmax), _ptr(argmax_out), ws.data_ptr(), ws.numel(), _stream(stream))
+
+    def __call__(self):
+        sc = self._sc
+        for i, s in enumerate(self.slots):
+            sc[i].len = s.len
+        _check(self._fn(*self._args))

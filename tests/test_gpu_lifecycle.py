@@ -174,3 +174,17 @@ def test_host_buffer_step_equals_device_step_bitwise(model):
     assert np.array_equal(bits(x_out.numpy()), bits(hd)) and np.array_equal(am_out.numpy(), ad)
     assert np.array_equal(bits(host(logits)), bits(ld))
     assert np.array_equal(host(k1).view(np.uint16), host(k2).view(np.uint16))
+    # the prepared form: the same call twice (slot len advanced by 3 in between)
+    k3, v3 = cache(14, L)
+    sl = luce.Slot(k3, v3, L)
+    plan = luce.HostStep(model, [sl], [3], x_in, x, ws, x_out=x_out, logits=logits, argmax=am, argmax_out=am_out)
+    plan()
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(x_out.numpy()), bits(hd)) and np.array_equal(am_out.numpy(), ad)
+    sl.len = L + 3
+    plan()
+    k4, v4 = cache(14, L)
+    step(model, [(k4, v4, L)], [xr], [3])
+    h2, _, a2 = step(model, [(k4, v4, L + 3)], [xr], [3])
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(x_out.numpy()), bits(h2)) and np.array_equal(am_out.numpy(), a2)
