@@ -69,8 +69,9 @@ cudaError_t launch_matvec(const int8_t* wq, const __half* wd, int N, int K, cons
 cudaError_t launch_matvec_tma(const int8_t* wq, const __half* wd, int N, int K, const int8_t* aq, const float* ad,
                               int T, float* y, int64_t ldy, const float* resid, int64_t ldr, cudaStream_t s);
 
-// The fused q|k|v + RoPE + K/V-append projection on the TMA ring (1..4
-// rows); cudaErrorNotSupported, with nothing launched, otherwise.
+// The fused q|k|v + RoPE + K/V-append projection on the TMA ring (1..8 rows
+// in one launch, 13..16 in two); cudaErrorNotSupported, with nothing
+// launched, otherwise.
 cudaError_t launch_qkv_rope_tma(const int8_t* wq, const __half* wd, int K, const int8_t* aq, const float* ad, int T,
                                 float* qkv, int Hq, int Hkv, const RowPos& pos, const RopeFreq& f, float* q_rot,
                                 const KvRows& kv, cudaStream_t s);

@@ -257,10 +257,10 @@ cudaError_t launch_qkv_rope(const int8_t* wq, const __half* wd, int K, const int
                             float* qkv, int Hq, int Hkv, const RowPos& pos, const RopeFreq& f, float* q_rot,
                             const KvRows& kv, cudaStream_t s)
 {
-    // up to 4 rows on the TMA ring when the shapes allow (matvec_tma.cu);
+    // 1..8 and 13..16 rows on the TMA ring when the shapes allow (matvec_tma.cu);
     // otherwise the plain kernel's launch shapes, except G = 4 where the plain
     // kernel takes G = 3 (T = 3, 12): the rotation pairs P = 2G must tile 64
-    if (T <= 4) {
+    {
         const cudaError_t e = launch_qkv_rope_tma(wq, wd, K, aq, ad, T, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
         if (e != cudaErrorNotSupported) return e;
     }

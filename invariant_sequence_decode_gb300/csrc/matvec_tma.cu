@@ -377,19 +377,20 @@ q8_matvec_tma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_consta
 
 // The decode step's q|k|v projection with the RoPE rotation and the K/V
 // append in the epilogue ("antirez/ds4 pull 604", Commit walkthrough): the
-// same chains, one group per CTA, the group being the rotation pairs
-// (i, i + 64) for i in [q0, q0 + 8) of head h = b / 8, q0 = 8 (b % 8).  Quads
-// 0-1 are rows h*128 + q0 + [0, 8), quads 2-3 rows h*128 + 64 + q0 + [0, 8);
-// md8 is the scale map with an 8-row box.  Thread idx < 8T finishes pair
-// p = idx / T of token t = idx % T exactly as q8_qkv_rope_kernel does.
-template <int T, bool BIAS>
+// same chains, one group per CTA, the group being the P = 2G rotation pairs
+// (i, i + 64) for i in [q0, q0 + P) of head h = b / (64/P), q0 = P (b % (64/P)).
+// Quads [0, G/2) are rows h*128 + q0 + [0, P), quads [G/2, G) rows
+// h*128 + 64 + q0 + [0, P); mdp is the scale map with a P-row box.  Thread
+// idx < P*T finishes pair p = idx / T of token t = idx % T exactly as
+// q8_qkv_rope_kernel does.
+template <int T, int G, int S, bool BIAS>
 __global__ void __launch_bounds__(kRingThreads)
-q8_qkv_rope_tma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap md8,
+q8_qkv_rope_tma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mdp,
                        const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mad, int K,
                        float* __restrict__ qkv, int Hq, int Hkv, const __grid_constant__ RowPos pos,
                        const __grid_constant__ RopeFreq f, float* __restrict__ q_rot, const __grid_constant__ KvRows kv)
 {
-    constexpr int G = 4, S = 2, P = 2 * G, GROUPS = (kHeadDim / 2) / P;
+    constexpr int P = 2 * G, GROUPS = (kHeadDim / 2) / P;
     using L = RingLayout<T, G, S>;
     static_assert(P * T <= 128, "one (pair, token) per consumer thread");
     extern __shared__ uint8_t smem_raw[];
@@ -410,9 +411,10 @@ q8_qkv_rope_tma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_cons
                 const int j = it % nj;
 #pragma unroll
                 for (int qq = 0; qq < G; ++qq)
-                    tma_load_3d(slot + qq * 4096, &mw, 0, 4 * j, (qq < 2 ? row0 : row1) + 4 * (qq & 1), bar);
-                tma_load_2d(slot + L::W, &md8, 32 * j, row0, bar);
-                tma_load_2d(slot + L::W + P * 64, &md8, 32 * j, row1, bar);
+                    tma_load_3d(slot + qq * 4096, &mw, 0, 4 * j,
+                                (qq < G / 2 ? row0 + 4 * qq : row1 + 4 * (qq - G / 2)), bar);
+                tma_load_2d(slot + L::W, &mdp, 32 * j, row0, bar);
+                tma_load_2d(slot + L::W + P * 64, &mdp, 32 * j, row1, bar);
             },
             [&](int) { return G * 4096 + L::D; });
         return;
@@ -569,18 +571,18 @@ cudaError_t launch_tma_t(const CUtensorMap& mw, const CUtensorMap& md, const CUt
     return e;
 }
 
-template <int T, bool BIAS>
-cudaError_t launch_qkv_tma_t(const CUtensorMap& mw, const CUtensorMap& md8, const CUtensorMap& ma,
+template <int T, int G, int S, bool BIAS>
+cudaError_t launch_qkv_tma_t(const CUtensorMap& mw, const CUtensorMap& mdp, const CUtensorMap& ma,
                              const CUtensorMap& mad, int K, float* qkv, int Hq, int Hkv, const RowPos& pos,
                              const RopeFreq& f, float* q_rot, const KvRows& kv, cudaStream_t s)
 {
-    using L = RingLayout<T, 4, 2>;
+    using L = RingLayout<T, G, S>;
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
-    if (set_smem_once(q8_qkv_rope_tma_kernel<T, BIAS>, L::SMEM, once, attr) != cudaSuccess) return attr;
-    const int groups = (Hq + 2 * Hkv) * ((kHeadDim / 2) / 8);
-    const cudaError_t e = launch_pdl_smem(q8_qkv_rope_tma_kernel<T, BIAS>, dim3(groups), dim3(kRingThreads), L::SMEM,
-                                          s, mw, md8, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv);
+    if (set_smem_once(q8_qkv_rope_tma_kernel<T, G, S, BIAS>, L::SMEM, once, attr) != cudaSuccess) return attr;
+    const int groups = (Hq + 2 * Hkv) * ((kHeadDim / 2) / (2 * G));
+    const cudaError_t e = launch_pdl_smem(q8_qkv_rope_tma_kernel<T, G, S, BIAS>, dim3(groups), dim3(kRingThreads),
+                                          L::SMEM, s, mw, mdp, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv);
     count_launches(1);
     return e;
 }
@@ -651,19 +653,52 @@ cudaError_t launch_matvec_tma(const int8_t* wq, const __half* wd, int N, int K, 
                             resid ? resid + 8 * ldr : nullptr, ldr, sms, s);
 }
 
+// One fused launch of T <= 8 rows: 8 rotation pairs per group over two slots
+// up to 4 rows, 4 pairs over three slots for 5..8.
+static cudaError_t qkv_ring_rows(const int8_t* wq, const __half* wd, int K, const int8_t* aq, const float* ad, int T,
+                                 float* qkv, int Hq, int Hkv, const RowPos& pos, const RopeFreq& f, float* q_rot,
+                                 const KvRows& kv, cudaStream_t s)
+{
+    const int N = (Hq + 2 * Hkv) * kHeadDim;
+    CUtensorMap mw, mdp, ma, mad;
+    if (!ring_maps(wq, wd, N, K, aq, ad, T, T <= 4 ? 8 : 4, &mw, &mdp, &ma, &mad)) return cudaErrorNotSupported;
+    constexpr int SW = kRingSlotsWide;
+    switch (T) {
+        case 1: return launch_qkv_tma_t<1, 4, 2, true>(mw, mdp, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
+        case 2: return launch_qkv_tma_t<2, 4, 2, false>(mw, mdp, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
+        case 3: return launch_qkv_tma_t<3, 4, 2, false>(mw, mdp, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
+        case 4: return launch_qkv_tma_t<4, 4, 2, false>(mw, mdp, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
+        case 5: return launch_qkv_tma_t<5, 2, SW, false>(mw, mdp, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
+        case 6: return launch_qkv_tma_t<6, 2, SW, false>(mw, mdp, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
+        case 7: return launch_qkv_tma_t<7, 2, SW, false>(mw, mdp, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
+        default: return launch_qkv_tma_t<8, 2, SW, false>(mw, mdp, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
+    }
+}
+
 cudaError_t launch_qkv_rope_tma(const int8_t* wq, const __half* wd, int K, const int8_t* aq, const float* ad, int T,
                                 float* qkv, int Hq, int Hkv, const RowPos& pos, const RopeFreq& f, float* q_rot,
                                 const KvRows& kv, cudaStream_t s)
 {
+    // 1..8 rows: one launch; 13..16 rows: rows 0..7, then rows 8..T-1 (their
+    // positions and K/V destinations shifted down); 9..12 rows: not taken
+    if (T < 1 || (T > 8 && T < 13) || T > 16) return cudaErrorNotSupported;
+    if (T <= 8) return qkv_ring_rows(wq, wd, K, aq, ad, T, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
     const int N = (Hq + 2 * Hkv) * kHeadDim;
-    CUtensorMap mw, md8, ma, mad;
-    if (T > 4 || !ring_maps(wq, wd, N, K, aq, ad, T, 8, &mw, &md8, &ma, &mad)) return cudaErrorNotSupported;
-    switch (T) {
-        case 1: return launch_qkv_tma_t<1, true>(mw, md8, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
-        case 2: return launch_qkv_tma_t<2, false>(mw, md8, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
-        case 3: return launch_qkv_tma_t<3, false>(mw, md8, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
-        default: return launch_qkv_tma_t<4, false>(mw, md8, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
+    CUtensorMap probe[4];
+    if (!ring_maps(wq, wd, N, K, aq + (size_t)8 * K, ad + (size_t)8 * (K / 32), T - 8, 4, &probe[0], &probe[1],
+                   &probe[2], &probe[3]))
+        return cudaErrorNotSupported;  // both halves take the ring or neither does
+    RowPos pos_hi{};
+    KvRows kv_hi{};
+    pos_hi.n_rows = kv_hi.n_rows = T - 8;
+    for (int t = 8; t < T; ++t) {
+        pos_hi.pos[t - 8] = pos.pos[t];
+        kv_hi.row[t - 8] = kv.row[t];
     }
+    const cudaError_t e = qkv_ring_rows(wq, wd, K, aq, ad, 8, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
+    if (e != cudaSuccess) return e;
+    return qkv_ring_rows(wq, wd, K, aq + (size_t)8 * K, ad + (size_t)8 * (K / 32), T - 8, qkv + (size_t)8 * N, Hq, Hkv,
+                         pos_hi, f, q_rot + (size_t)8 * Hq * kHeadDim, kv_hi, s);
 }
 
 cudaError_t launch_wait_expiry(uint64_t limit_ns, cudaStream_t s)

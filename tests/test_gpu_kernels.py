@@ -155,6 +155,40 @@ def test_matvec_tma_and_register_kernels_agree_bitwise(N, K):
     assert luce.wait_timeouts() == 0
 
 
+@pytest.mark.parametrize("K", [2048, 4096, 5120, 8192])
+def test_matvec_invariance_sweep_full_sizes(K):
+    """Batch-invariance sweep at the sweep's sizes: n_tok 1..4 x N in
+    {4096, 8192, 17408, 32768} (weights drawn on the device from a seeded
+    generator): every row of every launch, and of a launch with the rows
+    permuted, equals the row launched alone, bit for bit; rows past the
+    launch's are never written; sampled outputs match the oracle."""
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(2000 + K)
+    x = torch.randn((4, K), generator=gen, device="cuda")
+    aq, ad = luce.luce_q8_quantize_act(x)
+    for N in (4096, 8192, 17408, 32768):
+        W = torch.randint(-127, 128, (N, K), generator=gen, device="cuda", dtype=torch.int8)
+        D = (torch.rand((N, K // 32), generator=gen, device="cuda") * 2e-4 + 1e-5).to(torch.float16)
+        solo = [host(luce.luce_q8_matvec_batch(W, D, aq[t:t + 1], ad[t:t + 1]))[0] for t in range(4)]
+        for T in range(1, 5):
+            buf = torch.full((5, N), float("nan"), device="cuda")
+            luce.luce_q8_matvec_batch(W, D, aq[:T], ad[:T], buf[:T])
+            yb = host(buf)
+            for t in range(T):
+                assert np.array_equal(yb[t].view(np.uint32), solo[t].view(np.uint32)), (N, T, t)
+            assert np.all(np.isnan(yb[T:]))
+        perm = synth.permutation(K, N, 4)
+        yp = host(luce.luce_q8_matvec_batch(W, D, aq[perm], ad[perm]))
+        for i, t in enumerate(perm):
+            assert np.array_equal(yp[i].view(np.uint32), solo[t].view(np.uint32)), (N, "perm", i)
+        rows = np.sort(synth.permutation(K, N + 1, N)[:48])
+        idx = torch.from_numpy(rows).cuda()
+        ref = oracle.matvec(host(W[idx]), host(D[idx].view(torch.int16)).view(np.float16), host(aq), host(ad))
+        got = np.stack(solo)[:, rows].astype(np.float64)
+        assert np.all(rel_row_err(got, ref) <= 1e-5), (N, K)
+        del W, D
+
+
 def test_matvec_writes_only_its_outputs():
     N, K, T = 100, 256, 3
     wq, wd, aq, ad = mv_inputs(N, K, T)
