@@ -1,5 +1,6 @@
-// matvec_tma.cu - the q8_0 matvec for 1..4 activation rows, with the weights
-// streamed through shared memory by the tensor memory accelerator (TMA).
+// matvec_tma.cu - the q8_0 matvec for 1..8 activation rows (13..16 in two
+// launches), with the weights streamed through shared memory by the tensor
+// memory accelerator (TMA); also the fused q|k|v + RoPE + K/V-append form.
 //
 // Arithmetic: the same as q8_matvec_kernel (matvec.cu).  Block b of a weight
 // row feeds chain b mod 32; each chain adds its blocks in ascending order,
@@ -10,28 +11,29 @@
 // stays exact).
 //
 // Work split (GB300): persistent CTAs, three per SM, each owning a contiguous
-// range of 4-row quads of W.  A CTA walks its rows in groups of 16 (4 quads).
-// A stage is one kilobyte of K of a group: block c of stage j is block
-// 32j + c, one block for each of the 32 chains.  One producer thread keeps a
-// two-slot ring of stages in flight with tensor copies (W viewed as
-// [N][K/256][256], one 4-row x 1 KB box per quad; the group's scales, the
-// activation rows' 32 blocks and their scales as one box each), the arrival
-// of a slot signalled on an mbarrier by the copies' byte count.  Four consumer
-// warps read the slot from shared memory: lane (r = lane / 8, kb = lane % 8)
-// of warp w runs chain c = kb + 8w of rows r, r + 4, r + 8 and r + 12 of the
-// group, releases the slot once its operands are in registers, then does the
-// dp4a work.  The copy engine fills boxes past the end of W or of the
-// activations (rows >= N, blocks >= K/32) with zeros; the lanes that own such
-// blocks skip them and rows past the CTA's range are never written.
+// range of 4-row quads of W.  A CTA walks its rows in groups of G quads (4G
+// rows; G = 4 up to 4 activation rows, 2 for 5..8).  A stage is one kilobyte
+// of K of a group: block c of stage j is block 32j + c, one block for each of
+// the 32 chains.  One producer thread keeps a ring of S stages in flight (2 up
+// to 4 rows, 3 for 5..8) with tensor copies (W viewed as [N][K/256][256], one
+// 4-row x 1 KB box per quad; the group's scales, the activation rows' 32
+// blocks and their scales as one box each), the arrival of a slot signalled on
+// an mbarrier by the copies' byte count.  Four consumer warps read the slot
+// from shared memory: lane (r = lane / 8, kb = lane % 8) of warp w runs chain
+// c = kb + 8w of rows r, r + 4, ..., r + 4(G-1) of the group, releases the slot
+// once its operands are in registers, then does the dp4a work.  The copy
+// engine fills boxes past the end of W or of the activations (rows >= N,
+// blocks >= K/32) with zeros; the lanes that own such blocks skip them and
+// rows past the CTA's range are never written.
 //
 // Why: the register-pipelined kernel keeps one stage of weights in flight per
 // warp while it computes the other, and at 162 registers (12 warps per SM) that
 // left ~30 % of the HBM stream idle at 4 rows; here the ring keeps copies in
 // flight during the dp4a work and the consumers need ~125 registers.
 //
-// Every wait is bounded (about one second on the global timer); a wait that
-// expires adds one to a device counter (luce_wait_timeouts) and the CTA stops
-// consuming, leaving its remaining outputs unwritten.
+// Every wait is bounded (about one second on the global timer, 2^26 polls);
+// a wait that expires adds one to a device counter (luce_wait_timeouts) and
+// the CTA stops consuming, leaving its remaining outputs unwritten.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
