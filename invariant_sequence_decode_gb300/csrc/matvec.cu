@@ -89,7 +89,7 @@ __device__ __forceinline__ void q8_chains(const int8_t* __restrict__ wq, const _
     }
 }
 
-template <int T, int KL, int G, bool PF, bool BIAS>
+template <int T, int KL, int G, bool BIAS>
 __global__ void __launch_bounds__(32 * (32 / KL))
 q8_matvec_kernel(const int8_t* __restrict__ wq, const __half* __restrict__ wd, int N, int K,
                  const int8_t* __restrict__ aq, const float* __restrict__ ad,
@@ -106,7 +106,6 @@ q8_matvec_kernel(const int8_t* __restrict__ wq, const __half* __restrict__ wd, i
     int rows[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) rows[g] = min(row0 + r + RW * g, N - 1);
-    if (PF && threadIdx.x == 0) prefetch_l2(wq + (size_t)row0 * K, (uint32_t)(min(RC, N - row0) * K));
     float acc[G][T];
     q8_chains<T, KL, G, BIAS>(wq, wd, K, rows, c, aq, ad, acc);
 #pragma unroll
@@ -125,13 +124,13 @@ q8_matvec_kernel(const int8_t* __restrict__ wq, const __half* __restrict__ wd, i
     }
 }
 
-template <int T, int KL, int G, bool PF, bool BIAS>
+template <int T, int KL, int G, bool BIAS>
 static cudaError_t launch_t(const int8_t* wq, const __half* wd, int N, int K, const int8_t* aq,
                             const float* ad, float* y, int64_t ldy, const float* resid, int64_t ldr,
                             cudaStream_t s)
 {
     constexpr int RC = (32 / KL) * G;
-    const cudaError_t e = launch_pdl(q8_matvec_kernel<T, KL, G, PF, BIAS>, dim3((N + RC - 1) / RC),
+    const cudaError_t e = launch_pdl(q8_matvec_kernel<T, KL, G, BIAS>, dim3((N + RC - 1) / RC),
                                      dim3(32 * (32 / KL)), s, wq, wd, N, K, aq, ad, y, ldy, resid, ldr);
     count_launches(1);
     return e;
@@ -144,32 +143,32 @@ cudaError_t launch_matvec(const int8_t* wq, const __half* wd, int N, int K, cons
     // 1..8 and 13..16 rows with K a multiple of 256 and 16-byte aligned
     // operands: the weights stream through the TMA ring (matvec_tma.cu);
     // otherwise the register-pipelined kernel below.  KL (lanes per row), G
-    // (rows per lane), the L2 prefetch and the form of the int-to-float step
-    // (conversion, or the exact biased chain) only shape the pipeline; none of
-    // them, and neither kernel choice, changes any row's arithmetic.
+    // (rows per lane) and the form of the int-to-float step (conversion, or
+    // the exact biased chain) only shape the pipeline; none of them, and
+    // neither kernel choice, changes any row's arithmetic.
     {
         const cudaError_t e = launch_matvec_tma(wq, wd, N, K, aq, ad, T, y, ldy, resid, ldr, s);
         if (e != cudaErrorNotSupported) return e;
     }
     switch (T) {
-#define LUCE_MV(TT, KK, GG, PP, BB) \
-    case TT: return launch_t<TT, KK, GG, PP, BB>(wq, wd, N, K, aq, ad, y, ldy, resid, ldr, s);
-        LUCE_MV(1, 8, 1, false, true)
-        LUCE_MV(2, 8, 2, false, false)
-        LUCE_MV(3, 8, 3, false, false)
-        LUCE_MV(4, 8, 4, false, false)
-        LUCE_MV(5, 8, 4, false, true)
-        LUCE_MV(6, 8, 4, false, true)
-        LUCE_MV(7, 8, 4, false, true)
-        LUCE_MV(8, 8, 4, false, true)
-        LUCE_MV(9, 8, 2, false, false)
-        LUCE_MV(10, 8, 2, false, false)
-        LUCE_MV(11, 8, 2, false, false)
-        LUCE_MV(12, 8, 3, false, false)
-        LUCE_MV(13, 8, 2, false, false)
-        LUCE_MV(14, 8, 2, false, false)
-        LUCE_MV(15, 8, 2, false, false)
-        LUCE_MV(16, 8, 2, false, false)
+#define LUCE_MV(TT, KK, GG, BB) \
+    case TT: return launch_t<TT, KK, GG, BB>(wq, wd, N, K, aq, ad, y, ldy, resid, ldr, s);
+        LUCE_MV(1, 8, 1, true)
+        LUCE_MV(2, 8, 2, false)
+        LUCE_MV(3, 8, 3, false)
+        LUCE_MV(4, 8, 4, false)
+        LUCE_MV(5, 8, 4, true)
+        LUCE_MV(6, 8, 4, true)
+        LUCE_MV(7, 8, 4, true)
+        LUCE_MV(8, 8, 4, true)
+        LUCE_MV(9, 8, 2, false)
+        LUCE_MV(10, 8, 2, false)
+        LUCE_MV(11, 8, 2, false)
+        LUCE_MV(12, 8, 3, false)
+        LUCE_MV(13, 8, 2, false)
+        LUCE_MV(14, 8, 2, false)
+        LUCE_MV(15, 8, 2, false)
+        LUCE_MV(16, 8, 2, false)
 #undef LUCE_MV
         default: return cudaErrorInvalidValue;
     }

@@ -39,6 +39,7 @@
 
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -536,24 +537,40 @@ bool encode_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ba
     return true;
 }
 
-int sm_count()
+// Per-device host state: the SM count and which kernels have had their
+// dynamic shared-memory limit raised (a function attribute set per device).
+constexpr int kMaxDevices = 64;
+
+int current_device()
 {
-    static int counts[64];
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (counts[dev] == 0) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        counts[dev] = n;
-    }
-    return counts[dev];
+    return (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices) ? dev : -1;
 }
 
-template <typename Kern>
-cudaError_t set_smem_once(Kern kernel, int bytes, std::once_flag& once, cudaError_t& status)
+int sm_count()
 {
-    std::call_once(once, [&] { status = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes); });
-    return status;
+    static std::atomic<int> counts[kMaxDevices];
+    const int dev = current_device();
+    if (dev < 0) return 0;
+    int n = counts[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        counts[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
+// Raises `kernel`'s dynamic shared-memory limit to `bytes` once per device;
+// `done` is the kernel's own per-device flag table.
+template <typename Kern>
+cudaError_t set_smem_once(Kern kernel, int bytes, std::atomic<bool> (&done)[kMaxDevices])
+{
+    const int dev = current_device();
+    if (dev < 0) return cudaErrorInvalidDevice;
+    if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done[dev].store(true, std::memory_order_release);
+    return e;
 }
 
 template <int T, int G, int S, bool BIAS>
@@ -562,9 +579,9 @@ cudaError_t launch_tma_t(const CUtensorMap& mw, const CUtensorMap& md, const CUt
                          cudaStream_t s)
 {
     using L = RingLayout<T, G, S>;
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    if (set_smem_once(q8_matvec_tma_kernel<T, G, S, BIAS>, L::SMEM, once, attr) != cudaSuccess) return attr;
+    static std::atomic<bool> done[kMaxDevices];
+    const cudaError_t attr = set_smem_once(q8_matvec_tma_kernel<T, G, S, BIAS>, L::SMEM, done);
+    if (attr != cudaSuccess) return attr;
     const int nq = (N + 3) / 4;
     const int grid = min(ctas, (nq + G - 1) / G);
     const cudaError_t e = launch_pdl_smem(q8_matvec_tma_kernel<T, G, S, BIAS>, dim3(grid), dim3(kRingThreads), L::SMEM,
@@ -579,9 +596,9 @@ cudaError_t launch_qkv_tma_t(const CUtensorMap& mw, const CUtensorMap& mdp, cons
                              const RopeFreq& f, float* q_rot, const KvRows& kv, cudaStream_t s)
 {
     using L = RingLayout<T, G, S>;
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    if (set_smem_once(q8_qkv_rope_tma_kernel<T, G, S, BIAS>, L::SMEM, once, attr) != cudaSuccess) return attr;
+    static std::atomic<bool> done[kMaxDevices];
+    const cudaError_t attr = set_smem_once(q8_qkv_rope_tma_kernel<T, G, S, BIAS>, L::SMEM, done);
+    if (attr != cudaSuccess) return attr;
     const int groups = (Hq + 2 * Hkv) * ((kHeadDim / 2) / (2 * G));
     const cudaError_t e = launch_pdl_smem(q8_qkv_rope_tma_kernel<T, G, S, BIAS>, dim3(groups), dim3(kRingThreads),
                                           L::SMEM, s, mw, mdp, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv);
