@@ -17,7 +17,7 @@ Pages followed (cited by title and section):
     multi-sequence decode attention, pos-vector RoPE, logits one row per
     sequence).
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent:
   q8_0 weights stored as int8 [N][K] + binary16 scales [N][K/32]; activation
   scale stored in fp32, d = amax/127, q = round-half-away(x/d); RoPE pairs
   (i, i + D/2) at angle pos * theta^(-2i/D); GQA head h -> h // (Hq/Hkv);
