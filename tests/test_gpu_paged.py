@@ -84,14 +84,15 @@ def test_paged_attention_equals_flat_bitwise(lens, nq, Hq, Hkv):
 LAYER_FIELDS = ["attn_norm", "wqkv_q", "wqkv_d", "wo_q", "wo_d", "ffn_norm", "wgu_q", "wgu_d", "wdown_q", "wdown_d"]
 
 
-def test_paged_step_equals_flat_step_bitwise():
+@pytest.mark.parametrize("rws", [[1, 2, 3, 4], [2, 2, 2, 2], [4, 4, 4, 4]])  # 10, 8 and 16 rows
+def test_paged_step_equals_flat_step_bitwise(rws):
     D, NL, VOCAB = wl.TINY_LAYER, 2, 250
     layers = [luce.LayerTensors(*[cuda(getattr(wl.layer_host(31, l, D), f)) for f in LAYER_FIELDS])
               for l in range(NL)]
     fn, hq, hd = wl.head_host(31, D, VOCAB)
     model = luce.Model(layers, D.hidden, D.n_q_heads, D.n_kv_heads, D.ffn, rms_eps=D.rms_eps,
                        rope_theta=D.rope_theta, final_norm=cuda(fn), head_q=cuda(hq), head_d=cuda(hd))
-    lens, rws = [5, 127, 128, 300], [1, 2, 3, 4]   # row 1 and 2 cross or start a page
+    lens = [5, 127, 128, 300]   # rows of slots 1 and 2 cross or start a page
     cap = 512
     spans = [-(-(L + n) // PK) for L, n in zip(lens, rws)]
     tables, n_pages = page_tables(7, spans)
