@@ -14,8 +14,8 @@
 // range of 4-row quads of W.  A CTA walks its rows in groups of G quads (4G
 // rows; G = 4 up to 4 activation rows, 2 for 5..8).  A stage is one kilobyte
 // of K of a group: block c of stage j is block 32j + c, one block for each of
-// the 32 chains.  One producer thread keeps a ring of S stages in flight (2 up
-// to 4 rows, 3 for 5..8) with tensor copies (W viewed as [N][K/256][256], one
+// the 32 chains.  One producer thread keeps a ring of three stages in flight
+// with tensor copies (W viewed as [N][K/256][256], one
 // 4-row x 1 KB box per quad; the group's scales, the activation rows' 32
 // blocks and their scales as one box each), the arrival of a slot signalled on
 // an mbarrier by the copies' byte count.  Four consumer warps read the slot
@@ -54,6 +54,7 @@ namespace {
 constexpr int kRingCtasPerSm = 3;      // 1..4 rows
 constexpr int kRingCtasPerSmWide = 3;  // 5..8 rows (larger activation boxes)
 constexpr int kRingSlotsWide = 3;
+constexpr int kRingSlotsNarrow = 3;    // 1..4 rows
 constexpr int kRingThreads = 160;  // 4 consumer warps + 1 producer warp
 
 // Shape of a ring: T activation rows, G rows per lane (a group is G quads,
@@ -66,7 +67,11 @@ struct RingLayout {
     static constexpr int A = T * 1024;          // [T][1024 B]
     static constexpr int AD = T * 128;          // [T][32 fp32 scales]
     static constexpr int STAGE = W + D + A + AD;  // a multiple of 128
-    static constexpr int PART = 2 * ROWS * T * 33 * 4;
+    // chain buffers: two (one barrier per group) unless three CTAs per SM
+    // would then not fit in the SM's 228 KB, then one (two barriers per group)
+    static constexpr int PART1 = ROWS * T * 33 * 4;
+    static constexpr int PB = 3 * (128 + S * STAGE + 2 * PART1 + 2 * S * 8 + 1024) <= 233472 ? 2 : 1;
+    static constexpr int PART = PB * PART1;
     static constexpr int SMEM = 128 + S * STAGE + PART + 2 * S * 8;
 };
 
@@ -363,7 +368,8 @@ q8_matvec_tma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_consta
         float acc[G][T];
         ring_chains<T, G, S, BIAS>(R, it, nj, nb, r, c, lane, acc, ok);
         // two chain buffers, so one barrier per group separates writers and readers
-        float* pp = R.part + (gi & 1) * (L::ROWS * T * 33);
+        float* pp = R.part + (L::PB == 2 ? (gi & 1) * (L::ROWS * T * 33) : 0);
+        if (L::PB == 1 && gi > 0) asm volatile("bar.sync 1, 128;" ::: "memory");  // last group's readers are done
         store_chains<T, G>(pp, r, c, acc);
         asm volatile("bar.sync 1, 128;" ::: "memory");
         for (int idx = tid; idx < L::ROWS * T; idx += 128) {
@@ -630,9 +636,9 @@ bool ring_maps(const int8_t* wq, const __half* wd, int N, int K, const int8_t* a
 
 }  // namespace
 
-// One ring launch of T <= 8 rows: groups of 16 rows over two slots up to 4
-// rows, groups of 8 rows over three slots for 5..8 (shared memory for the
-// larger activation boxes).
+// One ring launch of T <= 8 rows, three slots: groups of 16 rows up to 4
+// rows, groups of 8 rows for 5..8 (shared memory for the larger activation
+// boxes).
 static cudaError_t launch_ring_rows(const int8_t* wq, const __half* wd, int N, int K, const int8_t* aq,
                                     const float* ad, int T, float* y, int64_t ldy, const float* resid, int64_t ldr,
                                     int sms, cudaStream_t s)
@@ -640,12 +646,12 @@ static cudaError_t launch_ring_rows(const int8_t* wq, const __half* wd, int N, i
     CUtensorMap mw, md, ma, mad;
     if (!ring_maps(wq, wd, N, K, aq, ad, T, T <= 4 ? 16 : 8, &mw, &md, &ma, &mad)) return cudaErrorNotSupported;
     const int narrow = kRingCtasPerSm * sms, wide = kRingCtasPerSmWide * sms;
-    constexpr int SW = kRingSlotsWide;
+    constexpr int SW = kRingSlotsWide, SN = kRingSlotsNarrow;
     switch (T) {
-        case 1: return launch_tma_t<1, 4, 2, true>(mw, md, ma, mad, N, K, y, ldy, resid, ldr, narrow, s);
-        case 2: return launch_tma_t<2, 4, 2, false>(mw, md, ma, mad, N, K, y, ldy, resid, ldr, narrow, s);
-        case 3: return launch_tma_t<3, 4, 2, false>(mw, md, ma, mad, N, K, y, ldy, resid, ldr, narrow, s);
-        case 4: return launch_tma_t<4, 4, 2, false>(mw, md, ma, mad, N, K, y, ldy, resid, ldr, narrow, s);
+        case 1: return launch_tma_t<1, 4, SN, true>(mw, md, ma, mad, N, K, y, ldy, resid, ldr, narrow, s);
+        case 2: return launch_tma_t<2, 4, SN, false>(mw, md, ma, mad, N, K, y, ldy, resid, ldr, narrow, s);
+        case 3: return launch_tma_t<3, 4, SN, false>(mw, md, ma, mad, N, K, y, ldy, resid, ldr, narrow, s);
+        case 4: return launch_tma_t<4, 4, SN, false>(mw, md, ma, mad, N, K, y, ldy, resid, ldr, narrow, s);
         case 5: return launch_tma_t<5, 2, SW, false>(mw, md, ma, mad, N, K, y, ldy, resid, ldr, wide, s);
         case 6: return launch_tma_t<6, 2, SW, false>(mw, md, ma, mad, N, K, y, ldy, resid, ldr, wide, s);
         case 7: return launch_tma_t<7, 2, SW, false>(mw, md, ma, mad, N, K, y, ldy, resid, ldr, wide, s);
@@ -672,8 +678,8 @@ cudaError_t launch_matvec_tma(const int8_t* wq, const __half* wd, int N, int K, 
                             resid ? resid + 8 * ldr : nullptr, ldr, sms, s);
 }
 
-// One fused launch of T <= 8 rows: 8 rotation pairs per group over two slots
-// up to 4 rows, 4 pairs over three slots for 5..8.
+// One fused launch of T <= 8 rows, three slots: 8 rotation pairs per group up
+// to 4 rows, 4 pairs for 5..8.
 static cudaError_t qkv_ring_rows(const int8_t* wq, const __half* wd, int K, const int8_t* aq, const float* ad, int T,
                                  float* qkv, int Hq, int Hkv, const RowPos& pos, const RopeFreq& f, float* q_rot,
                                  const KvRows& kv, cudaStream_t s)
@@ -681,12 +687,12 @@ static cudaError_t qkv_ring_rows(const int8_t* wq, const __half* wd, int K, cons
     const int N = (Hq + 2 * Hkv) * kHeadDim;
     CUtensorMap mw, mdp, ma, mad;
     if (!ring_maps(wq, wd, N, K, aq, ad, T, T <= 4 ? 8 : 4, &mw, &mdp, &ma, &mad)) return cudaErrorNotSupported;
-    constexpr int SW = kRingSlotsWide;
+    constexpr int SW = kRingSlotsWide, SN = kRingSlotsNarrow;
     switch (T) {
-        case 1: return launch_qkv_tma_t<1, 4, 2, true>(mw, mdp, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
-        case 2: return launch_qkv_tma_t<2, 4, 2, false>(mw, mdp, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
-        case 3: return launch_qkv_tma_t<3, 4, 2, false>(mw, mdp, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
-        case 4: return launch_qkv_tma_t<4, 4, 2, false>(mw, mdp, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
+        case 1: return launch_qkv_tma_t<1, 4, SN, true>(mw, mdp, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
+        case 2: return launch_qkv_tma_t<2, 4, SN, false>(mw, mdp, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
+        case 3: return launch_qkv_tma_t<3, 4, SN, false>(mw, mdp, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
+        case 4: return launch_qkv_tma_t<4, 4, SN, false>(mw, mdp, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
         case 5: return launch_qkv_tma_t<5, 2, SW, false>(mw, mdp, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
         case 6: return launch_qkv_tma_t<6, 2, SW, false>(mw, mdp, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
         case 7: return launch_qkv_tma_t<7, 2, SW, false>(mw, mdp, ma, mad, K, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
