@@ -221,3 +221,12 @@ def test_decode_attn_paged_refusals(lib):
     assert f(P, pv([(10, 1, 0)]), 1, 8, 2, 64, 0.1, P, P, ws, None) == luce.LUCE_EUNSUPPORTED
     assert f(P, pv([(10, 1, 0)]), 1, 8, 2, 128, 0.1, P, P, 16, None) == luce.LUCE_ENOSPACE
     assert f(P, pv([(200000, 1, 0)]), 1, 8, 2, 128, 0.1, P, P, ws, None) == luce.LUCE_EUNSUPPORTED
+
+
+def test_wait_counter_and_expiry_hook_refusals(lib):
+    """The timeout counter needs somewhere to write; the expiry hook takes a
+    limit between 1 us and 1 s.  Both refuse before touching the device."""
+    assert lib.luce_wait_timeouts(None, 0) == luce.LUCE_EINVAL
+    assert "null count" in status_msg(lib)
+    for bad in (0, 999, 1_000_000_001, -5):
+        assert lib.luce_test_wait_expiry(bad, None) == luce.LUCE_EINVAL
