@@ -69,9 +69,10 @@ def test_quantize_bit_exact(T, K):
 
 # K % 256 == 0 with T <= 4 runs the TMA-ring kernel: (37, 1280) has a partial
 # last kilobyte stage and a partial quad of rows, (100, 256) a K shorter than
-# one stage, (2049, 768) stages of 24 blocks over many CTAs
+# one stage, (2049, 768) stages of 24 blocks over many CTAs, (1, 512) and
+# (5, 256) a single group mostly past the end of W
 MV_SHAPES = [(1024, 1024), (1000, 1056), (33, 96), (7, 32), (301, 5120), (64, 17408), (37, 1280), (100, 256),
-             (2049, 768)]
+             (2049, 768), (1, 512), (5, 256)]
 
 
 def mv_inputs(N, K, T, seed=0):
