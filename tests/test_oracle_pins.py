@@ -389,6 +389,112 @@ def test_layer_verify_rows_are_causal():
     assert all(not np.array_equal(y[j], y3[j]) for j in range(4))
 
 
+# ----------------------------------------------------------- hand compositions (numpy, float64)
+#
+# The layer and the head written out again from their definitions with numpy
+# only (the quantizer, pinned above, is the one oracle routine they call):
+# RMSNorm x / sqrt(mean(x^2) + eps) * gamma; every projection is the q8_0
+# activation quantization of its fp32 input followed by the dequantized
+# float64 product; silu(g) * u with the gate half first.
+
+
+def np_rmsnorm(x, gamma, eps):
+    x = np.asarray(x, np.float64)
+    return x / np.sqrt(np.mean(x * x, axis=1, keepdims=True) + eps) * gamma.astype(np.float64)
+
+
+def np_q8_project(x32, wq, wd):
+    """q8_0 activations of fp32 rows x32 times q8_0 weights, dequantized, float64."""
+    aq, ad = oracle.quantize_act(x32)
+    a = aq.astype(np.float64) * np.repeat(ad.astype(np.float64), 32, axis=1)
+    w = wq.astype(np.float64) * np.repeat(wd.astype(np.float64), 32, axis=1)
+    return a @ w.T
+
+
+def np_ffn(x1, lw, eps):
+    xn2 = np_rmsnorm(x1, lw.ffn_norm, eps).astype(np.float32)
+    gu = np_q8_project(xn2, lw.wgu_q, lw.wgu_d)
+    F = gu.shape[1] // 2
+    g, u = gu[:, :F], gu[:, F:]
+    h = (g / (1.0 + np.exp(-g)) * u).astype(np.float32)
+    return x1 + np_q8_project(h, lw.wdown_q, lw.wdown_d)
+
+
+def np_first_token_layer(x, lw, dims):
+    """decode_layer for rows that are each the first token of their slot: a
+    row's only key is its own, so attention returns its own f16-rounded v."""
+    H, Hq, Hkv, D = dims.hidden, dims.n_q_heads, dims.n_kv_heads, dims.head_dim
+    xn = np_rmsnorm(x, lw.attn_norm, dims.rms_eps).astype(np.float32)
+    qkv = np_q8_project(xn, lw.wqkv_q, lw.wqkv_d)
+    v = qkv[:, (Hq + Hkv) * D:].reshape(-1, Hkv, D).astype(np.float16).astype(np.float64)
+    attn = np.repeat(v, Hq // Hkv, axis=1).reshape(-1, Hq * D).astype(np.float32)
+    x1 = np.asarray(x, np.float64) + np_q8_project(attn, lw.wo_q, lw.wo_d)
+    return np_ffn(x1, lw, dims.rms_eps)
+
+
+def rel(a, b):
+    return float(np.max(np.abs(a - b) / np.maximum(np.linalg.norm(b, axis=1, keepdims=True), 1e-300)))
+
+
+def test_lm_head_matches_numpy_norm_quantize_and_dequantized_product():
+    r = np.random.default_rng(11)
+    H, V = 256, 300
+    x = r.normal(0, 1, (3, H))
+    x[1] *= 1e-3        # mean(x^2) ~ 1e-6: the eps term matters here
+    x[2] *= 40.0
+    gamma = r.normal(1, 0.3, H).astype(np.float32)
+    wq, wd = rand_w(V, H)
+    got = oracle.lm_head(x, gamma, wq, wd, 1e-6)
+    want = np_q8_project(np_rmsnorm(x, gamma, 1e-6).astype(np.float32), wq, wd)
+    assert got.shape == (3, V)
+    assert rel(got, want) <= 1e-12
+    # a different eps changes the small row's logits beyond round-off
+    other = np_q8_project(np_rmsnorm(x, gamma, 1e-5).astype(np.float32), wq, wd)
+    assert rel(got[1:2], other[1:2]) > 1e-3
+
+
+def test_lm_head_scales_with_the_final_norm_and_vanishes_with_zero_weight_scales():
+    r = np.random.default_rng(12)
+    H, V = 128, 64
+    x = r.normal(0, 1, (2, H))
+    gamma = r.normal(1, 0.2, H).astype(np.float32)
+    wq, wd = rand_w(V, H)
+    base = oracle.lm_head(x, gamma, wq, wd, 1e-6)
+    # a power-of-two scale of gamma passes exactly through the fp32 cast, the
+    # quantizer (codes unchanged, scales doubled) and the product
+    assert np.array_equal(oracle.lm_head(x, gamma * np.float32(2), wq, wd, 1e-6), 2 * base)
+    # any other constant c scales the logits by c up to the quantization step
+    assert rel(oracle.lm_head(x, gamma * np.float32(3), wq, wd, 1e-6), 3 * base) < 2e-2
+    assert np.all(oracle.lm_head(x, gamma, wq, np.zeros_like(wd), 1e-6) == 0)
+
+
+def test_layer_ffn_branch_uses_ffn_norm_on_its_own_input():
+    # Wo silenced (x1 = x) with attn_norm and ffn_norm far apart: the output
+    # is x plus the FFN branch normalised by ffn_norm
+    lw, dims = tiny_layer(seed=21)
+    lw.attn_norm[:] = np.random.default_rng(1).normal(3, 1, dims.hidden).astype(np.float32)
+    lw.wo_d[:] = 0
+    r = np.random.default_rng(22)
+    x = r.normal(0, 1, (2, dims.hidden)).astype(np.float32)
+    got = oracle.decode_layer(x, lw, dims, [make_slot(r, dims, 4), make_slot(r, dims, 0)], [1, 1])
+    want = np_ffn(x.astype(np.float64), lw, dims.rms_eps)
+    assert rel(got, want) <= 1e-9
+
+
+def test_layer_matches_hand_composition_for_first_tokens():
+    # Wo live: the FFN must normalise x1 = x + Wo . attn, not x; each row is
+    # the first token of its slot, so its attention is its own value row
+    lw, dims = tiny_layer(seed=23)
+    lw.wo_d[:] = lw.wo_d * np.float16(32)                  # a branch of the size of x
+    r = np.random.default_rng(24)
+    x = r.normal(0, 1, (3, dims.hidden)).astype(np.float32)
+    slots = [make_slot(r, dims, 0) for _ in range(3)]
+    tr = {}
+    got = oracle.decode_layer(x, lw, dims, slots, [1, 1, 1], trace=tr)
+    assert rel(tr["x1"], x.astype(np.float64)) > 1e-1      # the attention branch is not negligible
+    assert rel(got, np_first_token_layer(x, lw, dims)) <= 1e-9
+
+
 def test_page_limits_fixture_is_consistent():
     lim = json.load(open(os.path.join(HERE, "golden", "page_limits.json")))
     assert lim["max_concurrent_slots"]["value"] * 4 == max(lim["verify_row_capacities"]["value"])
