@@ -70,7 +70,7 @@ def test_noalloc_matches_workspace_entry_point_twice(lib):
 
 def test_noalloc_refuses_work_beyond_its_scratch(lib):
     Hq, Hkv, L = 64, 8, 32768
-    need = 256 * math.ceil(64 * Hq / 256) + 4 * math.ceil(L / 256) * Hq * 528
+    need = 4 * math.ceil(L / 256) * Hq * 528  # 4 rows of 256-key chunks, 528 bytes per chunk and head
     assert need > lib.luce_decode_attn_noalloc_max_bytes()
     kv = torch.zeros((Hkv, L, 128), dtype=torch.float16, device="cuda")
     views = [luce.SeqView(kv, kv, L, 1, s) for s in range(4)]
