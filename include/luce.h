@@ -69,12 +69,24 @@ int luce_version(void);
 uint64_t luce_launch_count(void);
 
 /*
- * Bounded waits that expired on the current device.  The TMA-ring matvec
- * (1..4 rows, K a multiple of 256) waits on shared-memory barriers for its
- * weight copies; every such wait gives up after about one second, adds one to
- * this device counter and leaves the outputs of the rows still pending
- * unwritten, so a stalled copy engine surfaces as an error here instead of a
- * hung stream.  A healthy run reads 0.
+ * Bounded waits that expired on the current device.  The kernels that stream
+ * weights through a ring of shared-memory stages filled by tensor copies (the
+ * dp4a ring matvec, which luce_q8_matvec_batch takes at 1..4 rows; the
+ * tensor-core ring matvec, at 5..16 rows; the fused q|k|v + RoPE + K/V-append
+ * projection of the decode step on either ring) wait on shared-memory
+ * barriers for those copies.  Every such
+ * wait gives up after about one second and adds one to this device counter,
+ * so a stalled copy engine surfaces here instead of as a hung stream.  A
+ * healthy run reads 0.
+ *
+ * A non-zero count means the device context is suspect, not that some
+ * outputs were merely skipped: the CTA whose wait expired stops writing and
+ * may exit while tensor copies it issued are still in flight, and such a
+ * copy can land in shared memory that later belongs to another CTA.  Treat
+ * every result computed since the last zero reading as untrusted and
+ * recreate the context.  The decode step entry points return LUCE_OK
+ * without looking at this counter (reading it synchronises the device):
+ * callers that need the guarantee poll it after their steps.
  *   count (host) receives the counter; reset != 0 clears it afterwards.
  * Synchronises the device (it copies from device memory).  Returns LUCE_OK,
  * LUCE_EINVAL (null count) or LUCE_ECUDA.
@@ -124,9 +136,35 @@ int luce_q8_matvec_batch(const int8_t* wq, const uint16_t* wd, int N, int K,
                          const int8_t* aq, const float* ad, int T, float* y, int64_t ldy, void* stream);
 
 /*
+ * luce_q8_matvec_batch through one named kernel (a diagnostic for tests and
+ * benchmarks).  Every kernel computes the same chains and butterfly, so all
+ * give the same bits:
+ *   LUCE_MATVEC_AUTO      the library's choice (luce_q8_matvec_batch);
+ *   LUCE_MATVEC_REGISTER  register-pipelined dp4a loads (any shape);
+ *   LUCE_MATVEC_RING      dp4a on a TMA ring in shared memory (1..8 rows in
+ *                         one launch, 13..16 in two; K % 256 == 0, 16-byte
+ *                         aligned operands);
+ *   LUCE_MATVEC_TENSOR    block dots on the tensor cores from a TMA ring
+ *                         (1..16 rows in one launch; K % 256 == 0, 16-byte
+ *                         aligned operands).
+ * Arguments and errors as luce_q8_matvec_batch, plus LUCE_EUNSUPPORTED
+ * (nothing launched) when the named kernel does not serve the shape.
+ */
+#define LUCE_MATVEC_AUTO 0
+#define LUCE_MATVEC_REGISTER 1
+#define LUCE_MATVEC_RING 2
+#define LUCE_MATVEC_TENSOR 3
+int luce_q8_matvec_batch_path(const int8_t* wq, const uint16_t* wd, int N, int K, const int8_t* aq, const float* ad,
+                              int T, float* y, int64_t ldy, int path, void* stream);
+
+/*
  * Per-block integer dots out[t][n][b] = sum_i wq[n][32b+i] * aq[t][32b+i],
- * computed by the matvec kernel's own dot routine (exposed so the exactness
- * of the integer stage can be checked).  out (device) int32 [T][N][K/32].
+ * computed with the register-pipelined matvec kernel's dp4a routine (exposed
+ * so the exactness of the integer stage can be checked against the oracle).
+ * The other matvec kernels form the same integers differently (a biased dp4a
+ * chain, or f16 tensor-core products); that they agree is checked through
+ * their outputs, which equal the register kernel's bit for bit.
+ * out (device) int32 [T][N][K/32].
  */
 int luce_q8_block_dots(const int8_t* wq, int N, int K, const int8_t* aq, int T, int32_t* out, void* stream);
 
@@ -242,13 +280,13 @@ int luce_decode_attn_paged(const float* q, const luce_pagedview* views, int n_se
  * The scratch is one fixed array of luce_decode_attn_noalloc_max_bytes()
  * bytes (16 MiB) in the library's device memory; every GPU that loads the
  * library holds it until the process exits.  The call needs
- * roundup256(64 * Hq) + (sum over rows of its chunk count) * Hq * 528 bytes
- * of it (chunks as in luce_decode_attn_multiseq) and returns LUCE_ENOSPACE,
- * launching nothing, when that exceeds the array (at Hq = 40: 4 rows of up
- * to 32,768 keys, or 16 rows of up to 2,051 keys, fit).  It allocates nothing:
- * no cudaMalloc, cudaFree or allocating library routine.  It clears the
- * part of the array that must start at zero (with cudaMemsetAsync on
- * `stream`) on every call.
+ * (sum over rows of its chunk count) * Hq * 528 bytes of it (chunks as in
+ * luce_decode_attn_multiseq) and returns LUCE_ENOSPACE, launching nothing,
+ * when that exceeds the array (at Hq = 40: 4 rows of up to 32,768 keys, or
+ * 16 rows of up to 2,051 keys, fit).  It allocates nothing: no cudaMalloc,
+ * cudaFree or allocating library routine.  Nothing in the array needs to
+ * start at zero: every chunk writes its partials before the merge reads
+ * them, so the call clears nothing.
  *
  * The first call on each device (the calling thread's current device) looks
  * up the array's device address with cudaGetSymbolAddress; make that first

@@ -81,7 +81,7 @@ EXPORTS = ("luce_last_error", "luce_version", "luce_launch_count", "luce_q8_quan
            "luce_decode_attn_workspace_size", "luce_decode_step_layout", "luce_decode_step",
            "luce_decode_attn_multiseq_noalloc", "luce_decode_attn_noalloc_max_bytes", "luce_decode_attn_paged",
            "luce_decode_step_paged", "luce_wait_timeouts", "luce_decode_step_host",
-           "luce_test_wait_expiry")
+           "luce_test_wait_expiry", "luce_q8_matvec_batch_path")
 
 _lib = None
 
@@ -103,6 +103,7 @@ def load_library(path: str = LIB_PATH):
     lib.luce_launch_count.argtypes = []
     lib.luce_q8_quantize_act.argtypes = [vp, i32, i32, i64, vp, vp, vp]
     lib.luce_q8_matvec_batch.argtypes = [vp, vp, i32, i32, vp, vp, i32, vp, i64, vp]
+    lib.luce_q8_matvec_batch_path.argtypes = [vp, vp, i32, i32, vp, vp, i32, vp, i64, i32, vp]
     lib.luce_q8_block_dots.argtypes = [vp, i32, i32, vp, i32, vp, vp]
     lib.luce_rope_posvec.argtypes = [vp, i32, i32, i32, i64, vp, f64, vp]
     lib.luce_kv_append.argtypes = [vp, vp, i64, i32, i32, ctypes.POINTER(SeqViewC), i32, vp]
@@ -191,6 +192,24 @@ def luce_q8_matvec_batch(wq, wd, aq, ad, y=None, stream=None):
     y = torch.empty((T, N), dtype=torch.float32, device=wq.device) if y is None else y
     _check(load_library().luce_q8_matvec_batch(wq.data_ptr(), wd.data_ptr(), N, K, aq.data_ptr(), ad.data_ptr(),
                                                T, y.data_ptr(), y.stride(0), _stream(stream)))
+    return y
+
+
+MATVEC_AUTO, MATVEC_REGISTER, MATVEC_RING, MATVEC_TENSOR = 0, 1, 2, 3
+
+
+def luce_q8_matvec_batch_path(wq, wd, aq, ad, path: int, y=None, stream=None):
+    """luce_q8_matvec_batch through one named kernel (MATVEC_*); raises LuceError
+    (LUCE_EUNSUPPORTED) when that kernel does not serve the shape."""
+    import torch
+    _need(wq, torch.int8, "wq")
+    _need(aq, torch.int8, "aq")
+    _need(ad, torch.float32, "ad")
+    N, K = wq.shape
+    T = aq.shape[0]
+    y = torch.empty((T, N), dtype=torch.float32, device=wq.device) if y is None else y
+    _check(load_library().luce_q8_matvec_batch_path(wq.data_ptr(), wd.data_ptr(), N, K, aq.data_ptr(), ad.data_ptr(),
+                                                    T, y.data_ptr(), y.stride(0), int(path), _stream(stream)))
     return y
 
 

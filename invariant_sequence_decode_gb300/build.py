@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libluce.so")
 HEADER = os.path.join(ROOT, "include", "luce.h")
-SOURCES = ["api.cu", "matvec.cu", "matvec_tma.cu", "attn.cu", "rope_kv.cu", "elementwise.cu"]
+SOURCES = ["api.cu", "matvec.cu", "matvec_tma.cu", "matvec_mma.cu", "attn.cu", "rope_kv.cu", "elementwise.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-fmad=false", "-Xcompiler", "-fPIC,-O2",
               "--expt-relaxed-constexpr"] + ARCH

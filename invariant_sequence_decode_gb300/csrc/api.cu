@@ -139,6 +139,20 @@ int luce_q8_matvec_batch(const int8_t* wq, const uint16_t* wd, int N, int K, con
                        "q8_matvec_batch");
 }
 
+int luce_q8_matvec_batch_path(const int8_t* wq, const uint16_t* wd, int N, int K, const int8_t* aq, const float* ad,
+                              int T, float* y, int64_t ldy, int path, void* stream)
+{
+    int rc = check_matvec(wq, wd, N, K, aq, ad, T, y, ldy, "q8_matvec_batch_path");
+    if (rc) return rc;
+    REQUIRE(path >= LUCE_MATVEC_AUTO && path <= LUCE_MATVEC_TENSOR, LUCE_EINVAL, "q8_matvec_batch_path: path=%d",
+            path);
+    const cudaError_t e = launch_matvec_path(path, wq, reinterpret_cast<const __half*>(wd), N, K, aq, ad, T, y, ldy,
+                                             nullptr, 0, (cudaStream_t)stream);
+    REQUIRE(e != cudaErrorNotSupported, LUCE_EUNSUPPORTED,
+            "q8_matvec_batch_path: kernel %d does not serve T=%d, K=%d at these alignments", path, T, K);
+    return cuda_status(e, "q8_matvec_batch_path");
+}
+
 int luce_q8_block_dots(const int8_t* wq, int N, int K, const int8_t* aq, int T, int32_t* out, void* stream)
 {
     REQUIRE(wq && aq && out, LUCE_EINVAL, "q8_block_dots: null pointer");
@@ -660,12 +674,28 @@ static int flat_slots(const luce_model* m, const luce_slot* slots, const int32_t
                 "%s: slot %d len=%d + rows=%d exceeds cap=%d", who, s, sl.len, n, sl.cap);
         REQUIRE(sl.len + n <= kMaxKeys, LUCE_EUNSUPPORTED, "%s: slot %d would hold %d keys (at most %d)", who, s,
                 sl.len + n, kMaxKeys);
-        for (int p = 0; p < s; ++p)
-            REQUIRE(slots[p].k != sl.k && slots[p].v != sl.v, LUCE_EINVAL, "%s: slots %d and %d share a cache", who,
-                    p, s);
         ss[s] = StepSlot{reinterpret_cast<__half*>(sl.k), reinterpret_cast<__half*>(sl.v), sl.len, sl.cap, nullptr,
                          nullptr};
     }
+    // Every K and V cache of the call is a byte range [base, base + extent)
+    // with extent = n_layers * Hkv * cap * D binary16 values; no two of them
+    // (two slots, or one slot's K and V) may overlap, or one slot's appends
+    // would land in another's keys and break the untouched-slot guarantee.
+    struct Range {
+        uintptr_t lo, hi;
+        int slot;
+        char which;
+    } r[2 * LUCE_MAX_SEQ];
+    for (int s = 0; s < n_seq; ++s) {
+        const uint64_t extent = (uint64_t)m->n_layers * m->n_kv_heads * (uint64_t)slots[s].cap * m->head_dim * 2;
+        r[2 * s] = Range{(uintptr_t)slots[s].k, (uintptr_t)slots[s].k + extent, s, 'K'};
+        r[2 * s + 1] = Range{(uintptr_t)slots[s].v, (uintptr_t)slots[s].v + extent, s, 'V'};
+    }
+    for (int a = 0; a < 2 * n_seq; ++a)
+        for (int b = 0; b < a; ++b)
+            REQUIRE(r[a].hi <= r[b].lo || r[b].hi <= r[a].lo || r[a].lo == r[a].hi || r[b].lo == r[b].hi,
+                    LUCE_EINVAL, "%s: the %c cache of slot %d overlaps the %c cache of slot %d", who, r[a].which,
+                    r[a].slot, r[b].which, r[b].slot);
     return LUCE_OK;
 }
 

@@ -69,6 +69,20 @@ cudaError_t launch_matvec(const int8_t* wq, const __half* wd, int N, int K, cons
 cudaError_t launch_matvec_tma(const int8_t* wq, const __half* wd, int N, int K, const int8_t* aq, const float* ad,
                               int T, float* y, int64_t ldy, const float* resid, int64_t ldr, cudaStream_t s);
 
+// The tensor-core matvec (1..16 rows, one launch; matvec_mma.cu):
+// cudaErrorNotSupported, with nothing launched, when K % 256 != 0, an operand
+// is not 16-byte aligned or no tensor-map encoder is available.
+cudaError_t launch_matvec_mma(const int8_t* wq, const __half* wd, int N, int K, const int8_t* aq, const float* ad,
+                              int T, float* y, int64_t ldy, const float* resid, int64_t ldr, cudaStream_t s);
+
+// The matvec through one named kernel (kMatvecPath*); cudaErrorNotSupported,
+// with nothing launched, when that kernel does not serve the shape.
+// (the values of LUCE_MATVEC_AUTO .. LUCE_MATVEC_TENSOR in luce.h)
+enum { kMatvecAuto = 0, kMatvecRegister = 1, kMatvecRing = 2, kMatvecMma = 3 };
+cudaError_t launch_matvec_path(int path, const int8_t* wq, const __half* wd, int N, int K, const int8_t* aq,
+                               const float* ad, int T, float* y, int64_t ldy, const float* resid, int64_t ldr,
+                               cudaStream_t s);
+
 // The fused q|k|v + RoPE + K/V-append projection on the TMA ring (1..8 rows
 // in one launch, 13..16 in two); cudaErrorNotSupported, with nothing
 // launched, otherwise.
@@ -77,8 +91,10 @@ cudaError_t launch_qkv_rope_tma(const int8_t* wq, const __half* wd, int K, const
                                 const KvRows& kv, cudaStream_t s);
 
 // Bounded waits of the TMA-ring kernels that expired on the current device
-// (synchronous); reset clears the counter.
+// (synchronous; the dp4a ring's and the tensor-core ring's counters summed);
+// reset clears the counters.
 cudaError_t read_wait_timeouts(uint32_t* count, bool reset);
+cudaError_t read_mma_wait_timeouts(uint32_t* count, bool reset);
 
 // One bounded wait that nothing completes (limit_ns), counted as expired.
 cudaError_t launch_wait_expiry(uint64_t limit_ns, cudaStream_t s);

@@ -136,20 +136,13 @@ static cudaError_t launch_t(const int8_t* wq, const __half* wd, int N, int K, co
     return e;
 }
 
-cudaError_t launch_matvec(const int8_t* wq, const __half* wd, int N, int K, const int8_t* aq,
-                          const float* ad, int T, float* y, int64_t ldy, const float* resid,
-                          int64_t ldr, cudaStream_t s)
+static cudaError_t launch_matvec_register(const int8_t* wq, const __half* wd, int N, int K, const int8_t* aq,
+                                          const float* ad, int T, float* y, int64_t ldy, const float* resid,
+                                          int64_t ldr, cudaStream_t s)
 {
-    // 1..8 and 13..16 rows with K a multiple of 256 and 16-byte aligned
-    // operands: the weights stream through the TMA ring (matvec_tma.cu);
-    // otherwise the register-pipelined kernel below.  KL (lanes per row), G
-    // (rows per lane) and the form of the int-to-float step (conversion, or
-    // the exact biased chain) only shape the pipeline; none of them, and
-    // neither kernel choice, changes any row's arithmetic.
-    {
-        const cudaError_t e = launch_matvec_tma(wq, wd, N, K, aq, ad, T, y, ldy, resid, ldr, s);
-        if (e != cudaErrorNotSupported) return e;
-    }
+    // KL (lanes per row), G (rows per lane) and the form of the int-to-float
+    // step (conversion, or the exact biased chain) only shape the pipeline;
+    // none of them changes any row's arithmetic.
     switch (T) {
 #define LUCE_MV(TT, KK, GG, BB) \
     case TT: return launch_t<TT, KK, GG, BB>(wq, wd, N, K, aq, ad, y, ldy, resid, ldr, s);
@@ -172,6 +165,39 @@ cudaError_t launch_matvec(const int8_t* wq, const __half* wd, int N, int K, cons
 #undef LUCE_MV
         default: return cudaErrorInvalidValue;
     }
+}
+
+// Rows from which the tensor-core kernel (matvec_mma.cu) takes over from the
+// dp4a TMA ring (measured).
+constexpr int kMmaMinRows = 5;
+
+cudaError_t launch_matvec_path(int path, const int8_t* wq, const __half* wd, int N, int K, const int8_t* aq,
+                               const float* ad, int T, float* y, int64_t ldy, const float* resid, int64_t ldr,
+                               cudaStream_t s)
+{
+    switch (path) {
+        case kMatvecRegister: return launch_matvec_register(wq, wd, N, K, aq, ad, T, y, ldy, resid, ldr, s);
+        case kMatvecRing: return launch_matvec_tma(wq, wd, N, K, aq, ad, T, y, ldy, resid, ldr, s);
+        case kMatvecMma: return launch_matvec_mma(wq, wd, N, K, aq, ad, T, y, ldy, resid, ldr, s);
+        default: break;
+    }
+    // The library's choice: from kMmaMinRows rows the tensor-core ring, below
+    // it the dp4a ring (K a multiple of 256, 16-byte aligned operands), else
+    // the register-pipelined kernel.  All give the same bits.
+    if (T >= kMmaMinRows) {
+        const cudaError_t e = launch_matvec_mma(wq, wd, N, K, aq, ad, T, y, ldy, resid, ldr, s);
+        if (e != cudaErrorNotSupported) return e;
+    }
+    const cudaError_t e = launch_matvec_tma(wq, wd, N, K, aq, ad, T, y, ldy, resid, ldr, s);
+    if (e != cudaErrorNotSupported) return e;
+    return launch_matvec_register(wq, wd, N, K, aq, ad, T, y, ldy, resid, ldr, s);
+}
+
+cudaError_t launch_matvec(const int8_t* wq, const __half* wd, int N, int K, const int8_t* aq,
+                          const float* ad, int T, float* y, int64_t ldy, const float* resid,
+                          int64_t ldr, cudaStream_t s)
+{
+    return launch_matvec_path(kMatvecAuto, wq, wd, N, K, aq, ad, T, y, ldy, resid, ldr, s);
 }
 
 // ------------------------------------------------------------ q|k|v + RoPE + K/V append

@@ -34,9 +34,6 @@
 // Every wait is bounded (about one second on the global timer, 2^26 polls);
 // a wait that expires adds one to a device counter (luce_wait_timeouts) and
 // the CTA stops consuming, leaving its remaining outputs unwritten.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include <string.h>
 
 #include <atomic>
@@ -44,6 +41,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "ring.cuh"
 
 namespace luce {
 
@@ -75,58 +73,6 @@ struct RingLayout {
     static constexpr int SMEM = 128 + S * STAGE + PART + 2 * S * 8;
 };
 
-__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(b)), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* b)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(b)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity)
-{
-    uint32_t done;
-    asm volatile(
-        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-        : "=r"(done)
-        : "r"(smem_addr(b)), "r"(parity)
-        : "memory");
-    return done != 0;
-}
-
-__device__ __forceinline__ uint64_t global_ns()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-constexpr uint64_t kWaitLimitNs = 1000000000ull;  // about one second
-
-// Wait for the phase of parity `parity` to complete, for limit_ns at most
-// (and at most 2^26 polls, should the timer not advance); false (and one
-// more timeout counted) if it did not.
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, uint64_t limit_ns = kWaitLimitNs)
-{
-    if (mbar_try(b, parity)) return true;
-    const uint64_t t0 = global_ns();
-    for (uint32_t polls = 0; !mbar_try(b, parity); ++polls)
-        if (global_ns() - t0 > limit_ns || polls >= (1u << 26)) {
-            atomicAdd(&g_wait_timeouts, 1u);
-            return false;
-        }
-    return true;
-}
-
 // Exercises the expiry path: one thread waits, for limit_ns, on a barrier
 // that expects one arrival nobody makes (no copy is issued), so the wait
 // runs out, is counted, and the kernel returns normally.
@@ -136,32 +82,7 @@ __global__ void wait_expiry_kernel(uint64_t limit_ns)
     if (threadIdx.x != 0) return;
     mbar_init(&bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    mbar_wait(&bar, 0, limit_ns);
-}
-
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, int x, int y, int z, uint64_t* bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
-        "[%5];" ::"r"(smem_addr(dst)),
-        "l"(m), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, int x, int y, uint64_t* bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-        "[%4];" ::"r"(smem_addr(dst)),
-        "l"(m), "r"(x), "r"(y), "r"(smem_addr(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ uint4 lds128(const void* p)
-{
-    uint4 v;
-    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(smem_addr(p)));
-    return v;
+    mbar_wait(&bar, 0, &g_wait_timeouts, limit_ns);
 }
 
 // Exact int32 dot of one block held as two 16-byte halves per side (x pairs
@@ -249,7 +170,7 @@ __device__ __forceinline__ void ring_produce(const RingSmem<T, G, S>& R, int tot
     for (int it = 0; it < pre; ++it) load_acts(it);
     for (int it = pre; it < total; ++it) {
         const int s = it % S;
-        if (!mbar_wait(&R.empty[s], ((it / S) - 1) & 1)) break;
+        if (!mbar_wait(&R.empty[s], ((it / S) - 1) & 1, &g_wait_timeouts)) break;
         mbar_expect_tx(&R.full[s], (uint32_t)(weight_bytes(it) + L::A + L::AD));
         load_weights(it, R.slots + s * L::STAGE, &R.full[s]);
         load_acts(it);
@@ -273,7 +194,7 @@ __device__ __forceinline__ void ring_chains(const RingSmem<T, G, S>& R, int& it,
         for (int t = 0; t < T; ++t) acc[g][t] = 0.0f;
     for (int j = 0; j < nj; ++j, ++it) {
         const int s = it % S;
-        if (ok && !mbar_wait(&R.full[s], (it / S) & 1)) ok = false;
+        if (ok && !mbar_wait(&R.full[s], (it / S) & 1, &g_wait_timeouts)) ok = false;
         if (!ok) continue;
         const uint8_t* slot = R.slots + s * L::STAGE;
         const bool has = 32 * j + c < nb;
@@ -485,7 +406,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 // step's weights and workspace give the same keys every call).
 struct MapKey {
     uint64_t base, dims[3], strides[2];
-    uint32_t box[3], dt, rank;
+    uint32_t box[3], dt, rank, swizzle;
     bool operator==(const MapKey& o) const { return memcmp(this, &o, sizeof(MapKey)) == 0; }
 };
 
@@ -503,16 +424,17 @@ MapCache& map_cache()
     return c;
 }
 
-// A tiled tensor map of `rank` dims (dims[0] innermost, strides in bytes for
-// dims 1..rank-1), no swizzle, zero fill outside the tensor.
+}  // namespace
+
 bool encode_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const cuuint64_t* dims,
-                const cuuint64_t* strides, const cuuint32_t* box)
+                const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swizzle)
 {
     MapKey k;
     memset(&k, 0, sizeof k);
     k.base = (uint64_t)(uintptr_t)base;
     k.dt = (uint32_t)dt;
     k.rank = (uint32_t)rank;
+    k.swizzle = (uint32_t)swizzle;
     for (int i = 0; i < rank; ++i) {
         k.dims[i] = dims[i];
         k.box[i] = box[i];
@@ -533,8 +455,7 @@ bool encode_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ba
     if (!enc) return false;
     const cuuint32_t es[3] = {1, 1, 1};
     if (enc(m, dt, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return false;
     std::lock_guard<std::mutex> lock(c.mu);
     c.key[slot] = k;
@@ -542,10 +463,6 @@ bool encode_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ba
     c.used[slot] = true;
     return true;
 }
-
-// Per-device host state: the SM count and which kernels have had their
-// dynamic shared-memory limit raised (a function attribute set per device).
-constexpr int kMaxDevices = 64;
 
 int current_device()
 {
@@ -566,18 +483,7 @@ int sm_count()
     return n;
 }
 
-// Raises `kernel`'s dynamic shared-memory limit to `bytes` once per device;
-// `done` is the kernel's own per-device flag table.
-template <typename Kern>
-cudaError_t set_smem_once(Kern kernel, int bytes, std::atomic<bool> (&done)[kMaxDevices])
-{
-    const int dev = current_device();
-    if (dev < 0) return cudaErrorInvalidDevice;
-    if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
-    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e == cudaSuccess) done[dev].store(true, std::memory_order_release);
-    return e;
-}
+namespace {
 
 template <int T, int G, int S, bool BIAS>
 cudaError_t launch_tma_t(const CUtensorMap& mw, const CUtensorMap& md, const CUtensorMap& ma, const CUtensorMap& mad,
@@ -735,11 +641,14 @@ cudaError_t launch_wait_expiry(uint64_t limit_ns, cudaStream_t s)
 
 cudaError_t read_wait_timeouts(uint32_t* count, bool reset)
 {
-    cudaError_t e = cudaMemcpyFromSymbol(count, g_wait_timeouts, sizeof(uint32_t));
+    uint32_t mine = 0, mma = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&mine, g_wait_timeouts, sizeof(uint32_t));
     if (e == cudaSuccess && reset) {
         const uint32_t zero = 0;
         e = cudaMemcpyToSymbol(g_wait_timeouts, &zero, sizeof(uint32_t));
     }
+    if (e == cudaSuccess) e = read_mma_wait_timeouts(&mma, reset);
+    if (e == cudaSuccess) *count = mine + mma;
     return e;
 }
 

@@ -67,6 +67,8 @@ def main(argv=None):
     ap.add_argument("--reps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--no-flush", action="store_true")
+    ap.add_argument("--path", type=int, default=0,
+                    help="matvec kernel: 0 library choice, 1 register dp4a, 2 dp4a TMA ring, 3 tensor-core ring")
     a = ap.parse_args(argv)
     build.build()
     luce.load_library()
@@ -79,13 +81,14 @@ def main(argv=None):
         for T in [int(t) for t in a.T.split(",")]:
             aq, ad = luce.luce_q8_quantize_act(cu(wl.acts(0, T, a.K)))
             y = torch.empty((T, a.N), dtype=torch.float32, device="cuda")
-            fn = lambda: luce.luce_q8_matvec_batch(W, D, aq, ad, y)
+            fn = lambda: luce.luce_q8_matvec_batch_path(W, D, aq, ad, a.path, y)
             for _ in range(a.warmup):
                 fn()
             ms = time_launches(torch, fn, flush, a.reps)
             b = a.N * a.K * 34 // 32 + T * a.K + T * (a.K // 32) * 4 + T * a.N * 4
             m = statistics.mean(ms)
-            print(json.dumps({"kernel": "q8_matvec", "N": a.N, "K": a.K, "T": T, "us_mean": round(m * 1e3, 2),
+            print(json.dumps({"kernel": "q8_matvec", "path": a.path, "N": a.N, "K": a.K, "T": T,
+                              "us_mean": round(m * 1e3, 2),
                               "us_min": round(min(ms) * 1e3, 2), "gbps": round(b / m / 1e6, 1)}))
     elif a.kernel == "layer":
         # the four q8_0 projections of the 27B-shaped layer (qkv, o, gate||up, down)
@@ -94,18 +97,28 @@ def main(argv=None):
                   (2 * d.ffn, d.hidden), (d.hidden, d.ffn)]
         mats = [tuple(cu(m) for m in wl.q8_weights(1, wl.tid(wl.W_MAT, 8 + i), N, K)) for i, (N, K) in enumerate(shapes)]
         for T in [int(t) for t in a.T.split(",")]:
-            tot_b, tot_ms = 0, 0.0
+            tot_b, tot_ms, fns, per = 0, 0.0, [], []
             for (N, K), (W, D) in zip(shapes, mats):
                 aq, ad = luce.luce_q8_quantize_act(cu(wl.acts(0, T, K)))
                 y = torch.empty((T, N), dtype=torch.float32, device="cuda")
-                fn = lambda: luce.luce_q8_matvec_batch(W, D, aq, ad, y)
+                fn = (lambda W=W, D=D, aq=aq, ad=ad, y=y: luce.luce_q8_matvec_batch_path(W, D, aq, ad, a.path, y))
+                fns.append(fn)
                 for _ in range(a.warmup):
                     fn()
                 m = statistics.mean(time_launches(torch, fn, flush, a.reps))
-                tot_b += N * K * 34 // 32 + T * K + T * (K // 32) * 4 + T * N * 4
+                b = N * K * 34 // 32 + T * K + T * (K // 32) * 4 + T * N * 4
+                per.append(round(m * 1e3, 2))
+                tot_b += b
                 tot_ms += m
-            print(json.dumps({"kernel": "q8_matvec x4 (27B layer)", "T": T, "us_sum": round(tot_ms * 1e3, 2),
-                              "bytes": tot_b, "gbps": round(tot_b / tot_ms / 1e6, 1)}))
+
+            def layer():
+                for f in fns:
+                    f()
+            mb = statistics.mean(time_launches(torch, layer, flush, a.reps))
+            print(json.dumps({"kernel": "q8_matvec x4 (27B layer)", "path": a.path, "T": T,
+                              "us_alone": per, "us_sum": round(tot_ms * 1e3, 2),
+                              "us_back_to_back": round(mb * 1e3, 2), "bytes": tot_b,
+                              "gbps_alone": round(tot_b / tot_ms / 1e6, 1), "gbps": round(tot_b / mb / 1e6, 1)}))
     elif a.kernel == "attn":
         lens = [int(x) for x in a.lens.split(",")]
         d = wl.Dims(0, a.hq, a.hkv, 128, 0)

@@ -134,6 +134,17 @@ def test_decode_step_refusals(lib):
     # two slots may not share one cache
     same = (luce.SlotC * 2)(luce.SlotC(P, P + 64, 3, 64), luce.SlotC(P, P + 128, 3, 64))
     assert step(ctypes.byref(m), same, rows([1, 1]), 2, P, None, None, P, big, None) == luce.LUCE_EINVAL
+    # ... nor overlap at an offset: each cache here spans 2 layers x 2 heads x 64 positions x 128 halves = 64 KiB
+    ext = 2 * 2 * 64 * 128 * 2
+    apart = (luce.SlotC * 2)(luce.SlotC(P, P + 0x800000, 3, 64), luce.SlotC(P + ext, P + 0x900000, 3, 64))
+    # adjacent caches pass the overlap check (shown by the later workspace refusal; nothing is launched)
+    assert step(ctypes.byref(m), apart, rows([1, 1]), 2, P, None, None, P, 1024, None) == luce.LUCE_ENOSPACE
+    offset = (luce.SlotC * 2)(luce.SlotC(P, P + 0x800000, 3, 64), luce.SlotC(P + ext - 256, P + 0x900000, 3, 64))
+    assert step(ctypes.byref(m), offset, rows([1, 1]), 2, P, None, None, P, big, None) == luce.LUCE_EINVAL
+    assert "overlaps" in status_msg(lib)
+    kv_alias = (luce.SlotC * 1)(luce.SlotC(P, P + ext // 2, 3, 64))
+    assert step(ctypes.byref(m), kv_alias, rows([1]), 1, P, None, None, P, big, None) == luce.LUCE_EINVAL
+    assert "overlaps" in status_msg(lib)
     # logits without a head
     assert step(ctypes.byref(m), s, rows([1, 1]), 2, P, P, None, P, big, None) == luce.LUCE_EINVAL
     m64, _k2 = fake_model(head_dim=64)

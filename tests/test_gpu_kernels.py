@@ -156,6 +156,52 @@ def test_matvec_tma_and_register_kernels_agree_bitwise(N, K):
     assert luce.wait_timeouts() == 0
 
 
+@pytest.mark.parametrize("N,K", [(301, 5120), (37, 1280), (100, 256), (64, 17408), (1, 512), (5, 2048),
+                                 (1000, 1024), (17, 768)])
+def test_matvec_three_kernels_agree_bitwise_and_match_the_oracle(N, K):
+    """The register-pipelined dp4a kernel, the dp4a TMA ring and the
+    tensor-core ring, each named explicitly, at every row count 1..16: the
+    same bits (same chains, same butterfly; the tensor cores form each block
+    dot exactly), and the tensor-core rows within 1e-5 of the oracle.  Ragged
+    N (a 16-row tile mostly past W at N = 1, 5, 17), K shorter than one
+    kilobyte stage (256, 512, 768) and K % 1024 != 0 (1280)."""
+    wq, wd, aq, ad = mv_inputs(N, K, 16, seed=7)
+    W, D = cuda(wq), cuda(wd)
+    for T in range(1, 17):
+        A, Ad = cuda(aq[:T]), cuda(ad[:T])
+        reg = host(luce.luce_q8_matvec_batch_path(W, D, A, Ad, luce.MATVEC_REGISTER))
+        tc = host(luce.luce_q8_matvec_batch_path(W, D, A, Ad, luce.MATVEC_TENSOR))
+        assert np.array_equal(tc.view(np.uint32), reg.view(np.uint32)), ("tensor", T)
+        if 9 <= T <= 12:
+            with pytest.raises(luce.LuceError):
+                luce.luce_q8_matvec_batch_path(W, D, A, Ad, luce.MATVEC_RING)
+        else:
+            ring = host(luce.luce_q8_matvec_batch_path(W, D, A, Ad, luce.MATVEC_RING))
+            assert np.array_equal(ring.view(np.uint32), reg.view(np.uint32)), ("ring", T)
+        auto = host(luce.luce_q8_matvec_batch_path(W, D, A, Ad, luce.MATVEC_AUTO))
+        assert np.array_equal(auto.view(np.uint32), reg.view(np.uint32)), ("auto", T)
+        ref = oracle.matvec(wq, wd, aq[:T], ad[:T])
+        assert np.all(rel_row_err(tc.astype(np.float64), ref) <= 1e-5), T
+    assert luce.wait_timeouts() == 0
+
+
+def test_tensor_core_matvec_writes_only_its_outputs():
+    """Rows past N of the last 16-row tile and tokens past T of the 16-token
+    activation box are computed on zeros and never stored."""
+    N, K = 21, 512
+    for T in (3, 9, 16):
+        wq, wd, aq, ad = mv_inputs(N, K, T, seed=8)
+        buf = np.full((T + 1, N + 12), SENTINEL, np.uint32).view(np.float32)
+        yb = cuda(buf)
+        rc = luce.load_library().luce_q8_matvec_batch_path(
+            cuda(wq).data_ptr(), cuda(wd).data_ptr(), N, K, cuda(aq).data_ptr(), cuda(ad).data_ptr(), T,
+            yb.data_ptr(), N + 12, luce.MATVEC_TENSOR, torch.cuda.current_stream().cuda_stream)
+        assert rc == 0
+        out = host(yb).view(np.uint32)
+        assert np.all(out[:T, N:] == SENTINEL) and np.all(out[T] == SENTINEL)
+        assert not np.any(out[:T, :N] == SENTINEL)
+
+
 @pytest.mark.parametrize("K", [2048, 4096, 5120, 8192])
 def test_matvec_invariance_sweep_full_sizes(K):
     """Batch-invariance sweep at the sweep's sizes: n_tok 1..4 x N in
