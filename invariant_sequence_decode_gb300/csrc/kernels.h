@@ -106,6 +106,11 @@ cudaError_t launch_qkv_rope(const int8_t* wq, const __half* wd, int K, const int
                             float* qkv, int Hq, int Hkv, const RowPos& pos, const RopeFreq& f, float* q_rot,
                             const KvRows& kv, cudaStream_t s);
 
+// RoPE of the q and k heads and the K/V append from a q|k|v projection in
+// qkv [T][(Hq + 2 Hkv) 128] (the epilogue of launch_qkv_rope as its own launch).
+cudaError_t launch_qkv_rope_kv(const float* qkv, int T, int Hq, int Hkv, const RowPos& pos, const RopeFreq& f,
+                               float* q_rot, const KvRows& kv, cudaStream_t s);
+
 cudaError_t launch_block_dots(const int8_t* wq, int N, int K, const int8_t* aq, int T, int32_t* out,
                               cudaStream_t s);
 

@@ -32,6 +32,10 @@
 #include "common.cuh"
 #include "kernels.h"
 
+#ifndef QKV_MMA_MIN
+#define QKV_MMA_MIN 9  // measured: the one-layer step at 4 slots x 3 rows 159 -> 145 us, x 4 rows 161 -> 153 us; equal at 2 rows
+#endif
+
 namespace luce {
 
 // The chains of lane (r, kb) of warp w (c = kb + KL*w) for the G weight rows
@@ -168,8 +172,10 @@ static cudaError_t launch_matvec_register(const int8_t* wq, const __half* wd, in
 }
 
 // Rows from which the tensor-core kernel (matvec_mma.cu) takes over from the
-// dp4a TMA ring (measured).
+// dp4a TMA ring (measured), for the plain matvec and for the step's q|k|v
+// projection (which the dp4a ring serves with RoPE fused at 1..8 rows).
 constexpr int kMmaMinRows = 5;
+constexpr int kMmaQkvMinRows = QKV_MMA_MIN;
 
 cudaError_t launch_matvec_path(int path, const int8_t* wq, const __half* wd, int N, int K, const int8_t* aq,
                                const float* ad, int T, float* y, int64_t ldy, const float* resid, int64_t ldr,
@@ -282,9 +288,20 @@ cudaError_t launch_qkv_rope(const int8_t* wq, const __half* wd, int K, const int
                             float* qkv, int Hq, int Hkv, const RowPos& pos, const RopeFreq& f, float* q_rot,
                             const KvRows& kv, cudaStream_t s)
 {
-    // 1..8 and 13..16 rows on the TMA ring when the shapes allow (matvec_tma.cu);
-    // otherwise the plain kernel's launch shapes, except G = 4 where the plain
-    // kernel takes G = 3 (T = 3, 12): the rotation pairs P = 2G must tile 64
+    // From kMmaQkvMinRows rows: the tensor-core matvec, then RoPE and the
+    // K/V append as a launch of their own (the same rotation and rounding).
+    // Otherwise 1..8 and 13..16 rows on the TMA ring when the shapes allow
+    // (matvec_tma.cu), else the plain kernel's launch shapes, except G = 4
+    // where the plain kernel takes G = 3 (T = 3, 12): the rotation pairs
+    // P = 2G must tile 64
+    if (T >= kMmaQkvMinRows) {
+        const int N = (Hq + 2 * Hkv) * kHeadDim;
+        const cudaError_t e = launch_matvec_mma(wq, wd, N, K, aq, ad, T, qkv, N, nullptr, 0, s);
+        if (e != cudaErrorNotSupported) {
+            if (e != cudaSuccess) return e;
+            return launch_qkv_rope_kv(qkv, T, Hq, Hkv, pos, f, q_rot, kv, s);
+        }
+    }
     {
         const cudaError_t e = launch_qkv_rope_tma(wq, wd, K, aq, ad, T, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
         if (e != cudaErrorNotSupported) return e;

@@ -39,6 +39,48 @@ cudaError_t launch_rope_posvec(float* x, int T, int n_heads, int64_t ldx, const 
     return e;
 }
 
+// RoPE and the K/V append of the decode step from a q|k|v projection already
+// in memory (the wide-verify path, where the projection runs on the tensor
+// cores without an epilogue): one 64-thread CTA per (row t, head h of the
+// q|k|v output), thread i owning the pair (i, i + 64).  q and k heads rotate
+// by the row's position, q heads go to q_rot [T][Hq][128], k and v heads are
+// rounded to binary16 at the row's K/V destination.  These are the rotation
+// and conversion of the fused q|k|v epilogue (rope_cs, rope_rotate, round to
+// nearest), so either path gives the same bits; cos/sin are formed before the
+// wait on the projection.
+__global__ void __launch_bounds__(64)
+qkv_rope_kv_kernel(const float* __restrict__ qkv, int Hq, int Hkv, RowPos pos, RopeFreq f, float* __restrict__ q_rot,
+                   KvRows kv)
+{
+    pdl_trigger();
+    const int t = blockIdx.x, h = blockIdx.y, i = threadIdx.x;
+    const bool rot = h < Hq + Hkv;
+    const float2 cs = rot ? rope_cs(pos.pos[t], f.inv[i]) : make_float2(1.0f, 0.0f);
+    pdl_wait();
+    const float* src = qkv + (size_t)t * (Hq + 2 * Hkv) * kHeadDim + (size_t)h * kHeadDim;
+    float x0 = src[i], x1 = src[i + kHeadDim / 2];
+    if (rot) rope_rotate(x0, x1, cs.x, cs.y);
+    if (h < Hq) {
+        float* dst = q_rot + ((size_t)t * Hq + h) * kHeadDim;
+        dst[i] = x0;
+        dst[i + kHeadDim / 2] = x1;
+    } else {
+        const KvRow r = kv.row[t];
+        __half* dst = rot ? r.k + (h - Hq) * r.head_stride : r.v + (h - Hq - Hkv) * r.head_stride;
+        dst[i] = __float2half_rn(x0);
+        dst[i + kHeadDim / 2] = __float2half_rn(x1);
+    }
+}
+
+cudaError_t launch_qkv_rope_kv(const float* qkv, int T, int Hq, int Hkv, const RowPos& pos, const RopeFreq& f,
+                               float* q_rot, const KvRows& kv, cudaStream_t s)
+{
+    const cudaError_t e =
+        launch_pdl(qkv_rope_kv_kernel, dim3(T, Hq + 2 * Hkv), dim3(kHeadDim / 2), s, qkv, Hq, Hkv, pos, f, q_rot, kv);
+    count_launches(1);
+    return e;
+}
+
 // Standalone K/V append: one CTA per row; fp32 -> binary16 round-to-nearest.
 __global__ void __launch_bounds__(256)
 kv_append_kernel(const float* __restrict__ k, const float* __restrict__ v, int64_t ld, int Hkv, KvRows rows)

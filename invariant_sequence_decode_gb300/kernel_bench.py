@@ -64,6 +64,7 @@ def main(argv=None):
     ap.add_argument("--hq", type=int, default=40)
     ap.add_argument("--hkv", type=int, default=8)
     ap.add_argument("--nseq", type=int, default=4)
+    ap.add_argument("--rows", type=int, default=1, help="step: rows per slot (1 decode, 2..4 verify)")
     ap.add_argument("--reps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--no-flush", action="store_true")
@@ -146,18 +147,20 @@ def main(argv=None):
         model = luce.Model([luce.LayerTensors(*[cu(getattr(Lh, f)) for f in fields])], d.hidden, d.n_q_heads,
                            d.n_kv_heads, d.ffn)
         slots = []
+        cap = 2050 + a.rows
         for s in range(a.nseq):
-            k, v = wl.cache_host(1, s, 0, d, 2051, 2050)
+            k, v = wl.cache_host(1, s, 0, d, cap, 2050)
             slots.append(luce.Slot(cu(k[None]), cu(v[None]), 2050))
-        x = cu(wl.acts(1, a.nseq, d.hidden))
-        ws = model.workspace(a.nseq, 2051)
-        fn = lambda: luce.luce_decode_step(model, slots, [1] * a.nseq, x, ws)
+        T = a.nseq * a.rows
+        x = cu(wl.acts(1, T, d.hidden))
+        ws = model.workspace(T, cap)
+        fn = lambda: luce.luce_decode_step(model, slots, [a.rows] * a.nseq, x, ws)
         for _ in range(a.warmup):
             fn()
         ms = time_launches(torch, fn, flush, a.reps)
         m = statistics.mean(ms)
-        print(json.dumps({"kernel": "decode_step", "nseq": a.nseq, "us_mean": round(m * 1e3, 2),
-                          "tok_s": round(a.nseq / (m / 1e3), 1)}))
+        print(json.dumps({"kernel": "decode_step", "nseq": a.nseq, "rows_per_slot": a.rows,
+                          "us_mean": round(m * 1e3, 2), "tok_s": round(T / (m / 1e3), 1)}))
 
 
 if __name__ == "__main__":
