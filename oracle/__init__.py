@@ -48,7 +48,7 @@ def build(force: bool = False) -> str:
     if not force and os.path.exists(_SO) and os.path.getmtime(_SO) >= os.path.getmtime(_SRC):
         return _SO
     subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
-                    "-fno-fast-math", _SRC, "-o", _SO, "-lm"], check=True)
+                    "-fno-fast-math", "-fopenmp", _SRC, "-o", _SO, "-lm"], check=True)
     return _SO
 
 
@@ -75,8 +75,23 @@ def _load():
         lib.orc_attention_row.argtypes = [vp, vp, vp, i32, i32, i32, i32, i64, i64, dbl, vp]
         lib.orc_swiglu.argtypes = [vp, i32, i32, vp]
         lib.orc_argmax.argtypes = [vp, i32, i32, vp]
+        lib.orc_set_threads.argtypes = [i32]
+        lib.orc_set_threads.restype = i32
+        lib.orc_parallel.restype = i32
         _lib = lib
     return _lib
+
+
+def set_threads(n: int) -> int:
+    """Host threads the oracle's loops use (1 by default); returns the previous
+    count.  Results do not depend on it: each output is computed by one thread
+    with the same serial code."""
+    return int(_load().orc_set_threads(int(n)))
+
+
+def parallel() -> bool:
+    """Whether the oracle library was built with OpenMP."""
+    return bool(_load().orc_parallel())
 
 
 def _c(a: np.ndarray, dtype) -> np.ndarray:

@@ -10,7 +10,11 @@
  * precision the method stores activations in.
  *
  * Build: gcc -O2 -ffp-contract=off (no fast-math), so every float/double
- * operation is a single IEEE-754 operation.
+ * operation is a single IEEE-754 operation; -fopenmp spreads the loops over
+ * independent outputs (rows, heads, blocks) across host threads.  Every
+ * output is still computed by one thread with the serial code below, in the
+ * same order, so the results do not depend on the thread count
+ * (orc_set_threads; 1 by default).
  *
  * Sources ("pages"):
  *   [P1] "feat(qwen4exp): exact 4-slot concurrent serving", section "How it
@@ -30,6 +34,30 @@
 #include <string.h>
 
 #define QK 32 /* q8_0 block length [P5, Commit walkthrough: "each 32-weight block"] */
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+static int orc_threads = 1;
+
+/* Threads the loops below use (>= 1); returns the previous value. */
+int orc_set_threads(int n)
+{
+    int old = orc_threads;
+    orc_threads = n < 1 ? 1 : n;
+    return old;
+}
+
+/* Whether the library was built with OpenMP (otherwise everything runs on one thread). */
+int orc_parallel(void)
+{
+#ifdef _OPENMP
+    return 1;
+#else
+    return 0;
+#endif
+}
 
 /* IEEE-754 binary16 -> double, from the format definition:
  * normal (e in 1..30): (1024 + m) * 2^(e - 25); subnormal: m * 2^-24. */
@@ -75,6 +103,7 @@ uint16_t orc_double_to_half(double f)
 void orc_quantize_act(const float* x, int T, int K, int64_t ldx, int8_t* q, float* d)
 {
     int nb = K / QK;
+#pragma omp parallel for collapse(2) schedule(static) num_threads(orc_threads)
     for (int t = 0; t < T; ++t) {
         for (int b = 0; b < nb; ++b) {
             const float* xb = x + (int64_t)t * ldx + (int64_t)b * QK;
@@ -106,6 +135,7 @@ void orc_quantize_act(const float* x, int T, int K, int64_t ldx, int8_t* q, floa
 void orc_block_dots(const int8_t* wq, int N, int K, const int8_t* aq, int T, int32_t* out)
 {
     int nb = K / QK;
+#pragma omp parallel for collapse(2) schedule(static) num_threads(orc_threads)
     for (int t = 0; t < T; ++t)
         for (int n = 0; n < N; ++n)
             for (int b = 0; b < nb; ++b) {
@@ -128,6 +158,7 @@ void orc_matvec(const int8_t* wq, const uint16_t* wd, int N, int K,
                 const int8_t* aq, const float* ad, int T, double* y)
 {
     int nb = K / QK;
+#pragma omp parallel for collapse(2) schedule(static) num_threads(orc_threads)
     for (int t = 0; t < T; ++t)
         for (int n = 0; n < N; ++n) {
             double acc = 0.0;
@@ -146,6 +177,7 @@ void orc_matvec(const int8_t* wq, const uint16_t* wd, int N, int K,
 /* RMSNorm: y = x / sqrt(mean(x^2) + eps) * gamma, per row of length H. */
 void orc_rmsnorm(const double* x, int T, int H, const float* gamma, double eps, double* y)
 {
+#pragma omp parallel for schedule(static) num_threads(orc_threads)
     for (int t = 0; t < T; ++t) {
         const double* xr = x + (int64_t)t * H;
         double ss = 0.0;
@@ -164,6 +196,7 @@ void orc_rmsnorm(const double* x, int T, int H, const float* gamma, double eps, 
 void orc_rope(double* x, int T, int n_heads, int D, const int32_t* pos, double theta)
 {
     int half = D / 2;
+#pragma omp parallel for collapse(2) schedule(static) num_threads(orc_threads)
     for (int t = 0; t < T; ++t)
         for (int h = 0; h < n_heads; ++h) {
             double* xr = x + ((int64_t)t * n_heads + h) * D;
@@ -189,8 +222,9 @@ void orc_attention_row(const double* q, const uint16_t* k, const uint16_t* v, in
                        double scale, double* out)
 {
     int group = Hq / Hkv;
-    double* s = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+#pragma omp parallel for schedule(static) num_threads(orc_threads)
     for (int h = 0; h < Hq; ++h) {
+        double* s = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
         int g = h / group;
         const double* qh = q + (int64_t)h * D;
         double m = -INFINITY;
@@ -212,14 +246,15 @@ void orc_attention_row(const double* q, const uint16_t* k, const uint16_t* v, in
                 o += s[j] * orc_half_to_double(v[g * head_stride + j * tok_stride + d]);
             out[(int64_t)h * D + d] = L > 0 ? o / l : 0.0;
         }
+        free(s);
     }
-    free(s);
 }
 
 /* SwiGLU: h[t][i] = silu(gu[t][i]) * gu[t][F + i], silu(z) = z / (1 + e^-z);
  * the gate half comes first in the concatenated gate||up output. */
 void orc_swiglu(const double* gu, int T, int F, double* h)
 {
+#pragma omp parallel for collapse(2) schedule(static) num_threads(orc_threads)
     for (int t = 0; t < T; ++t)
         for (int i = 0; i < F; ++i) {
             double g = gu[(int64_t)t * 2 * F + i];
