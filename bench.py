@@ -6,8 +6,9 @@ every projection q8_0) for 4 sequences at 2,051 keys each: RMSNorm ->
 quantize -> QKV matvec -> RoPE + KV append -> split-K attention -> quantize ->
 O matvec -> RMSNorm -> quantize -> gate||up matvec -> SwiGLU -> quantize ->
 down matvec.  Inputs are seeded synthetic data resident in HBM; the L2 is
-flushed between steps (a 256 MiB write, then a read of it so that no dirty
-lines remain), outside the timed events.
+flushed between steps (a 256 MiB write, then a read of a second 256 MiB
+buffer, so the L2 holds clean lines of unrelated data), outside the timed
+events.
 
 Prints ONE JSON line.  `value` = aggregate decode tok/s (rows per second) at
 n_seq = 4; the q8_0 matvec's HBM GB/s (the other half of the metric) is in
@@ -48,7 +49,7 @@ def workload_config(n_seq: int) -> dict:
                         f"{n_seq} sequences x 1 row at {KV_TOKENS} keys of f16 KV",
             "hidden": d.hidden, "n_q_heads": d.n_q_heads, "n_kv_heads": d.n_kv_heads, "head_dim": d.head_dim,
             "ffn": d.ffn, "n_seq": n_seq, "rows": n_seq, "kv_tokens": KV_TOKENS, "seed": 1,
-            "l2": "flushed between steps (256 MiB write then read, outside the timed events)"}
+            "l2": "flushed between steps (256 MiB write, then a read of another 256 MiB; outside the timed events)"}
 
 
 def layer_bytes(d) -> int:
@@ -58,31 +59,22 @@ def layer_bytes(d) -> int:
     return nk * 34 // 32
 
 
-MATVEC_SOURCES = ("matvec.cu", "matvec_tma.cu", "common.cuh")
-
-
-def matvec_sources_hash() -> str:
-    """First 16 hex digits of the SHA-256 over the matvec kernels' sources."""
-    import hashlib
-    h = hashlib.sha256()
-    for f in MATVEC_SOURCES:
-        h.update(open(os.path.join(ROOT, "invariant_sequence_decode_gb300", "csrc", f), "rb").read())
-    return h.hexdigest()[:16]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "q8_matvec_27b_layer_t4_traffic.json")
 
 
 def measured_traffic():
-    """DRAM bytes (read + write) of the four projections at n_tok = 4 from the
-    committed ncu summary, or None when the matvec sources have changed since
-    those counters were taken."""
-    import re
-    prof = os.path.join(ROOT, "profiles", "q8_matvec_27b_layer_t4_traffic.md")
+    """DRAM bytes (read + write) of the layer's four projections at n_tok = 4,
+    as the committed ncu capture recorded them (written by
+    invariant_sequence_decode_gb300.profile_summary), or None when the matvec
+    sources have changed since those counters were taken."""
+    from invariant_sequence_decode_gb300.profile_summary import matvec_sources_hash
     try:
-        m = re.search(r"traffic_bytes_layer_t4=(\d+) matvec_src_sha256_16=([0-9a-f]+)", open(prof).read())
-        if m and matvec_sources_hash() == m.group(2):
-            return int(m.group(1))
-    except OSError:
-        pass
-    return None
+        d = json.load(open(TRAFFIC_FILE))
+    except (OSError, ValueError):
+        return None
+    if d.get("matvec_src_sha256_16") != matvec_sources_hash():
+        return None
+    return d.get("traffic_bytes_per_group")
 
 
 def peaks() -> dict:

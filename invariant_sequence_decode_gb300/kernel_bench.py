@@ -5,9 +5,9 @@
   python -m invariant_sequence_decode_gb300.kernel_bench step --nseq 4
   python -m invariant_sequence_decode_gb300.kernel_bench layer --T 4
 
-Prints one JSON line per case with the mean launch time and the algorithmic
-GB/s (weights N*K*34/32 + activations + outputs for the matvec; K/V bytes
-for attention).  `--reps` launches are timed; use a small `--reps` under a
+Prints one JSON line per case with the launch time (mean, and median where a
+single launch is timed) and the algorithmic GB/s (weights N*K*34/32 +
+activations + outputs for the matvec; K/V bytes for attention).  `--reps` launches are timed; use a small `--reps` under a
 profiler.
 """
 from __future__ import annotations
@@ -20,18 +20,21 @@ import numpy as np
 
 
 class L2Flush:
-    """Write, then read, a 256 MiB buffer: the L2 ends up holding clean lines
-    of an unrelated buffer, so the next launch pays neither hits nor dirty
-    write-backs."""
+    """Write one 256 MiB buffer, then read a second one: the write evicts
+    whatever the L2 held, and the read (twice the L2's size) writes the dirty
+    lines back and leaves the L2 holding clean lines of unrelated data, so the
+    next launch pays neither hits nor write-backs it did not cause.  (Reading
+    back the buffer just written would leave its last lines dirty in L2.)"""
 
     def __init__(self, torch):
         self.torch = torch
         self.buf = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        self.clean = torch.zeros(256 << 20, dtype=torch.uint8, device="cuda")
         self.sink = torch.empty(1, dtype=torch.int64, device="cuda")
 
     def __call__(self):
         self.buf.fill_(1)
-        self.sink.copy_(self.buf.view(self.torch.int64).sum().view(1))
+        self.sink.copy_(self.clean.view(self.torch.int64).sum().view(1))
 
 
 def time_launches(torch, fn, flush, reps: int):
@@ -89,7 +92,7 @@ def main(argv=None):
             b = a.N * a.K * 34 // 32 + T * a.K + T * (a.K // 32) * 4 + T * a.N * 4
             m = statistics.mean(ms)
             print(json.dumps({"kernel": "q8_matvec", "path": a.path, "N": a.N, "K": a.K, "T": T,
-                              "us_mean": round(m * 1e3, 2),
+                              "us_mean": round(m * 1e3, 2), "us_median": round(statistics.median(ms) * 1e3, 2),
                               "us_min": round(min(ms) * 1e3, 2), "gbps": round(b / m / 1e6, 1)}))
     elif a.kernel == "layer":
         # the four q8_0 projections of the 27B-shaped layer (qkv, o, gate||up, down)
@@ -137,8 +140,10 @@ def main(argv=None):
         ms = time_launches(torch, fn, flush, a.reps)
         b = sum(lens) * a.hkv * 128 * 2 * 2
         m = statistics.mean(ms)
+        med = statistics.median(ms)
         print(json.dumps({"kernel": "decode_attn", "lens": lens, "hq": a.hq, "hkv": a.hkv,
-                          "us_mean": round(m * 1e3, 2), "gbps": round(b / m / 1e6, 1)}))
+                          "us_mean": round(m * 1e3, 2), "us_median": round(med * 1e3, 2),
+                          "gbps_median": round(b / med / 1e6, 1)}))
     else:
         d = wl.LAYER27B
         fields = ["attn_norm", "wqkv_q", "wqkv_d", "wo_q", "wo_d", "ffn_norm", "wgu_q", "wgu_d", "wdown_q",
@@ -159,8 +164,10 @@ def main(argv=None):
             fn()
         ms = time_launches(torch, fn, flush, a.reps)
         m = statistics.mean(ms)
+        med = statistics.median(ms)
         print(json.dumps({"kernel": "decode_step", "nseq": a.nseq, "rows_per_slot": a.rows,
-                          "us_mean": round(m * 1e3, 2), "tok_s": round(T / (m / 1e3), 1)}))
+                          "us_mean": round(m * 1e3, 2), "us_median": round(med * 1e3, 2),
+                          "tok_s_median": round(T / (med / 1e3), 1)}))
 
 
 if __name__ == "__main__":
