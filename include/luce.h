@@ -117,6 +117,44 @@ int luce_test_wait_expiry(int64_t limit_ns, void* stream);
 int luce_q8_quantize_act(const float* x, int T, int K, int64_t ldx, int8_t* q, float* d, void* stream);
 
 /*
+ * luce_q8_quantize_act with the block scale stored as binary16, the form a
+ * fused producer must reproduce exactly [qfuse, item 2: match the consuming
+ * quantizer's finite-half guards and division/rounding convention].  The
+ * pages name the guards without stating them; read as: d = amax / 127 (fp32,
+ * IEEE division) rounded to the nearest binary16; a scale that overflows
+ * binary16 (amax / 127 >= 65520) is stored as the largest finite half, 65504,
+ * so no stored scale is infinite; the codes are taken against the stored
+ * scale, q = round(x / float(d)) with the IEEE fp32 division and rounding
+ * half away from zero, clamped to [-127, 127]; a stored scale of zero (also
+ * when amax / 127 underflows binary16) gives all-zero codes; a NaN quotient
+ * gives 0.  float(d) is exact in fp32, so (q, float(d)) feeds
+ * luce_q8_matvec_batch unchanged.
+ *   x (device) fp32 [T][ldx];  q (device) int8 [T][K];  d (device) binary16 [T][K/32]
+ */
+int luce_q8_quantize_act_f16(const float* x, int T, int K, int64_t ldx, int8_t* q, uint16_t* d, void* stream);
+
+/*
+ * The decode step's fused producers of q8_0 activations, as entry points of
+ * their own.  Each writes its fp32 output and that output's q8_0 codes and
+ * scales with the very per-lane routine of luce_q8_quantize_act (half_scale
+ * == 0: d is fp32 [T][K/32]) or of luce_q8_quantize_act_f16 (half_scale != 0:
+ * d is binary16 [T][K/32]), so the codes equal a standalone quantization of
+ * the fp32 output bit for bit [qfuse, item 2].
+ *   luce_rmsnorm_q8: xn[t] = x[t] / sqrt(mean(x[t]^2) + eps) * gamma, the sum
+ *     of squares in a fixed order that depends on H only (8 slices of the
+ *     row's blocks, each summed per lane in ascending order, lanes by an xor
+ *     butterfly, warps in order, then the slices in order); x, xn fp32 [T][H],
+ *     gamma fp32 [H], q int8 [T][H]; 1 <= T <= LUCE_MAX_ROWS, H % 32 == 0.
+ *   luce_swiglu_q8: h[t][i] = silu(gu[t][i]) * gu[t][F + i] (gate half first),
+ *     silu(z) = z / (1 + e^-z); gu fp32 [T][2F], h fp32 [T][F], q int8 [T][F];
+ *     F % 32 == 0.
+ * All pointers (device).
+ */
+int luce_rmsnorm_q8(const float* x, int T, int H, const float* gamma, float eps, float* xn, int8_t* q, void* d,
+                    int half_scale, void* stream);
+int luce_swiglu_q8(const float* gu, int T, int F, float* h, int8_t* q, void* d, int half_scale, void* stream);
+
+/*
  * Narrow-batch q8_0 matvec [ds4-604, Commit walkthrough: each 32-weight
  * block read once and dotted against all tokens; exact-4-slot, How it stays
  * exact: the same arithmetic for 1 row as for 4]:

@@ -81,7 +81,8 @@ EXPORTS = ("luce_last_error", "luce_version", "luce_launch_count", "luce_q8_quan
            "luce_decode_attn_workspace_size", "luce_decode_step_layout", "luce_decode_step",
            "luce_decode_attn_multiseq_noalloc", "luce_decode_attn_noalloc_max_bytes", "luce_decode_attn_paged",
            "luce_decode_step_paged", "luce_wait_timeouts", "luce_decode_step_host",
-           "luce_test_wait_expiry", "luce_q8_matvec_batch_path")
+           "luce_test_wait_expiry", "luce_q8_matvec_batch_path", "luce_q8_quantize_act_f16", "luce_rmsnorm_q8",
+           "luce_swiglu_q8")
 
 _lib = None
 
@@ -102,6 +103,9 @@ def load_library(path: str = LIB_PATH):
     lib.luce_launch_count.restype = ctypes.c_uint64
     lib.luce_launch_count.argtypes = []
     lib.luce_q8_quantize_act.argtypes = [vp, i32, i32, i64, vp, vp, vp]
+    lib.luce_q8_quantize_act_f16.argtypes = [vp, i32, i32, i64, vp, vp, vp]
+    lib.luce_rmsnorm_q8.argtypes = [vp, i32, i32, vp, f32, vp, vp, vp, i32, vp]
+    lib.luce_swiglu_q8.argtypes = [vp, i32, i32, vp, vp, vp, i32, vp]
     lib.luce_q8_matvec_batch.argtypes = [vp, vp, i32, i32, vp, vp, i32, vp, i64, vp]
     lib.luce_q8_matvec_batch_path.argtypes = [vp, vp, i32, i32, vp, vp, i32, vp, i64, i32, vp]
     lib.luce_q8_block_dots.argtypes = [vp, i32, i32, vp, i32, vp, vp]
@@ -177,6 +181,46 @@ def luce_q8_quantize_act(x, q=None, d=None, stream=None):
     d = torch.empty((T, K // QK), dtype=torch.float32, device=x.device) if d is None else d
     _check(load_library().luce_q8_quantize_act(x.data_ptr(), T, K, K, q.data_ptr(), d.data_ptr(), _stream(stream)))
     return q, d
+
+
+def luce_q8_quantize_act_f16(x, q=None, d=None, stream=None):
+    """fp32 [T][K] -> (int8 [T][K], binary16 scales as float16 [T][K/32]): the half-scale form."""
+    import torch
+    _need(x, torch.float32, "x")
+    T, K = x.shape
+    q = torch.empty((T, K), dtype=torch.int8, device=x.device) if q is None else q
+    d = torch.empty((T, K // QK), dtype=torch.float16, device=x.device) if d is None else d
+    _check(load_library().luce_q8_quantize_act_f16(x.data_ptr(), T, K, K, q.data_ptr(), d.data_ptr(),
+                                                   _stream(stream)))
+    return q, d
+
+
+def luce_rmsnorm_q8(x, gamma, eps: float, half_scale: bool = False, stream=None):
+    """RMSNorm of fp32 rows [T][H] and its q8_0 blocks: (xn fp32, q int8, d fp32 or float16)."""
+    import torch
+    _need(x, torch.float32, "x")
+    _need(gamma, torch.float32, "gamma")
+    T, H = x.shape
+    xn = torch.empty_like(x)
+    q = torch.empty((T, H), dtype=torch.int8, device=x.device)
+    d = torch.empty((T, H // QK), dtype=torch.float16 if half_scale else torch.float32, device=x.device)
+    _check(load_library().luce_rmsnorm_q8(x.data_ptr(), T, H, gamma.data_ptr(), float(eps), xn.data_ptr(),
+                                          q.data_ptr(), d.data_ptr(), 1 if half_scale else 0, _stream(stream)))
+    return xn, q, d
+
+
+def luce_swiglu_q8(gu, half_scale: bool = False, stream=None):
+    """SwiGLU of gate||up rows [T][2F] and its q8_0 blocks: (h fp32, q int8, d fp32 or float16)."""
+    import torch
+    _need(gu, torch.float32, "gu")
+    T, F2 = gu.shape
+    F = F2 // 2
+    h = torch.empty((T, F), dtype=torch.float32, device=gu.device)
+    q = torch.empty((T, F), dtype=torch.int8, device=gu.device)
+    d = torch.empty((T, F // QK), dtype=torch.float16 if half_scale else torch.float32, device=gu.device)
+    _check(load_library().luce_swiglu_q8(gu.data_ptr(), T, F, h.data_ptr(), q.data_ptr(), d.data_ptr(),
+                                         1 if half_scale else 0, _stream(stream)))
+    return h, q, d
 
 
 def luce_q8_matvec_batch(wq, wd, aq, ad, y=None, stream=None):

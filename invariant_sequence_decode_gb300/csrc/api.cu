@@ -112,7 +112,39 @@ int luce_q8_quantize_act(const float* x, int T, int K, int64_t ldx, int8_t* q, f
     REQUIRE(K >= 32 && K % 32 == 0, LUCE_EINVAL, "quantize_act: K=%d must be a positive multiple of 32", K);
     REQUIRE(ldx >= K, LUCE_EINVAL, "quantize_act: ldx=%lld < K", (long long)ldx);
     REQUIRE(aligned(x, 4) && aligned(d, 4), LUCE_EINVAL, "quantize_act: x and d must be 4-byte aligned");
-    return cuda_status(launch_quantize(x, T, K, ldx, q, d, (cudaStream_t)stream), "quantize_act");
+    return cuda_status(launch_quantize(x, T, K, ldx, q, d, false, (cudaStream_t)stream), "quantize_act");
+}
+
+int luce_q8_quantize_act_f16(const float* x, int T, int K, int64_t ldx, int8_t* q, uint16_t* d, void* stream)
+{
+    REQUIRE(x && q && d, LUCE_EINVAL, "quantize_act_f16: null pointer");
+    REQUIRE(T >= 1, LUCE_EINVAL, "quantize_act_f16: T=%d must be >= 1", T);
+    REQUIRE(K >= 32 && K % 32 == 0, LUCE_EINVAL, "quantize_act_f16: K=%d must be a positive multiple of 32", K);
+    REQUIRE(ldx >= K, LUCE_EINVAL, "quantize_act_f16: ldx=%lld < K", (long long)ldx);
+    REQUIRE(aligned(x, 4) && aligned(d, 2), LUCE_EINVAL, "quantize_act_f16: x must be 4- and d 2-byte aligned");
+    return cuda_status(launch_quantize(x, T, K, ldx, q, d, true, (cudaStream_t)stream), "quantize_act_f16");
+}
+
+int luce_rmsnorm_q8(const float* x, int T, int H, const float* gamma, float eps, float* xn, int8_t* q, void* d,
+                    int half_scale, void* stream)
+{
+    REQUIRE(x && gamma && xn && q && d, LUCE_EINVAL, "rmsnorm_q8: null pointer");
+    REQUIRE(T >= 1 && T <= LUCE_MAX_ROWS, LUCE_EINVAL, "rmsnorm_q8: T=%d outside 1..%d", T, LUCE_MAX_ROWS);
+    REQUIRE(H >= 32 && H % 32 == 0, LUCE_EINVAL, "rmsnorm_q8: H=%d must be a positive multiple of 32", H);
+    REQUIRE(eps >= 0 && isfinite(eps), LUCE_EINVAL, "rmsnorm_q8: eps must be >= 0");
+    REQUIRE(aligned(x, 4) && aligned(gamma, 4) && aligned(xn, 4) && aligned(d, half_scale ? 2 : 4), LUCE_EINVAL,
+            "rmsnorm_q8: misaligned");
+    return cuda_status(launch_rmsnorm_quant(x, T, H, gamma, eps, xn, q, d, half_scale != 0, (cudaStream_t)stream),
+                       "rmsnorm_q8");
+}
+
+int luce_swiglu_q8(const float* gu, int T, int F, float* h, int8_t* q, void* d, int half_scale, void* stream)
+{
+    REQUIRE(gu && h && q && d, LUCE_EINVAL, "swiglu_q8: null pointer");
+    REQUIRE(T >= 1, LUCE_EINVAL, "swiglu_q8: T=%d must be >= 1", T);
+    REQUIRE(F >= 32 && F % 32 == 0, LUCE_EINVAL, "swiglu_q8: F=%d must be a positive multiple of 32", F);
+    REQUIRE(aligned(gu, 4) && aligned(h, 4) && aligned(d, half_scale ? 2 : 4), LUCE_EINVAL, "swiglu_q8: misaligned");
+    return cuda_status(launch_swiglu_quant(gu, T, F, h, q, d, half_scale != 0, (cudaStream_t)stream), "swiglu_q8");
 }
 
 static int check_matvec(const int8_t* wq, const uint16_t* wd, int N, int K, const int8_t* aq, const float* ad,
@@ -610,7 +642,7 @@ static int decode_step_impl(const luce_model* m, const StepSlot* slots, const in
         }
         ar.total_chunks = c;
 
-        if ((e = launch_rmsnorm_quant(x, T, H, w.attn_norm, m->rms_eps, xn, xn_q, xn_d, st))) break;
+        if ((e = launch_rmsnorm_quant(x, T, H, w.attn_norm, m->rms_eps, xn, xn_q, xn_d, false, st))) break;
         if ((e = launch_qkv_rope(w.wqkv_q, (const __half*)w.wqkv_d, H, xn_q, xn_d, T, qkv, Hq, Hkv, pos, freq, q_rot,
                                  kv, st)))
             break;
@@ -619,11 +651,11 @@ static int decode_step_impl(const luce_model* m, const StepSlot* slots, const in
             break;
         if ((e = launch_matvec(w.wo_q, (const __half*)w.wo_d, H, Hq * D, attn_q, attn_d, T, x1, H, x, H, st)))
             break;
-        if ((e = launch_rmsnorm_quant(x1, T, H, w.ffn_norm, m->rms_eps, xn2, xn2_q, xn2_d, st))) break;
+        if ((e = launch_rmsnorm_quant(x1, T, H, w.ffn_norm, m->rms_eps, xn2, xn2_q, xn2_d, false, st))) break;
         if ((e = launch_matvec(w.wgu_q, (const __half*)w.wgu_d, 2 * F, H, xn2_q, xn2_d, T, gu, 2 * F, nullptr, 0,
                                st)))
             break;
-        if ((e = launch_swiglu_quant(gu, T, F, hh, h_q, h_d, st))) break;
+        if ((e = launch_swiglu_quant(gu, T, F, hh, h_q, h_d, false, st))) break;
         if ((e = launch_matvec(w.wdown_q, (const __half*)w.wdown_d, H, F, h_q, h_d, T, x, H, x1, H, st))) break;
     }
     if (e != cudaSuccess) return cuda_status(e, who);
@@ -632,7 +664,7 @@ static int decode_step_impl(const luce_model* m, const StepSlot* slots, const in
         float* xf = (float*)(wsb + L.xf);
         int8_t* xf_q = (int8_t*)(wsb + L.xf_q);
         float* xf_d = (float*)(wsb + L.xf_d);
-        if ((e = launch_rmsnorm_quant(x, T, H, m->final_norm, m->rms_eps, xf, xf_q, xf_d, st)))
+        if ((e = launch_rmsnorm_quant(x, T, H, m->final_norm, m->rms_eps, xf, xf_q, xf_d, false, st)))
             return cuda_status(e, who);
         if ((e = launch_matvec(m->head_q, (const __half*)m->head_d, m->vocab, H, xf_q, xf_d, T, logits, m->vocab,
                                nullptr, 0, st)))

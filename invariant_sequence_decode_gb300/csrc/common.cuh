@@ -175,6 +175,42 @@ __device__ __forceinline__ int q8_quantize_lane(float x, float* d_out)
     return q8_code(x, d);
 }
 
+// The half-scale form of the same quantizer: the block scale is stored as
+// binary16.  d = amax / 127 (fp32, IEEE division) is rounded to the nearest
+// binary16; a scale that overflows binary16 is replaced by the largest finite
+// half, 65504, so the stored scale is always finite; the codes are taken
+// against the stored scale, q = round(x / float(d16)) with the division and
+// rounding of q8_code (a stored scale of zero gives all-zero codes).  Returns
+// lane i's code; *d_out receives the scale's binary16 bits on every lane.
+__device__ __forceinline__ int q8_quantize_lane_h(float x, uint16_t* d_out)
+{
+    float a = fabsf(x);
+    float amax = (a == a) ? a : 0.0f;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    __half h = __float2half_rn(__fdiv_rn(amax, 127.0f));
+    if (__hisinf(h)) h = __ushort_as_half((unsigned short)0x7BFF);
+    *d_out = __half_as_ushort(h);
+    return q8_code(x, __half2float(h));
+}
+
+// One lane's quantization in either form; the scale goes to d (fp32 or
+// binary16 bits) at block index bi when write_scale.
+template <bool HALF>
+__device__ __forceinline__ int q8_quantize_store(float x, void* d, size_t bi, bool write_scale)
+{
+    if (HALF) {
+        uint16_t dh;
+        const int code = q8_quantize_lane_h(x, &dh);
+        if (write_scale) static_cast<uint16_t*>(d)[bi] = dh;
+        return code;
+    }
+    float dd;
+    const int code = q8_quantize_lane(x, &dd);
+    if (write_scale) static_cast<float*>(d)[bi] = dd;
+    return code;
+}
+
 // Pairwise xor-butterfly sum over the 32 lanes (offsets 16, 8, 4, 2, 1).
 // Both lanes of a pair add the same two values, so all lanes end equal.
 __device__ __forceinline__ float warp_sum_butterfly(float v)

@@ -16,10 +16,11 @@ namespace cg = cooperative_groups;
 
 namespace luce {
 
-// One warp per 32-value block; lane i quantizes element i.
+// One warp per 32-value block; lane i quantizes element i.  HALF: the
+// scales are stored as binary16 (q8_quantize_lane_h).
+template <bool HALF>
 __global__ void __launch_bounds__(256)
-quantize_kernel(const float* __restrict__ x, int T, int K, int64_t ldx, int8_t* __restrict__ q,
-                float* __restrict__ d)
+quantize_kernel(const float* __restrict__ x, int T, int K, int64_t ldx, int8_t* __restrict__ q, void* d)
 {
     pdl_trigger();
     pdl_wait();
@@ -29,17 +30,17 @@ quantize_kernel(const float* __restrict__ x, int T, int K, int64_t ldx, int8_t* 
     if (blk >= (int64_t)T * nb) return;
     const int t = (int)(blk / nb), b = (int)(blk - (int64_t)t * nb);
     const float v = x[(size_t)t * ldx + (size_t)b * 32 + lane];
-    float dd;
-    const int code = q8_quantize_lane(v, &dd);
+    const int code = q8_quantize_store<HALF>(v, d, (size_t)t * nb + b, lane == 0);
     q[(size_t)t * K + (size_t)b * 32 + lane] = (int8_t)code;
-    if (lane == 0) d[(size_t)t * nb + b] = dd;
 }
 
-cudaError_t launch_quantize(const float* x, int T, int K, int64_t ldx, int8_t* q, float* d, cudaStream_t s)
+cudaError_t launch_quantize(const float* x, int T, int K, int64_t ldx, int8_t* q, void* d, bool half_scale,
+                            cudaStream_t s)
 {
     const int64_t blocks = (int64_t)T * (K >> 5);
-    const cudaError_t e = launch_pdl(quantize_kernel, dim3((unsigned)((blocks + 7) / 8)), dim3(256), s, x, T, K, ldx,
-                                     q, d);
+    const dim3 grid((unsigned)((blocks + 7) / 8));
+    const cudaError_t e = half_scale ? launch_pdl(quantize_kernel<true>, grid, dim3(256), s, x, T, K, ldx, q, d)
+                                     : launch_pdl(quantize_kernel<false>, grid, dim3(256), s, x, T, K, ldx, q, d);
     count_launches(1);
     return e;
 }
@@ -59,10 +60,10 @@ constexpr int kNormCtas = 8;
 constexpr int kNormThreads = 128;
 constexpr int kNormMaxPerThread = 16;  // blocks per warp on the register path: H <= 16384
 
-template <bool REG>
+template <bool REG, bool HALF>
 __global__ void __launch_bounds__(kNormThreads)
 rmsnorm_quant_kernel(const float* __restrict__ x, int H, const float* __restrict__ gamma, float eps,
-                     float* __restrict__ xn, int8_t* __restrict__ q, float* __restrict__ d)
+                     float* __restrict__ xn, int8_t* __restrict__ q, void* d)
 {
     constexpr int NW = kNormThreads / 32;
     __shared__ float red[NW];
@@ -122,34 +123,40 @@ rmsnorm_quant_kernel(const float* __restrict__ x, int H, const float* __restrict
             const float e = REG ? v[k] : xr[i];
             const float vn = __fmul_rn(__fmul_rn(e, r), REG ? gv[k] : gamma[i]);
             xn[(size_t)t * H + i] = vn;
-            float dd;
-            const int code = q8_quantize_lane(vn, &dd);
+            const int code = q8_quantize_store<HALF>(vn, d, (size_t)t * nb + b, lane == 0);
             q[(size_t)t * H + i] = (int8_t)code;
-            if (lane == 0) d[(size_t)t * nb + b] = dd;
         }
     }
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");  // no CTA leaves while another may still read its sum
 }
 
-cudaError_t launch_rmsnorm_quant(const float* x, int T, int H, const float* gamma, float eps,
-                                 float* xn, int8_t* q, float* d, cudaStream_t s)
+template <bool HALF>
+static cudaError_t launch_rmsnorm_quant_t(const float* x, int T, int H, const float* gamma, float eps, float* xn,
+                                         int8_t* q, void* d, cudaStream_t s)
 {
     const int bpc = ((H >> 5) + kNormCtas - 1) / kNormCtas;
     const dim3 grid(kNormCtas, T);
-    const cudaError_t e =
-        bpc <= (kNormThreads / 32) * kNormMaxPerThread
-            ? launch_pdl_cluster(rmsnorm_quant_kernel<true>, grid, dim3(kNormThreads), kNormCtas, s, x, H, gamma, eps,
-                                 xn, q, d)
-            : launch_pdl_cluster(rmsnorm_quant_kernel<false>, grid, dim3(kNormThreads), kNormCtas, s, x, H, gamma,
-                                 eps, xn, q, d);
+    return bpc <= (kNormThreads / 32) * kNormMaxPerThread
+               ? launch_pdl_cluster(rmsnorm_quant_kernel<true, HALF>, grid, dim3(kNormThreads), kNormCtas, s, x, H,
+                                    gamma, eps, xn, q, d)
+               : launch_pdl_cluster(rmsnorm_quant_kernel<false, HALF>, grid, dim3(kNormThreads), kNormCtas, s, x, H,
+                                    gamma, eps, xn, q, d);
+}
+
+cudaError_t launch_rmsnorm_quant(const float* x, int T, int H, const float* gamma, float eps, float* xn, int8_t* q,
+                                 void* d, bool half_scale, cudaStream_t s)
+{
+    const cudaError_t e = half_scale ? launch_rmsnorm_quant_t<true>(x, T, H, gamma, eps, xn, q, d, s)
+                                     : launch_rmsnorm_quant_t<false>(x, T, H, gamma, eps, xn, q, d, s);
     count_launches(1);
     return e;
 }
 
 // SwiGLU of the concatenated gate||up row (gate first), then q8_0.
+template <bool HALF>
 __global__ void __launch_bounds__(256)
-swiglu_quant_kernel(const float* __restrict__ gu, int T, int F, float* __restrict__ h,
-                    int8_t* __restrict__ q, float* __restrict__ d)
+swiglu_quant_kernel(const float* __restrict__ gu, int T, int F, float* __restrict__ h, int8_t* __restrict__ q,
+                    void* d)
 {
     pdl_trigger();
     pdl_wait();
@@ -163,18 +170,17 @@ swiglu_quant_kernel(const float* __restrict__ gu, int T, int F, float* __restric
     const float u = gu[(size_t)t * 2 * F + F + i];
     const float v = silu_mul(g, u);
     h[(size_t)t * F + i] = v;
-    float dd;
-    const int code = q8_quantize_lane(v, &dd);
+    const int code = q8_quantize_store<HALF>(v, d, (size_t)t * nb + b, lane == 0);
     q[(size_t)t * F + i] = (int8_t)code;
-    if (lane == 0) d[(size_t)t * nb + b] = dd;
 }
 
-cudaError_t launch_swiglu_quant(const float* gu, int T, int F, float* h, int8_t* q, float* d,
+cudaError_t launch_swiglu_quant(const float* gu, int T, int F, float* h, int8_t* q, void* d, bool half_scale,
                                 cudaStream_t s)
 {
     const int64_t blocks = (int64_t)T * (F >> 5);
-    const cudaError_t e = launch_pdl(swiglu_quant_kernel, dim3((unsigned)((blocks + 7) / 8)), dim3(256), s, gu, T, F,
-                                     h, q, d);
+    const dim3 grid((unsigned)((blocks + 7) / 8));
+    const cudaError_t e = half_scale ? launch_pdl(swiglu_quant_kernel<true>, grid, dim3(256), s, gu, T, F, h, q, d)
+                                     : launch_pdl(swiglu_quant_kernel<false>, grid, dim3(256), s, gu, T, F, h, q, d);
     count_launches(1);
     return e;
 }

@@ -57,7 +57,9 @@ struct RopeFreq {
 };
 RopeFreq rope_freq(double theta);
 
-cudaError_t launch_quantize(const float* x, int T, int K, int64_t ldx, int8_t* q, float* d, cudaStream_t s);
+// d: fp32 [T][K/32] scales, or binary16 bits when half_scale.
+cudaError_t launch_quantize(const float* x, int T, int K, int64_t ldx, int8_t* q, void* d, bool half_scale,
+                            cudaStream_t s);
 
 cudaError_t launch_matvec(const int8_t* wq, const __half* wd, int N, int K, const int8_t* aq,
                           const float* ad, int T, float* y, int64_t ldy, const float* resid,
@@ -134,10 +136,10 @@ cudaError_t launch_attention(const float* q, int64_t ldq, const AttnRows& rows, 
                              float scale, float* part, float* out, int64_t ldo,
                              int8_t* out_q, float* out_d, cudaStream_t s);
 
-cudaError_t launch_rmsnorm_quant(const float* x, int T, int H, const float* gamma, float eps,
-                                 float* xn, int8_t* q, float* d, cudaStream_t s);
+cudaError_t launch_rmsnorm_quant(const float* x, int T, int H, const float* gamma, float eps, float* xn, int8_t* q,
+                                 void* d, bool half_scale, cudaStream_t s);
 
-cudaError_t launch_swiglu_quant(const float* gu, int T, int F, float* h, int8_t* q, float* d,
+cudaError_t launch_swiglu_quant(const float* gu, int T, int F, float* h, int8_t* q, void* d, bool half_scale,
                                 cudaStream_t s);
 
 cudaError_t launch_argmax(const float* x, int T, int V, int32_t* out, cudaStream_t s);

@@ -19,7 +19,9 @@ Pages followed (cited by title and section):
 
 Readings where the pages are silent:
   q8_0 weights stored as int8 [N][K] + binary16 scales [N][K/32]; activation
-  scale stored in fp32, d = amax/127, q = round-half-away(x/d); RoPE pairs
+  scale stored in fp32, d = amax/127, q = round-half-away(x/d) (or, in the
+  half-scale form, d rounded to binary16 with overflow stored as 65504 and
+  the codes taken against the stored d); RoPE pairs
   (i, i + D/2) at angle pos * theta^(-2i/D); GQA head h -> h // (Hq/Hkv);
   pre-norm layer without biases, SwiGLU with the gate rows first; row j of a
   slot with cached length ``len`` sits at position ``len + j`` and attends to
@@ -68,6 +70,7 @@ def _load():
         lib.orc_double_to_half.argtypes = [dbl]
         lib.orc_double_to_half.restype = ctypes.c_uint16
         lib.orc_quantize_act.argtypes = [vp, i32, i32, i64, vp, vp]
+        lib.orc_quantize_act_f16.argtypes = [vp, i32, i32, i64, vp, vp]
         lib.orc_block_dots.argtypes = [vp, i32, i32, vp, i32, vp]
         lib.orc_matvec.argtypes = [vp, vp, i32, i32, vp, vp, i32, vp]
         lib.orc_rmsnorm.argtypes = [vp, i32, i32, vp, dbl, vp]
@@ -134,6 +137,19 @@ def quantize_act(x: np.ndarray):
     q = np.empty((T, K), np.int8)
     d = np.empty((T, K // QK), np.float32)
     _load().orc_quantize_act(_p(x), T, K, K, _p(q), _p(d))
+    return q, d
+
+
+def quantize_act_f16(x: np.ndarray):
+    """The half-scale form: fp32 [T][K] -> (int8 [T][K], binary16 bits [T][K/32] as uint16)."""
+    x = _c(x, np.float32)
+    if x.ndim == 1:
+        x = x[None]
+    T, K = x.shape
+    assert K % QK == 0
+    q = np.empty((T, K), np.int8)
+    d = np.empty((T, K // QK), np.uint16)
+    _load().orc_quantize_act_f16(_p(x), T, K, K, _p(q), _p(d))
     return q, d
 
 

@@ -131,6 +131,50 @@ void orc_quantize_act(const float* x, int T, int K, int64_t ldx, int8_t* q, floa
     }
 }
 
+/*
+ * The half-scale form of the quantizer [P4 item 2: a fused producer must match
+ * the consuming quantizer's finite-half guards and division/rounding
+ * convention].  Reading: the block scale amax / 127 (fp32 division) is stored
+ * as the nearest binary16; a scale that overflows binary16 is stored as the
+ * largest finite half (65504); the codes are round-half-away(x / s) against
+ * the stored scale s (fp32 division), clamped to [-127, 127], 0 when s == 0
+ * or the quotient is NaN.  d receives binary16 bits [T][K/32].
+ */
+void orc_quantize_act_f16(const float* x, int T, int K, int64_t ldx, int8_t* q, uint16_t* d)
+{
+    int nb = K / QK;
+#pragma omp parallel for collapse(2) schedule(static) num_threads(orc_threads)
+    for (int t = 0; t < T; ++t) {
+        for (int b = 0; b < nb; ++b) {
+            const float* xb = x + (int64_t)t * ldx + (int64_t)b * QK;
+            float amax = 0.0f;
+            for (int i = 0; i < QK; ++i) {
+                float a = fabsf(xb[i]);
+                if (a > amax) amax = a;
+            }
+            _Float16 h = (_Float16)(amax / 127.0f);
+            if (isinf((float)h)) h = (_Float16)65504.0f;
+            uint16_t bits;
+            memcpy(&bits, &h, 2);
+            d[(int64_t)t * nb + b] = bits;
+            float s = (float)h;
+            for (int i = 0; i < QK; ++i) {
+                int v = 0;
+                if (s != 0.0f) {
+                    float r = xb[i] / s;
+                    if (r == r) {
+                        float rr = roundf(r);
+                        if (rr > 127.0f) rr = 127.0f;
+                        if (rr < -127.0f) rr = -127.0f;
+                        v = (int)rr;
+                    }
+                }
+                q[(int64_t)t * K + (int64_t)b * QK + i] = (int8_t)v;
+            }
+        }
+    }
+}
+
 /* Per-block integer dots: out[t][n][b] = sum_i wq[n][32b+i] * aq[t][32b+i]. */
 void orc_block_dots(const int8_t* wq, int N, int K, const int8_t* aq, int T, int32_t* out)
 {

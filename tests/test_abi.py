@@ -64,6 +64,19 @@ def test_matvec_ldy_smaller_than_n(lib):
     assert lib.luce_q8_matvec_batch(P, P, 64, 64, P, P, 1, P, 32, None) == luce.LUCE_EINVAL
 
 
+def test_half_scale_and_fused_producer_refusals(lib):
+    assert lib.luce_q8_quantize_act_f16(P, 1, 33, 33, P, P, None) == luce.LUCE_EINVAL       # K not a multiple of 32
+    assert lib.luce_q8_quantize_act_f16(None, 1, 32, 32, P, P, None) == luce.LUCE_EINVAL
+    assert lib.luce_q8_quantize_act_f16(P, 1, 64, 32, P, P, None) == luce.LUCE_EINVAL       # ldx < K
+    assert lib.luce_rmsnorm_q8(P, 17, 64, P, 1e-6, P, P, P, 0, None) == luce.LUCE_EINVAL    # more than 16 rows
+    assert lib.luce_rmsnorm_q8(P, 1, 48, P, 1e-6, P, P, P, 1, None) == luce.LUCE_EINVAL     # H not a multiple of 32
+    assert lib.luce_rmsnorm_q8(P, 1, 64, P, -1.0, P, P, P, 0, None) == luce.LUCE_EINVAL     # negative eps
+    assert lib.luce_rmsnorm_q8(P, 1, 64, P, 1e-6, P, P, P + 2, 0, None) == luce.LUCE_EINVAL  # fp32 scales misaligned
+    assert lib.luce_swiglu_q8(P, 1, 33, P, P, P, 0, None) == luce.LUCE_EINVAL
+    assert lib.luce_swiglu_q8(P, 0, 64, P, P, P, 1, None) == luce.LUCE_EINVAL
+    assert lib.luce_swiglu_q8(P, 1, 64, None, P, P, 1, None) == luce.LUCE_EINVAL
+
+
 def test_quantize_and_rope_refusals(lib):
     assert lib.luce_q8_quantize_act(P, 1, 40, 40, P, P, None) == luce.LUCE_EINVAL
     assert lib.luce_q8_quantize_act(P, 1, 64, 32, P, P, None) == luce.LUCE_EINVAL

@@ -389,6 +389,69 @@ def test_layer_verify_rows_are_causal():
     assert all(not np.array_equal(y[j], y3[j]) for j in range(4))
 
 
+# ----------------------------------------------------------- the half-scale quantizer
+
+def half_bits_of(v):
+    return int(np.array([v], np.float16).view(np.uint16)[0])
+
+
+def test_quantize_f16_equals_the_fp32_form_when_the_scale_is_a_half():
+    # amax = 127 * (a binary16 value): amax / 127 is exact in fp32 and in
+    # binary16, so both forms must give the same codes and the same scale
+    r = np.random.default_rng(41)
+    halves = [1.0, 0.5, 3.0, 1024.0, 65504.0, 2.0 ** -14, 2.0 ** -20, 1.5 * 2.0 ** -17]
+    x = r.uniform(-1, 1, (len(halves), 32)).astype(np.float32)
+    for i, h in enumerate(halves):
+        x[i] *= np.float32(127 * h) / np.max(np.abs(x[i]))
+        x[i, i] = np.float32(127 * h) * (1 if i % 2 else -1)
+    assert np.all(np.max(np.abs(x), axis=1) == np.float32(127) * np.array(halves, np.float32))
+    q16, d16 = oracle.quantize_act_f16(x)
+    q32, d32 = oracle.quantize_act(x)
+    assert np.array_equal(q16, q32)
+    assert np.array_equal(d16[:, 0], np.array([half_bits_of(h) for h in halves], np.uint16))
+    assert np.array_equal(d16.view(np.float16).astype(np.float32), d32)
+
+
+def test_quantize_f16_hand_worked_ties():
+    rows = [l.split() for l in open(os.path.join(HERE, "golden", "q8_ties.txt")) if l.strip() and not l.startswith("#")]
+    x = np.array([float(a) for a, _ in rows], np.float32)
+    want = np.array([int(b) for _, b in rows], np.int8)
+    q, d = oracle.quantize_act_f16(x[None])
+    assert d[0, 0] == half_bits_of(1.0) and np.array_equal(q[0], want)
+
+
+def test_quantize_f16_overflow_is_stored_as_the_largest_finite_half():
+    x = np.zeros((4, 32), np.float32)
+    x[0, :] = np.float32(127.0 * 65504.0)          # exactly the largest half: no guard needed
+    x[1, :] = np.float32(127.0 * 65520.0)          # amax / 127 rounds to inf in binary16
+    x[1, 3] = -np.float32(127.0 * 65520.0)
+    x[2, :] = np.float32(1.0)
+    x[2, 7] = np.float32(np.inf)                   # an infinite entry
+    x[3, :] = np.float32(127.0 * 65519.0)          # just below the rounding boundary: rounds to 65504
+    q, d = oracle.quantize_act_f16(x)
+    assert np.all(d[:, 0] == 0x7BFF)
+    assert np.all(q[0] == 127)
+    assert np.all(q[1][np.arange(32) != 3] == 127) and q[1, 3] == -127
+    assert q[2, 7] == 127 and np.all(q[2][np.arange(32) != 7] == 0)   # 1 / 65504 rounds to 0
+    assert np.all(q[3] == 127)
+    assert np.all(np.isfinite(d.view(np.float16)))
+
+
+def test_quantize_f16_subnormal_and_underflowing_scales():
+    x = np.zeros((3, 32), np.float32)
+    x[0] = np.float32(127.0 * 2.0 ** -20) * np.linspace(-1, 1, 32, dtype=np.float32)   # subnormal half scale
+    x[1] = np.float32(127.0 * 2.0 ** -26)                                           # rounds to zero
+    x[2] = np.float32(127.0 * 1.5 * 2.0 ** -25)                                     # rounds up to 2^-24
+    q, d = oracle.quantize_act_f16(x)
+    assert d[0, 0] == 0x0010                                    # 2^-20 = 16 * 2^-24
+    s0 = np.float32(2.0 ** -20)
+    want0 = np.clip(np.sign(x[0]) * np.floor(np.abs(x[0] / s0) + np.float32(0.5)), -127, 127)
+    assert np.array_equal(q[0], want0.astype(np.int8))
+    assert d[1, 0] == 0 and np.all(q[1] == 0)
+    assert d[2, 0] == 0x0001
+    assert np.all(q[2] == 95)                                    # 127 * 1.5 * 2^-25 / 2^-24 = 95.25 -> 95
+
+
 # ----------------------------------------------------------- hand compositions (numpy, float64)
 #
 # The layer and the head written out again from their definitions with numpy
