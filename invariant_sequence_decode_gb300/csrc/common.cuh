@@ -211,6 +211,37 @@ __device__ __forceinline__ int q8_quantize_store(float x, void* d, size_t bi, bo
     return code;
 }
 
+// The same quantization with the scale returned instead of stored: s holds
+// the fp32 bits (or the binary16 bits when HALF) for q8_store_scale.
+struct Q8Lane {
+    int code;
+    uint32_t s;
+};
+template <bool HALF>
+__device__ __forceinline__ Q8Lane q8_quantize_value(float x)
+{
+    Q8Lane r;
+    if (HALF) {
+        uint16_t dh;
+        r.code = q8_quantize_lane_h(x, &dh);
+        r.s = dh;
+    } else {
+        float dd;
+        r.code = q8_quantize_lane(x, &dd);
+        r.s = __float_as_uint(dd);
+    }
+    return r;
+}
+
+template <bool HALF>
+__device__ __forceinline__ void q8_store_scale(void* d, size_t bi, uint32_t s)
+{
+    if (HALF)
+        static_cast<uint16_t*>(d)[bi] = (uint16_t)s;
+    else
+        static_cast<float*>(d)[bi] = __uint_as_float(s);
+}
+
 // Pairwise xor-butterfly sum over the 32 lanes (offsets 16, 8, 4, 2, 1).
 // Both lanes of a pair add the same two values, so all lanes end equal.
 __device__ __forceinline__ float warp_sum_butterfly(float v)

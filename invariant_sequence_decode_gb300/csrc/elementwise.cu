@@ -7,12 +7,8 @@
 // quantize, SwiGLU + quantize) call the very same per-lane routine as the
 // standalone quantizer, on the same fp32 value they also store, so their
 // codes equal a standalone quantization of their fp32 output bit for bit.
-#include <cooperative_groups.h>
-
 #include "common.cuh"
 #include "kernels.h"
-
-namespace cg = cooperative_groups;
 
 namespace luce {
 
@@ -45,102 +41,147 @@ cudaError_t launch_quantize(const float* x, int T, int K, int64_t ldx, int8_t* q
     return e;
 }
 
-// RMSNorm of one row by a cluster of kNormCtas CTAs (128 threads each), then
-// q8_0 quantization of the normalised row.  CTA c of the row owns the
-// 32-value blocks [c*bpc, (c+1)*bpc), bpc = ceil((H/32) / kNormCtas); its warp
-// w the blocks c*bpc + w, c*bpc + w + 4, ... and lane l element 32b + l of
-// each, read once and kept in registers (gamma is read before the wait on the
-// previous kernel).  Sum of squares, in an order that depends on H only: each
-// thread adds its elements' squares with fma in ascending b; warp partials by
-// butterfly; thread 0 adds its CTA's 4 warp sums in warp order; every thread
-// then adds the kNormCtas CTA sums in rank order, read from the CTAs' shared
-// memory, so all CTAs of the row hold the same r = 1 / sqrt(ss / H + eps)
+// RMSNorm of one row, then q8_0 quantization of the normalised row.  The
+// order of the sum of squares depends on H only: the row's 32-value blocks
+// are cut into kNormSlices slices, slice c = blocks [c*bpc, (c+1)*bpc), bpc =
+// ceil((H/32) / kNormSlices); 4 chains per slice, chain w of slice c taking
+// the blocks c*bpc + w, c*bpc + w + 4, ... with lane l adding element 32b + l
+// (its square, by fma, in ascending b), the chain's 32 lane partials meeting
+// in a butterfly; a slice's sum is its 4 chains added in chain order, the
+// row's sum the slice sums in slice order, and r = 1 / sqrt(ss / H + eps)
 // (IEEE division and square root).
-constexpr int kNormCtas = 8;
-constexpr int kNormThreads = 128;
-constexpr int kNormMaxPerThread = 16;  // blocks per warp on the register path: H <= 16384
+// Launch: kNormCtasPerRow CTAs of 8 warps per row; warp p of CTA k runs the
+// chains p + 8 ((k / 2 + j) % 4), j = 0..3 (chain v = 4c + w), so every CTA
+// forms the row's sum in full, and then normalises and quantizes every second
+// block (from block k % 2) of its first chain, 8 (k / 2) + p, which spreads
+// the per-element divisions over several SMs with few registers per CTA.  gamma
+// is read before the wait on the previous kernel, x once.
+constexpr int kNormSlices = 8;
+constexpr int kNormChains = 4 * kNormSlices;
+constexpr int kNormCtasPerRow = 8;
+constexpr int kNormThreads = 256;
+static_assert(kNormChains * 2 == kNormCtasPerRow * (kNormThreads / 32), "half a chain per warp");
 
-template <bool REG, bool HALF>
+template <int MAXK, bool HALF>  // MAXK: blocks per chain held in registers (0: loop over x)
 __global__ void __launch_bounds__(kNormThreads)
 rmsnorm_quant_kernel(const float* __restrict__ x, int H, const float* __restrict__ gamma, float eps,
                      float* __restrict__ xn, int8_t* __restrict__ q, void* d)
 {
-    constexpr int NW = kNormThreads / 32;
-    __shared__ float red[NW];
-    __shared__ float part;
-    cg::cluster_group cluster = cg::this_cluster();
+    constexpr int NJ = kNormChains / (kNormThreads / 32);  // chains per warp
+    constexpr int KR = MAXK > 0 ? MAXK : 1;
+    __shared__ float red[kNormChains];
+    __shared__ float rs;
     pdl_trigger();
-    const int c = (int)cluster.block_rank();
-    const int t = blockIdx.y;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int t = blockIdx.y, k = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, p = tid >> 5;
     const int nb = H >> 5;
-    const int bpc = (nb + kNormCtas - 1) / kNormCtas;
-    const int b0 = c * bpc, b1 = min(nb, b0 + bpc);
+    const int bpc = (nb + kNormSlices - 1) / kNormSlices;
+    auto first = [&](int v) { return (v >> 2) * bpc + (v & 3); };     // first block of chain v
+    auto end = [&](int v) { return min(nb, ((v >> 2) + 1) * bpc); };  // its slice's end
+    auto chain = [&](int j) { return p + 8 * (((k >> 1) + j) & 3); };
+    const int vo = chain(0), half = k & 1;  // this warp normalises blocks half, half + 2, ... of chain vo
     const float* xr = x + (size_t)t * H;
-    float v[kNormMaxPerThread], gv[kNormMaxPerThread];
-    if (REG) {
+    float gv[KR];
+    if (MAXK > 0) {
 #pragma unroll
-        for (int k = 0; k < kNormMaxPerThread; ++k) {
-            const int b = b0 + warp + NW * k;
-            gv[k] = b < b1 ? gamma[b * 32 + lane] : 0.0f;
+        for (int m = 0; m < KR; ++m) {
+            const int b = first(vo) + 4 * m;
+            gv[m] = ((m & 1) == half && b < end(vo)) ? gamma[b * 32 + lane] : 0.0f;
         }
     }
     pdl_wait();
-    float ss = 0.0f;
-    if (REG) {
+    float xv[NJ][KR];
+    if (MAXK > 0) {
 #pragma unroll
-        for (int k = 0; k < kNormMaxPerThread; ++k) {
-            const int b = b0 + warp + NW * k;
-            v[k] = b < b1 ? xr[b * 32 + lane] : 0.0f;
+        for (int j = 0; j < NJ; ++j)
+#pragma unroll
+            for (int m = 0; m < KR; ++m) {
+                const int v = chain(j), b = first(v) + 4 * m;
+                xv[j][m] = b < end(v) ? xr[b * 32 + lane] : 0.0f;
+            }
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+            const int v = chain(j);
+            float ss = 0.0f;
+#pragma unroll
+            for (int m = 0; m < KR; ++m)
+                if (first(v) + 4 * m < end(v)) ss = __fmaf_rn(xv[j][m], xv[j][m], ss);
+            ss = warp_sum_butterfly(ss);
+            if (lane == 0) red[v] = ss;
+
         }
-#pragma unroll
-        for (int k = 0; k < kNormMaxPerThread; ++k)
-            if (b0 + warp + NW * k < b1) ss = __fmaf_rn(v[k], v[k], ss);
     } else {
-        for (int b = b0 + warp; b < b1; b += NW) {
-            const float e = xr[b * 32 + lane];
-            ss = __fmaf_rn(e, e, ss);
+        for (int j = 0; j < NJ; ++j) {
+            const int v = chain(j);
+            float ss = 0.0f;
+            for (int b = first(v); b < end(v); b += 4) {
+                const float e = xr[b * 32 + lane];
+                ss = __fmaf_rn(e, e, ss);
+            }
+            ss = warp_sum_butterfly(ss);
+            if (lane == 0) red[v] = ss;
         }
     }
-    ss = warp_sum_butterfly(ss);
-    if (lane == 0) red[warp] = ss;
     __syncthreads();
     if (tid == 0) {
-        float s = red[0];
-        for (int w = 1; w < NW; ++w) s = __fadd_rn(s, red[w]);
-        part = s;
+        float tot = 0.0f;
+        for (int c = 0; c < kNormSlices; ++c) {
+            float sl = red[4 * c];
+            for (int w = 1; w < 4; ++w) sl = __fadd_rn(sl, red[4 * c + w]);
+            tot = c == 0 ? sl : __fadd_rn(tot, sl);
+        }
+        rs = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(tot, (float)H), eps)));
     }
-    cluster.sync();  // every CTA's sum is in place
-    float tot = *cluster.map_shared_rank(&part, 0);
-    for (int cc = 1; cc < kNormCtas; ++cc) tot = __fadd_rn(tot, *cluster.map_shared_rank(&part, cc));
-    // done reading the other CTAs' sums: arrive now, wait only before leaving
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-    const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(tot, (float)H), eps)));
+    __syncthreads();
+    const float r = rs;
+    if (MAXK > 0) {
+        // every owned block's quantization computed branch-free (the shuffles
+        // and divisions of the blocks interleave), the stores predicated
+        constexpr int KH = (KR + 1) / 2;
+        float vn[KH];
+        Q8Lane qz[KH];
 #pragma unroll
-    for (int k = 0; k < (REG ? kNormMaxPerThread : 1); ++k) {
-        for (int b = b0 + warp + NW * k; b < b1; b += (REG ? nb : NW)) {
+        for (int h = 0; h < KH; ++h) {
+            // block 2h + half of the chain, picked without indexing by half
+            constexpr int dummy = 0;
+            const int m1 = 2 * h + 1 < KR ? 2 * h + 1 : dummy;
+            const float e = half ? (2 * h + 1 < KR ? xv[0][m1] : 0.0f) : xv[0][2 * h];
+            const float g = half ? (2 * h + 1 < KR ? gv[m1] : 0.0f) : gv[2 * h];
+            vn[h] = __fmul_rn(__fmul_rn(e, r), g);
+        }
+#pragma unroll
+        for (int h = 0; h < KH; ++h) qz[h] = q8_quantize_value<HALF>(vn[h]);
+#pragma unroll
+        for (int h = 0; h < KH; ++h) {
+            const int m = 2 * h + half, b = first(vo) + 4 * m;
+            if (m < KR && b < end(vo)) {
+                const int i = b * 32 + lane;
+                xn[(size_t)t * H + i] = vn[h];
+                q[(size_t)t * H + i] = (int8_t)qz[h].code;
+                if (lane == 0) q8_store_scale<HALF>(d, (size_t)t * nb + b, qz[h].s);
+            }
+        }
+    } else {
+        for (int b = first(vo) + 4 * half; b < end(vo); b += 8) {
             const int i = b * 32 + lane;
-            const float e = REG ? v[k] : xr[i];
-            const float vn = __fmul_rn(__fmul_rn(e, r), REG ? gv[k] : gamma[i]);
+            const float vn = __fmul_rn(__fmul_rn(xr[i], r), gamma[i]);
             xn[(size_t)t * H + i] = vn;
             const int code = q8_quantize_store<HALF>(vn, d, (size_t)t * nb + b, lane == 0);
             q[(size_t)t * H + i] = (int8_t)code;
         }
     }
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");  // no CTA leaves while another may still read its sum
 }
 
 template <bool HALF>
 static cudaError_t launch_rmsnorm_quant_t(const float* x, int T, int H, const float* gamma, float eps, float* xn,
                                          int8_t* q, void* d, cudaStream_t s)
 {
-    const int bpc = ((H >> 5) + kNormCtas - 1) / kNormCtas;
-    const dim3 grid(kNormCtas, T);
-    return bpc <= (kNormThreads / 32) * kNormMaxPerThread
-               ? launch_pdl_cluster(rmsnorm_quant_kernel<true, HALF>, grid, dim3(kNormThreads), kNormCtas, s, x, H,
-                                    gamma, eps, xn, q, d)
-               : launch_pdl_cluster(rmsnorm_quant_kernel<false, HALF>, grid, dim3(kNormThreads), kNormCtas, s, x, H,
-                                    gamma, eps, xn, q, d);
+    const int bpc = ((H >> 5) + kNormSlices - 1) / kNormSlices;
+    const int per_chain = (bpc + 3) / 4;
+    const dim3 grid(kNormCtasPerRow, T), block(kNormThreads);
+    if (per_chain <= 8) return launch_pdl(rmsnorm_quant_kernel<8, HALF>, grid, block, s, x, H, gamma, eps, xn, q, d);
+    if (per_chain <= 16) return launch_pdl(rmsnorm_quant_kernel<16, HALF>, grid, block, s, x, H, gamma, eps, xn, q, d);
+    return launch_pdl(rmsnorm_quant_kernel<0, HALF>, grid, block, s, x, H, gamma, eps, xn, q, d);
 }
 
 cudaError_t launch_rmsnorm_quant(const float* x, int T, int H, const float* gamma, float eps, float* xn, int8_t* q,
