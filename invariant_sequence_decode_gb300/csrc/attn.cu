@@ -54,6 +54,7 @@ constexpr int kTileKeys = 128;    // keys staged in shared memory at a time
 // Row stride of the probabilities: 264 = 8 (mod 32) words, so the value loads
 // of 4 heads x 4 key pairs in one half-warp hit 16 distinct bank pairs.
 constexpr int kPStride = kAttnChunk + 8;
+constexpr int kAttnMaxGroupRows = 4;  // rows of one slot served by one CTA
 
 size_t attn_part_floats(int total_chunks, int Hq) { return (size_t)total_chunks * Hq * kPartStride; }
 
@@ -117,28 +118,57 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_
     lo = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
 }
 
-template <int GQ>
-__global__ void __launch_bounds__(kAttnThreads)
-attn_kernel(const float* __restrict__ q, int64_t ldq, AttnRows rows, int Hq, int Hkv, float scale,
+// Rows that attend to the same cache (a slot's verify rows) are served by one
+// CTA per (chunk, KV head): the chunk's K rows stay in the A fragments and its
+// V tile in shared memory while each row in turn takes its scores, softmax
+// and p.V with its own key count, so the cache is read once per slot rather
+// than once per row.  A row's arithmetic is the same as alone: keys at or
+// past its own count get the score -inf and the probability 0 (the shared V
+// rows there hold other rows' keys instead of zeros, so such a product is a
+// zero of either sign).  Groups take 128-key chunks only (one tile).
+struct AttnGroups {
+    int first[16];
+    int count[16];
+    int chunk_begin[16];  // the group's first chunk index in the grid
+    int n_groups;
+};
+
+// 4 CTAs per SM: a 4 x 2,051-key grid runs in one wave
+template <int GQ, bool GROUPED>
+__global__ void __launch_bounds__(kAttnThreads, 4)
+attn_kernel(const float* __restrict__ q, int64_t ldq, AttnRows rows, AttnGroups groups, int Hq, int Hkv, float scale,
             float* __restrict__ part)
 {
     __shared__ __align__(128) AttnSmem<GQ> sm;
     pdl_trigger();
-    const int chunk = blockIdx.x, g = blockIdx.y;
+    const int g = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int gr = lane >> 2, tq = lane & 3;  // mma fragment: row group, thread in group
     const int mi = lane >> 3, mr = lane & 7;  // ldmatrix: the matrix and row this lane addresses
 
-    int r = 0;
+    // the rows this CTA serves: r0 .. r0 + R - 1, sharing row r0's cache
+    int r0 = 0, R = 1, c = 0;
+    if (GROUPED) {
+        int gi = 0;
 #pragma unroll 1
-    for (int i = 1; i < rows.n_rows; ++i)
-        if (chunk >= rows.row[i].chunk0) r = i;
-    const AttnRow row = rows.row[r];
+        for (int i = 1; i < groups.n_groups; ++i)
+            if ((int)blockIdx.x >= groups.chunk_begin[i]) gi = i;
+        r0 = groups.first[gi];
+        R = groups.count[gi];
+        c = blockIdx.x - groups.chunk_begin[gi];
+    } else {
+#pragma unroll 1
+        for (int i = 1; i < rows.n_rows; ++i)
+            if ((int)blockIdx.x >= rows.row[i].chunk0) r0 = i;
+        c = blockIdx.x - rows.row[r0].chunk0;
+    }
+    const AttnRow row = rows.row[r0];
     const int CH = row.chunk;
-    const int c = chunk - row.chunk0;
     const int key0 = c * CH;
-    const int nvalid = min(CH, row.len - key0);
-    const int ntile = (nvalid + kTileKeys - 1) / kTileKeys;  // tiles of this chunk: 1 or 2
+    int len_max = row.len;
+    for (int i = 1; i < R; ++i) len_max = max(len_max, rows.row[r0 + i].len);
+    const int nvmax = min(CH, len_max - key0);                 // keys of the chunk any row sees
+    const int ntile = (nvmax + kTileKeys - 1) / kTileKeys;     // tiles of this chunk: 1 or 2
     const int h0 = g * GQ;
     // the first key of tile t (keys key0 + 128t ..) of KV head g: tiles
     // never straddle a page, so within a tile keys are tok_stride apart
@@ -152,12 +182,12 @@ attn_kernel(const float* __restrict__ q, int64_t ldq, AttnRows rows, int Hq, int
     if (tid == 0) {
         // stage the first tile's K and V rows in L2 while the previous kernel
         // ends (a cache hint only: the rows it writes are read after pdl_wait)
-        const uint32_t span = (uint32_t)(((int64_t)(min(nvalid, kTileKeys) - 1) * row.tok_stride + kHeadDim) * 2);
+        const uint32_t span = (uint32_t)(((int64_t)(min(nvmax, kTileKeys) - 1) * row.tok_stride + kHeadDim) * 2);
         prefetch_l2(kbase, span);
         prefetch_l2(vbase, span);
     }
     pdl_wait();
-    stage_tile(sm.vt, vbase, row.tok_stride, 0, nvalid);
+    stage_tile(sm.vt, vbase, row.tok_stride, 0, nvmax);
     cp_async_commit();
 
     // K rows of keys j0 + 16w + gr (ka) and + 8 (kb): dims 32tq .. 32tq + 31,
@@ -185,121 +215,144 @@ attn_kernel(const float* __restrict__ q, int64_t ldq, AttnRows rows, int Hq, int
     };
     auto load_k = [&](const __half* kt, int j0) {
         const int ja = j0 + 16 * warp + gr, jb = ja + 8;
-        load_row(kt + (int64_t)(ja - j0) * row.tok_stride + 32 * tq, ja < nvalid, ka);
-        load_row(kt + (int64_t)(jb - j0) * row.tok_stride + 32 * tq, jb < nvalid, kb);
+        load_row(kt + (int64_t)(ja - j0) * row.tok_stride + 32 * tq, ja < nvmax, ka);
+        load_row(kt + (int64_t)(jb - j0) * row.tok_stride + 32 * tq, jb < nvmax, kb);
     };
     load_k(kbase, 0);
-
-    // q as B fragments: step s, lane (head n = lane / 4, t = lane % 4) holds
-    // q[n][32t + 4s .. 32t + 4s + 3]; heads past the group are zero
+    // every row's q slice this thread turns into B fragments: step s = warp,
+    // lane (head n = lane / 4, t = lane % 4) holds q[n][32t + 4s .. 32t + 4s + 3]
+    // (heads past the group are zero), loaded with the first K/V rows
+    constexpr int MR = GROUPED ? kAttnMaxGroupRows : 1;
+    float4 qv[MR];
     {
-        const int s = tid >> 5, n = lane >> 2, t = lane & 3;
-        float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        if (n < GQ)
-            v = *reinterpret_cast<const float4*>(q + (size_t)r * ldq + (size_t)(h0 + n) * kHeadDim + 32 * t + 4 * s);
-        uint4 f;
-        split2(v.x, v.y, f.x, f.z);
-        split2(v.z, v.w, f.y, f.w);
-        sm.qf[s][lane] = f;
-    }
-    __syncthreads();
-
-    // ---- scores of keys j0 + 16w .. j0 + 16w + 15
-    auto scores = [&](int j0) {
-        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        const int n = lane >> 2, t = lane & 3;
 #pragma unroll
-        for (int s = 0; s < 8; ++s) {
-            const uint32_t a[4] = {ka[2 * s], kb[2 * s], ka[2 * s + 1], kb[2 * s + 1]};
-            const uint4 f = sm.qf[s][lane];
-            mma16816(acc, a, f.x, f.y);
-            mma16816(acc, a, f.z, f.w);
+        for (int ri = 0; ri < MR; ++ri) {
+            qv[ri] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (ri < R && n < GQ)
+                qv[ri] = *reinterpret_cast<const float4*>(q + (size_t)(r0 + ri) * ldq + (size_t)(h0 + n) * kHeadDim +
+                                                          32 * t + 4 * warp);
         }
-        // acc: keys ja (c0, c1) and ja + 8 (c2, c3); heads 2tq (c0, c2) and 2tq + 1
-        const int ja = j0 + 16 * warp + gr, jb = ja + 8, h = 2 * tq;
+    }
+
+#pragma unroll
+    for (int ri = 0; ri < MR; ++ri) {
+        if (ri >= R) break;
+        const int r = r0 + ri;
+        const int len = GROUPED ? rows.row[r].len : row.len;
+        if (key0 >= len) continue;  // this row's keys end before the chunk (the same for every thread)
+        const int nvalid = min(CH, len - key0);
+        if (ri > 0) __syncthreads();  // the previous row is done with the q fragments and probabilities
+
+        // q as B fragments (hi, lo)
+        {
+            uint4 f;
+            split2(qv[ri].x, qv[ri].y, f.x, f.z);
+            split2(qv[ri].z, qv[ri].w, f.y, f.w);
+            sm.qf[warp][lane] = f;
+        }
+        __syncthreads();
+
+        // ---- scores of keys j0 + 16w .. j0 + 16w + 15
+        auto scores = [&](int j0) {
+            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const uint32_t a[4] = {ka[2 * s], kb[2 * s], ka[2 * s + 1], kb[2 * s + 1]};
+                const uint4 f = sm.qf[s][lane];
+                mma16816(acc, a, f.x, f.y);
+                mma16816(acc, a, f.z, f.w);
+            }
+            // acc: keys ja (c0, c1) and ja + 8 (c2, c3); heads 2tq (c0, c2) and 2tq + 1
+            const int ja = j0 + 16 * warp + gr, jb = ja + 8, h = 2 * tq;
+            if (h < GQ) {
+                sm.p[h][ja] = ja < nvalid ? __fmul_rn(acc[0], scale) : -INFINITY;
+                sm.p[h][jb] = jb < nvalid ? __fmul_rn(acc[2], scale) : -INFINITY;
+            }
+            if (h + 1 < GQ) {
+                sm.p[h + 1][ja] = ja < nvalid ? __fmul_rn(acc[1], scale) : -INFINITY;
+                sm.p[h + 1][jb] = jb < nvalid ? __fmul_rn(acc[3], scale) : -INFINITY;
+            }
+        };
+        scores(0);
+        if (ntile == 2) {  // 256-key chunks: never grouped (R == 1)
+            load_k(tile_base(row.k, 1), kTileKeys);
+            scores(kTileKeys);
+        }
+        __syncthreads();
+
+        // ---- chunk softmax statistics, warp h per head
+        float* pout = part + ((size_t)(rows.row[r].chunk0 + c) * Hq + h0) * kPartStride;
+        for (int h = warp; h < GQ; h += 8) {
+            float sv[kAttnChunk / 32];
+            float m = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < kAttnChunk / 32; ++i) {
+                const int j = lane + 32 * i;
+                sv[i] = (32 * i < CH && j < nvalid) ? sm.p[h][j] : -INFINITY;
+                m = fmaxf(m, sv[i]);
+            }
+            m = warp_max(m);
+            float l = 0.0f;
+#pragma unroll
+            for (int i = 0; i < kAttnChunk / 32; ++i) {
+                const int j = lane + 32 * i;
+                if (32 * i < CH) {
+                    const float p = j < nvalid ? expf(__fsub_rn(sv[i], m)) : 0.0f;
+                    sm.p[h][j] = p;
+                    l = __fadd_rn(l, p);
+                }
+            }
+            l = warp_sum_butterfly(l);
+            if (lane == 0) {
+                pout[(size_t)h * kPartStride + 128] = m;
+                pout[(size_t)h * kPartStride + 129] = l;
+            }
+        }
+        if (ri == 0) cp_async_wait_all();
+        __syncthreads();
+
+        // ---- p . V for dims 16w .. 16w + 15, 16 keys per step: D[dim][head]
+        // += V^T (A: the tile's rows read transposed) times P^T (B: the
+        // probabilities of heads gr, split hi + lo)
+        float o[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        const uint32_t vt = (uint32_t)__cvta_generic_to_shared(sm.vt);
+        auto values = [&](int j0) {
+#pragma unroll 2
+            for (int ks = 0; ks < kTileKeys / 16; ++ks) {
+                float2 x = make_float2(0.0f, 0.0f), y = make_float2(0.0f, 0.0f);
+                if (gr < GQ) {
+                    x = *reinterpret_cast<const float2*>(&sm.p[gr][j0 + 16 * ks + 2 * tq]);
+                    y = *reinterpret_cast<const float2*>(&sm.p[gr][j0 + 16 * ks + 2 * tq + 8]);
+                }
+                uint32_t bh0, bl0, bh1, bl1;
+                split2(x.x, x.y, bh0, bl0);
+                split2(y.x, y.y, bh1, bl1);
+                uint32_t a[4];  // (keys 0-7 | 8-15 of the step) x (dims 0-7 | 8-15 of the warp)
+                ldsm_x4_trans(vt + 2 * tile_off(16 * ks + 8 * (mi >> 1) + mr, 2 * warp + (mi & 1)), a);
+                mma16816(o, a, bh0, bh1);
+                mma16816(o, a, bl0, bl1);
+            }
+        };
+        values(0);
+        if (ntile == 2) {
+            __syncthreads();  // every warp is done with the first V tile
+            stage_tile(sm.vt, tile_base(row.v, 1), row.tok_stride, kTileKeys, nvalid);
+            cp_async_commit();
+            cp_async_wait_all();
+            __syncthreads();
+            values(kTileKeys);
+        }
+        // o: dims 16w + gr (o0, o1) and 16w + gr + 8 (o2, o3); heads 2tq (o0, o2) and 2tq + 1
+        const int d = 16 * warp + gr, h = 2 * tq;
         if (h < GQ) {
-            sm.p[h][ja] = ja < nvalid ? __fmul_rn(acc[0], scale) : -INFINITY;
-            sm.p[h][jb] = jb < nvalid ? __fmul_rn(acc[2], scale) : -INFINITY;
+            pout[(size_t)h * kPartStride + d] = o[0];
+            pout[(size_t)h * kPartStride + d + 8] = o[2];
         }
         if (h + 1 < GQ) {
-            sm.p[h + 1][ja] = ja < nvalid ? __fmul_rn(acc[1], scale) : -INFINITY;
-            sm.p[h + 1][jb] = jb < nvalid ? __fmul_rn(acc[3], scale) : -INFINITY;
+            pout[(size_t)(h + 1) * kPartStride + d] = o[1];
+            pout[(size_t)(h + 1) * kPartStride + d + 8] = o[3];
         }
-    };
-    scores(0);
-    if (ntile == 2) {
-        load_k(tile_base(row.k, 1), kTileKeys);
-        scores(kTileKeys);
-    }
-    __syncthreads();
-
-    // ---- chunk softmax statistics, warp h per head
-    float* pout = part + ((size_t)chunk * Hq + h0) * kPartStride;
-    for (int h = warp; h < GQ; h += 8) {
-        float sv[kAttnChunk / 32];
-        float m = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < kAttnChunk / 32; ++i) {
-            const int j = lane + 32 * i;
-            sv[i] = (32 * i < CH && j < nvalid) ? sm.p[h][j] : -INFINITY;
-            m = fmaxf(m, sv[i]);
-        }
-        m = warp_max(m);
-        float l = 0.0f;
-#pragma unroll
-        for (int i = 0; i < kAttnChunk / 32; ++i) {
-            const int j = lane + 32 * i;
-            if (32 * i < CH) {
-                const float p = j < nvalid ? expf(__fsub_rn(sv[i], m)) : 0.0f;
-                sm.p[h][j] = p;
-                l = __fadd_rn(l, p);
-            }
-        }
-        l = warp_sum_butterfly(l);
-        if (lane == 0) {
-            pout[(size_t)h * kPartStride + 128] = m;
-            pout[(size_t)h * kPartStride + 129] = l;
-        }
-    }
-    cp_async_wait_all();
-    __syncthreads();
-
-    // ---- p . V for dims 16w .. 16w + 15, 16 keys per step
-    float o[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
-    const uint32_t vt = (uint32_t)__cvta_generic_to_shared(sm.vt);
-    auto values = [&](int j0) {
-#pragma unroll 2
-        for (int ks = 0; ks < kTileKeys / 16; ++ks) {
-            float2 x = make_float2(0.0f, 0.0f), y = make_float2(0.0f, 0.0f);
-            if (gr < GQ) {
-                x = *reinterpret_cast<const float2*>(&sm.p[gr][j0 + 16 * ks + 2 * tq]);
-                y = *reinterpret_cast<const float2*>(&sm.p[gr][j0 + 16 * ks + 2 * tq + 8]);
-            }
-            uint32_t ah[4], al[4];
-            split2(x.x, x.y, ah[0], al[0]);
-            split2(y.x, y.y, ah[2], al[2]);
-            ah[1] = ah[3] = al[1] = al[3] = 0u;  // rows 8..15 of A: no heads
-            uint32_t b[4];
-            ldsm_x4_trans(vt + 2 * tile_off(16 * ks + 8 * (mi & 1) + mr, 2 * warp + (mi >> 1)), b);
-            mma16816(o[0], ah, b[0], b[1]);
-            mma16816(o[0], al, b[0], b[1]);
-            mma16816(o[1], ah, b[2], b[3]);
-            mma16816(o[1], al, b[2], b[3]);
-        }
-    };
-    values(0);
-    if (ntile == 2) {
-        __syncthreads();  // every warp is done with the first V tile
-        stage_tile(sm.vt, tile_base(row.v, 1), row.tok_stride, kTileKeys, nvalid);
-        cp_async_commit();
-        cp_async_wait_all();
-        __syncthreads();
-        values(kTileKeys);
-    }
-    if (gr < GQ) {
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-            *reinterpret_cast<float2*>(pout + (size_t)gr * kPartStride + 16 * warp + 8 * nt + 2 * tq) =
-                make_float2(o[nt][0], o[nt][1]);
     }
 }
 
@@ -374,8 +427,36 @@ template <int GQ>
 static cudaError_t launch_g(const float* q, int64_t ldq, const AttnRows& rows, int Hq, int Hkv, float scale,
                             float* part, float* out, int64_t ldo, int8_t* out_q, float* out_d, cudaStream_t s)
 {
-    cudaError_t e = launch_pdl(attn_kernel<GQ>, dim3(rows.total_chunks, Hkv), dim3(kAttnThreads), s, q, ldq, rows,
-                               Hq, Hkv, scale, part);
+    // consecutive rows on the same cache with 128-key chunks form a group (at
+    // most kAttnMaxGroupRows rows); a launch with no group of two or more rows
+    // keeps one CTA per row chunk
+    AttnGroups grp{};
+    int n = 0, chunks = 0;
+    bool any = false;
+    for (int r = 0; r < rows.n_rows;) {
+        const AttnRow& a = rows.row[r];
+        int cnt = 1, len_max = a.len;
+        while (r + cnt < rows.n_rows && cnt < kAttnMaxGroupRows) {
+            const AttnRow& b = rows.row[r + cnt];
+            if (b.k != a.k || b.v != a.v || b.head_stride != a.head_stride || b.tok_stride != a.tok_stride ||
+                b.pages != a.pages || b.page_stride != a.page_stride || a.chunk != kTileKeys || b.chunk != kTileKeys)
+                break;
+            len_max = max(len_max, b.len);
+            ++cnt;
+        }
+        grp.first[n] = r;
+        grp.count[n] = cnt;
+        grp.chunk_begin[n] = chunks;
+        chunks += (len_max + a.chunk - 1) / a.chunk;
+        any = any || cnt > 1;
+        ++n;
+        r += cnt;
+    }
+    grp.n_groups = n;
+    cudaError_t e = any ? launch_pdl(attn_kernel<GQ, true>, dim3(chunks, Hkv), dim3(kAttnThreads), s, q, ldq, rows,
+                                     grp, Hq, Hkv, scale, part)
+                        : launch_pdl(attn_kernel<GQ, false>, dim3(rows.total_chunks, Hkv), dim3(kAttnThreads), s, q,
+                                     ldq, rows, grp, Hq, Hkv, scale, part);
     count_launches(1);
     if (e != cudaSuccess) return e;
     e = launch_pdl(attn_merge_kernel, dim3(Hq, rows.n_rows), dim3(kHeadDim), s, rows, Hq, (const float*)part, out,
