@@ -391,6 +391,32 @@ def test_attention_batched_equals_solo_bitwise():
         assert np.array_equal(perm[newr0:newr0 + n].view(np.uint32), batched[old:old + n].view(np.uint32))
 
 
+def test_attention_grouped_rows_equal_separate_caches_bitwise():
+    """Rows of one view (one cache) are served together, one CTA per (chunk,
+    KV head) for all of them; the same rows, each on its own copy of the
+    cache, are served one CTA per row.  Same bits: rows whose key counts end
+    in different chunks (127..130 keys), a 27B-shaped slot, and rows on both
+    sides of the 16,384-key chunk-size switch (which are not grouped)."""
+    scale = 0.08838834764831845
+    lens, nq = [130, 2051, 16386, 1], [4, 4, 4, 1]
+    q, caches, views = attn_case(13, lens, nq, 40, 8)
+    grouped = run_attn(q, caches, views, 8, scale)
+    rows = []  # (cache, key count, row) of every row, each row on a cache of its own
+    for (k, v), (L, n, r0) in zip(caches, views):
+        for j in range(n):
+            rows.append(((cuda(k), cuda(v)), L - n + 1 + j, r0 + j))
+    separate = np.empty_like(grouped)
+    for i in range(0, len(rows), 4):  # at most 4 views per call
+        part = rows[i:i + 4]
+        sv = [luce.SeqView(kk, vv, L, 1, j) for j, ((kk, vv), L, _) in enumerate(part)]
+        got = host(luce.luce_decode_attn_multiseq(cuda(q[[r for _, _, r in part]]), sv, 8, scale))
+        for j, (_, _, r) in enumerate(part):
+            separate[r] = got[j]
+    assert np.array_equal(grouped.view(np.uint32), separate.view(np.uint32))
+    ref = oracle_attn(q, caches, views, 8, scale)
+    assert np.max(np.abs(grouped - ref)) <= 2e-3
+
+
 def test_bounded_wait_expires_counts_and_leaves_the_context_usable():
     """A wait on a barrier that nothing completes gives up after its limit,
     is counted by luce_wait_timeouts, and the next launches run normally."""
