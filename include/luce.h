@@ -74,10 +74,12 @@ uint64_t luce_launch_count(void);
  * dp4a ring matvec, which luce_q8_matvec_batch takes at 1..4 rows; the
  * tensor-core ring matvec, at 5..16 rows; the fused q|k|v + RoPE + K/V-append
  * projection of the decode step on either ring) wait on shared-memory
- * barriers for those copies.  Every such
- * wait gives up after about one second and adds one to this device counter,
- * so a stalled copy engine surfaces here instead of as a hung stream.  A
- * healthy run reads 0.
+ * barriers for those copies, and the attention that serves a slot's verify
+ * rows together waits on one for its tcgen05 MMAs.  Every such wait gives up
+ * after about one second and adds one to this device counter, so a stalled
+ * copy engine or tensor core surfaces here instead of as a hung stream.  A
+ * healthy run reads 0 (an attention CTA whose wait expired writes none of its
+ * partial outputs).
  *
  * A non-zero count means the device context is suspect, not that some
  * outputs were merely skipped: the CTA whose wait expired stops writing and

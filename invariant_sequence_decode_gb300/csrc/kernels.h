@@ -92,11 +92,12 @@ cudaError_t launch_qkv_rope_tma(const int8_t* wq, const __half* wd, int K, const
                                 float* qkv, int Hq, int Hkv, const RowPos& pos, const RopeFreq& f, float* q_rot,
                                 const KvRows& kv, cudaStream_t s);
 
-// Bounded waits of the TMA-ring kernels that expired on the current device
-// (synchronous; the dp4a ring's and the tensor-core ring's counters summed);
+// Bounded waits that expired on the current device (synchronous; the dp4a
+// ring's, the tensor-core ring's and the slot attention's counters summed);
 // reset clears the counters.
 cudaError_t read_wait_timeouts(uint32_t* count, bool reset);
 cudaError_t read_mma_wait_timeouts(uint32_t* count, bool reset);
+cudaError_t read_attn_wait_timeouts(uint32_t* count, bool reset);
 
 // One bounded wait that nothing completes (limit_ns), counted as expired.
 cudaError_t launch_wait_expiry(uint64_t limit_ns, cudaStream_t s);

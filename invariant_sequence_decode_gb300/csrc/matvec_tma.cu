@@ -641,14 +641,15 @@ cudaError_t launch_wait_expiry(uint64_t limit_ns, cudaStream_t s)
 
 cudaError_t read_wait_timeouts(uint32_t* count, bool reset)
 {
-    uint32_t mine = 0, mma = 0;
+    uint32_t mine = 0, mma = 0, attn = 0;
     cudaError_t e = cudaMemcpyFromSymbol(&mine, g_wait_timeouts, sizeof(uint32_t));
     if (e == cudaSuccess && reset) {
         const uint32_t zero = 0;
         e = cudaMemcpyToSymbol(g_wait_timeouts, &zero, sizeof(uint32_t));
     }
     if (e == cudaSuccess) e = read_mma_wait_timeouts(&mma, reset);
-    if (e == cudaSuccess) *count = mine + mma;
+    if (e == cudaSuccess) e = read_attn_wait_timeouts(&attn, reset);
+    if (e == cudaSuccess) *count = mine + mma + attn;
     return e;
 }
 

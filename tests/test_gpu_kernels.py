@@ -391,16 +391,21 @@ def test_attention_batched_equals_solo_bitwise():
         assert np.array_equal(perm[newr0:newr0 + n].view(np.uint32), batched[old:old + n].view(np.uint32))
 
 
-def test_attention_grouped_rows_equal_separate_caches_bitwise():
-    """Rows of one view (one cache) are served together, one CTA per (chunk,
-    KV head) for all of them; the same rows, each on its own copy of the
-    cache, are served one CTA per row.  Same bits: rows whose key counts end
-    in different chunks (127..130 keys), a 27B-shaped slot, and rows on both
-    sides of the 16,384-key chunk-size switch (which are not grouped)."""
+def test_attention_slot_rows_with_chunk_edges():
+    """A slot's verify rows on 128-key chunks are served together (one CTA per
+    (chunk, KV head), p.V on tcgen05), a single such row by the one-row form
+    of the same kernel, rows past 16,384 keys one CTA per row chunk.  Rows
+    whose key counts end in different chunks (127..130 keys), a 27B-shaped
+    slot, rows on both sides of the 16,384-key chunk-size switch and a single
+    row: within the oracle's tolerance, bit for bit the same rows served one
+    by one (each on a cache of its own), and a slot's rows keep their bits
+    when the other slots of the launch change."""
     scale = 0.08838834764831845
     lens, nq = [130, 2051, 16386, 1], [4, 4, 4, 1]
     q, caches, views = attn_case(13, lens, nq, 40, 8)
     grouped = run_attn(q, caches, views, 8, scale)
+    ref = oracle_attn(q, caches, views, 8, scale)
+    assert np.max(np.abs(grouped - ref)) <= 2e-3
     rows = []  # (cache, key count, row) of every row, each row on a cache of its own
     for (k, v), (L, n, r0) in zip(caches, views):
         for j in range(n):
@@ -413,8 +418,12 @@ def test_attention_grouped_rows_equal_separate_caches_bitwise():
         for j, (_, _, r) in enumerate(part):
             separate[r] = got[j]
     assert np.array_equal(grouped.view(np.uint32), separate.view(np.uint32))
-    ref = oracle_attn(q, caches, views, 8, scale)
-    assert np.max(np.abs(grouped - ref)) <= 2e-3
+    # the 130-key slot with other company: its rows keep their bits
+    q2, caches2, views2 = attn_case(21, [700, 130], [1, 4], 40, 8)
+    caches2[1] = caches[0]
+    q2[1:5] = q[0:4]
+    other = run_attn(q2, caches2, views2, 8, scale)
+    assert np.array_equal(other[1:5].view(np.uint32), grouped[0:4].view(np.uint32))
 
 
 def test_bounded_wait_expires_counts_and_leaves_the_context_usable():
