@@ -330,6 +330,7 @@ def oracle_attn(q, caches, views, Hkv, scale):
     ([2051, 2051, 2051, 2051], [1, 1, 1, 1], 40, 8),   # the 27B layer's attention
     ([1030, 1800, 2051, 1500], [4, 3, 2, 4], 40, 8),   # verify rows (causal)
     ([600], [4], 4, 4),
+    ([1100, 300, 130, 2051], [4, 2, 1, 3], 64, 8),  # 8 query heads per KV head: the widest slot form
 ])
 def test_attention_parity(lens, nq, Hq, Hkv):
     scale = np.float32(1 / math.sqrt(128))
