@@ -8,49 +8,53 @@
 // A row's keys are cut into chunks of CH keys, CH = attn_chunk_keys(row's key
 // count) (128 up to 16,384 keys, else 256: small contexts get smaller chunks
 // so the GPU has enough independent work).  One CTA of 256 threads (8 warps)
-// per (row, chunk, KV head g) serves all GQ = Hq/Hkv query heads of g, so each
-// K/V byte is read once.  Both contractions run on the tensor cores (mma
-// m16n8k16: f16 operands, fp32 accumulation).  f16 holds K and V exactly; q
-// and the probabilities are fp32, so each is split into two f16 parts,
-// x = hi + lo with hi = f16(x) and lo = f16(x - hi), and both parts are
-// multiplied in.  Keys are taken 128 at a time (a tile):
-//   scores   warp w owns keys 16w..16w+15 of the tile and loads their K rows
-//            straight into its A fragments: lane quarter t holds dims
-//            32t..32t+31, and step s = 0..7 contracts dims 32t+4s..32t+4s+3
-//            of every quarter t (q is laid out the same way); per step the
-//            q_hi, then the q_lo product is accumulated; s_h = scale * dot;
+// per (row unit, chunk, KV head g) serves all GQ = Hq/Hkv query heads of g,
+// so each K/V byte is read once.  Both contractions run on the tensor cores
+// with f16 operands and fp32 accumulation.  f16 holds K and V exactly; q and
+// the probabilities are fp32, so each is split into two f16 parts, x = hi +
+// lo with hi = f16(x) and lo = f16(x - hi), and both parts are multiplied in.
+// Keys are taken 128 at a time (a tile):
+//   scores   (mma.sync m16n8k16) warp w owns keys 16w..16w+15 of the tile and
+//            loads their K rows straight into its A fragments: lane quarter
+//            t holds dims 32t..32t+31, and step s = 0..7 contracts dims
+//            32t+4s..32t+4s+3 of every quarter t (q is laid out the same
+//            way); per step the q_hi, then the q_lo product is accumulated;
+//            s_h = scale * dot;
 //   softmax  warp h owns head h: m = max_j s_hj, p_hj = exp(s_hj - m),
 //            l = sum p_hj (lane-serial over j = lane + 32i, then butterfly);
-//   values   the tile's V rows are staged in shared memory by cp.async
-//            (16-byte pieces, piece c of key j at c ^ (j & 7), so ldmatrix
-//            reads them without bank conflicts) while the scores and the
-//            softmax run; warp w owns dims 16w..16w+15 and, for each step of
-//            16 keys in key order, accumulates p_hi.V, then p_lo.V.
-//   -> scratch (o_h[128], m_h, l_h) for the chunk.
-// A second kernel, launched behind the first with programmatic dependent
-// launch (its wait returns once every chunk is written), merges each (row,
-// query head) over the row's chunks, one CTA per pair and one thread per dim:
+//   values   the tile's V rows are staged in shared memory by cp.async while
+//            the scores and the softmax run, then p.V:
+//            - rows with 128-key chunks (attn_slot_kernel): consecutive rows
+//              on one cache (a slot's verify rows) share one CTA, each row
+//              taking its scores and softmax in turn, and p.V of all of them
+//              is one tcgen05.mma pass: D[dim][n] = sum over the chunk's keys
+//              of V[key][dim] P[n][key], A = the V tile (MN-major), B = the
+//              rows' hi and lo probabilities (K-major), D in tensor memory
+//              (lane = dim), out = D[hi] + D[lo]; each output column depends
+//              on its own probability row only, so a row gives the same bits
+//              alone, with its slot's other rows or as a single decode row;
+//              the MMAs' completion wait is bounded and counts in
+//              luce_wait_timeouts;
+//            - rows past 16,384 keys (256-key chunks, two tiles through one V
+//              buffer; attn_kernel): mma.sync, warp w owns dims 16w..16w+15
+//              and for each step of 16 keys in key order accumulates
+//              p_hi.V, then p_lo.V (A = the tile read transposed).
+//   -> scratch (o_h[128], m_h, l_h) per row and chunk.
+// A further kernel, launched behind with programmatic dependent launch (its
+// wait returns once every chunk is written), merges each (row, query head)
+// over the row's chunks, one CTA per pair and one thread per dim:
 //   M = max_c m_c, w_c = e^(m_c - M), L = sum_c l_c w_c, O = sum_c o_c w_c,
 //   out = O / L  (O sequential over c; L lane-serial over c = lane + 32i,
 //   then a butterfly),
 // and optionally quantizes out to q8_0 blocks (the Wo projection's input).
-// Every chunking and reduction order depends only on the row's own key
-// count, never on the other rows, on which CTA merges or on the grid.
+// Every chunking and reduction order, and which kernel serves a row, depends
+// only on the row's own key count, never on the other rows, on which CTA
+// merges or on the grid.
 // A row's cache is flat or paged: pages hold 128 keys, one tile, so only the
 // address of a tile's first key comes from the page table and a paged cache
 // gives the flat cache's bits.
 // The split of q assumes |q| < 65504 (the f16 range); larger entries make
 // the row's scores non-finite.
-// Rows with 128-key chunks (up to 16,384 keys) are served by attn_slot_kernel:
-// consecutive ones on one cache (a slot's verify rows) together, one CTA per
-// (chunk, KV head) for all of them, so the cache is read once per slot; each
-// row takes its scores and softmax as above (K stays in the A fragments),
-// and p.V of all the rows is one tcgen05.mma pass with the V tile and the
-// probabilities in shared memory and the accumulator in tensor memory (its
-// bounded waits count in luce_wait_timeouts).  Each output column depends on
-// its own probability row only, so a row gives the same bits alone, with its
-// slot's other rows or as a single decode row; which kernel serves a row
-// depends on its own key count only.
 #include <math.h>
 
 #include "common.cuh"
