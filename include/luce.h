@@ -266,9 +266,16 @@ int luce_kv_append(const float* k, const float* v, int64_t ldkv, int Hkv, int D,
  *   out (device) fp32 [T][Hq][D]
  *   ws  (device) scratch of at least luce_decode_attn_workspace_size(...)
  *       bytes, 16-byte aligned (the chunk partials; no initial contents).
- * Two kernels: the chunks, then their merge, launched behind it on the same
- * stream (it starts once every chunk is written); no kernel waits on another
- * CTA and nothing needs zeroing between calls.
+ * The chunks run on the tensor cores: rows with 128-key chunks in one kernel
+ * (a view's rows share one CTA per (chunk, KV head), so the view's cache is
+ * read once; scores on mma.sync, p.V on tcgen05.mma into tensor memory, whose
+ * bounded wait counts in luce_wait_timeouts), rows with 256-key chunks in
+ * another (mma.sync); which serves a row depends on its own key count only,
+ * and a row gives the same bits alone or with its view's other rows.  Their
+ * merge is launched behind them on the same stream (it starts once every
+ * chunk is written): two launches, or three when both kinds of rows are
+ * present.  No kernel waits on another CTA and nothing needs zeroing between
+ * calls.
  * D == 128, Hq % Hkv == 0, Hq / Hkv <= 8, 1 <= n_seq <= LUCE_MAX_SEQ,
  * 1 <= len - n_q + 1, len <= cap, len <= LUCE_MAX_KEYS.
  */
