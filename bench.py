@@ -433,25 +433,49 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                 "algorithmic_bytes": mv["4"]["layer"]["bytes"],
                 "achieved_launches_alone": round(mv["4"]["all"]["gbps"], 1)}
 
-    # end to end through the C ABI with host buffers (luce_decode_step_host,
-    # arguments marshalled once by HostStep): pinned H2D of the step's rows,
-    # the step, D2H of its output rows, then a stream synchronisation, all
-    # inside the timed region
+    # end to end through the C ABI with host buffers: the step's rows from
+    # page-locked host memory, the step, its output rows back to page-locked
+    # host memory, then a stream synchronisation, all inside the timed region.
+    # The buffers are mapped, so the first and last kernels move the rows over
+    # the host link (no copy-engine transfer).  Headline: luce_decode_step_host
+    # (HostStep), the launches issued one by one; the same loop through the
+    # step graph (luce_step_graph_run, StepGraph) is reported beside it.  The
+    # slots' length alternates between two values from step to step, as in
+    # decoding where it grows, so positions, K/V destinations and attention
+    # rows change every step (and every graph run refreshes those nodes).
     xh = torch.from_numpy(L.x_host[:n_seq].copy()).pin_memory()
     outh = torch.empty_like(xh).pin_memory()
     xd = torch.empty((n_seq, L.d.hidden), dtype=torch.float32, device="cuda")
+
+    def e2e_loop(step):
+        ms = []
+        c0 = luce.launch_count()
+        for i in range(args.warmup + args.steps):
+            for s in L.slots[:n_seq]:
+                s.len = L.len - (i & 1)
+            L.flush_l2()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            step()
+            torch.cuda.synchronize()
+            if i >= args.warmup:
+                ms.append((time.perf_counter() - t0) * 1e3)
+        for s in L.slots[:n_seq]:
+            s.len = L.len
+        n_calls = args.warmup + args.steps
+        return (replicas.aggregate(sum(ms), n_seq * args.steps, device="cuda")["rows_per_s"],
+                (luce.launch_count() - c0) / n_calls)
+
     step_host = luce.HostStep(L.model, L.slots[:n_seq], [1] * n_seq, xh, xd, L.ws, x_out=outh)
-    e2e_ms = []
-    for i in range(args.warmup + args.steps):
-        L.flush_l2()
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        step_host()
-        torch.cuda.synchronize()
-        if i >= args.warmup:
-            e2e_ms.append((time.perf_counter() - t0) * 1e3)
-    e2e = {"value": replicas.aggregate(sum(e2e_ms), n_seq * args.steps, device="cuda")["rows_per_s"], "unit": "tok/s",
-           "h2d_bytes_per_step": int(xh.numel() * 4), "d2h_bytes_per_step": int(outh.numel() * 4)}
+    v, per = e2e_loop(step_host)
+    e2e = {"value": v, "unit": "tok/s", "api": "luce_decode_step_host",
+           "h2d_bytes_per_step": int(xh.numel() * 4), "d2h_bytes_per_step": int(outh.numel() * 4),
+           "host_buffers": "page-locked, mapped (rows moved by the first and last kernels)",
+           "kernels_per_step": per}
+    graph = luce.StepGraph(L.model, L.slots[:n_seq], [1] * n_seq, xh, xd, L.ws, x_out=outh)
+    v, per = e2e_loop(graph)
+    detail["e2e_step_graph"] = {"tok_s": v, "kernels_per_step": per, **graph.stats()}
+    graph.close()
 
     cpu = None
     if rank == 0 and world == 1:

@@ -414,14 +414,61 @@ int luce_decode_step(const luce_model* m, const luce_slot* slots, const int32_t*
  * on the stream and without waiting: x_in (host, fp32 [T][hidden]) is copied
  * to x (device, the step's in/out rows), the step runs, then x is copied to
  * x_out (host, nullable) and argmax to argmax_out (host, nullable; needs
- * argmax).  Host buffers should be page-locked so the copies run
- * asynchronously; the caller synchronises the stream before reading x_out.
+ * argmax).  A host buffer that is page-locked memory mapped into the device's
+ * address space (cudaPointerGetAttributes gives a device address for all of
+ * it; 16-byte aligned for x_out) is not copied by the copy engine: the first
+ * RMSNorm reads x_in through the mapping (and fills x), and one kernel after
+ * the last layer stores x_out and argmax_out through it.  Other buffers take
+ * cudaMemcpyAsync (pageable ones then wait for the host).  Either way the
+ * caller synchronises the stream before reading x_out.
  * Validation is luce_decode_step's (plus a non-null x_in); a refused call
  * enqueues nothing.
  */
 int luce_decode_step_host(const luce_model* m, const luce_slot* slots, const int32_t* rows_per_slot, int n_seq,
                           const float* x_in, float* x, float* x_out, float* logits, int32_t* argmax,
                           int32_t* argmax_out, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * The step of luce_decode_step_host as one CUDA graph, for repeated steps over
+ * the same slots and buffers [ds4-604, section 2; the step's launches are
+ * the same ones].  A host call that issues the step's 9 or more launches
+ * one by one costs tens of microseconds on the host per step; a graph is
+ * started with one call.
+ *
+ * luce_step_graph_create binds the model, the slots' caches (k, v, cap; len
+ * is taken per run), rows_per_slot, and the buffers of luce_decode_step_host
+ * (x_in host, x device, x_out host or NULL, logits/argmax device or NULL,
+ * argmax_out host or NULL, ws), validating them as luce_decode_step_host
+ * would at the slots' given lengths; it makes no CUDA call.  All of them must
+ * stay valid, unchanged and unmoved until luce_step_graph_destroy; *out is
+ * the new object (NULL on error).
+ *
+ * luce_step_graph_run (lens: host int32 [n_seq], each slot's current length)
+ * enqueues on the stream exactly what luce_decode_step_host would with those
+ * lengths - every layer, with x_in read and x_out / argmax_out written through
+ * their mapping - with the same kernels and arguments, hence the same bits.
+ * The host buffers must be page-locked and mapped (else LUCE_EUNSUPPORTED,
+ * checked at the first run).  The first run captures the
+ * launches into a graph on a private stream; a later run whose launches form
+ * the same sequence refreshes only the kernel nodes whose arguments changed
+ * (positions, K/V destinations, attention rows and grids), otherwise it
+ * captures anew.  Validation is luce_decode_step_host's; a refused run
+ * enqueues nothing.  One object serves one thread at a time; runs on
+ * different streams are not ordered with each other.
+ *
+ * luce_step_graph_stats: how many captures and node refreshes the object has
+ * made, and the kernel nodes of its graph (each pointer nullable).
+ * luce_step_graph_destroy releases the graph (NULL is accepted); the caller
+ * first waits for the runs it enqueued.
+ */
+typedef struct luce_step_graph luce_step_graph;
+
+int luce_step_graph_create(const luce_model* m, const luce_slot* slots, const int32_t* rows_per_slot, int n_seq,
+                           const float* x_in, float* x, float* x_out, float* logits, int32_t* argmax,
+                           int32_t* argmax_out, void* ws, size_t ws_bytes, luce_step_graph** out);
+int luce_step_graph_run(luce_step_graph* g, const int32_t* lens, void* stream);
+int luce_step_graph_stats(const luce_step_graph* g, int64_t* captures, int64_t* node_updates, int32_t* kernels);
+int luce_step_graph_destroy(luce_step_graph* g);
 
 /*
  * A slot whose K/V lives in pages of LUCE_PAGE_KEYS tokens: pool page p holds

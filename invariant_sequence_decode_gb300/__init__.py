@@ -82,7 +82,8 @@ EXPORTS = ("luce_last_error", "luce_version", "luce_launch_count", "luce_q8_quan
            "luce_decode_attn_multiseq_noalloc", "luce_decode_attn_noalloc_max_bytes", "luce_decode_attn_paged",
            "luce_decode_step_paged", "luce_wait_timeouts", "luce_decode_step_host",
            "luce_test_wait_expiry", "luce_q8_matvec_batch_path", "luce_q8_quantize_act_f16", "luce_rmsnorm_q8",
-           "luce_swiglu_q8")
+           "luce_swiglu_q8", "luce_step_graph_create", "luce_step_graph_run", "luce_step_graph_stats",
+           "luce_step_graph_destroy")
 
 _lib = None
 
@@ -127,6 +128,13 @@ def load_library(path: str = LIB_PATH):
     lib.luce_test_wait_expiry.argtypes = [i64, vp]
     lib.luce_decode_step_host.argtypes = [ctypes.POINTER(ModelC), ctypes.POINTER(SlotC), ctypes.POINTER(ctypes.c_int32),
                                           i32, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.luce_step_graph_create.argtypes = [ctypes.POINTER(ModelC), ctypes.POINTER(SlotC),
+                                           ctypes.POINTER(ctypes.c_int32), i32, vp, vp, vp, vp, vp, vp, vp, sz,
+                                           ctypes.POINTER(vp)]
+    lib.luce_step_graph_run.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), vp]
+    lib.luce_step_graph_stats.argtypes = [vp, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64),
+                                          ctypes.POINTER(ctypes.c_int32)]
+    lib.luce_step_graph_destroy.argtypes = [vp]
     for name in EXPORTS:
         if name not in ("luce_last_error", "luce_version", "luce_launch_count", "luce_decode_attn_workspace_size",
                         "luce_decode_attn_noalloc_max_bytes"):
@@ -537,3 +545,59 @@ class HostStep:
         for i, s in enumerate(self.slots):
             sc[i].len = s.len
         _check(self._fn(*self._args))
+
+
+class StepGraph:
+    """luce_step_graph: the step of HostStep (same arguments) kept as one CUDA
+    graph.  Each call passes the slots' current ``len`` to luce_step_graph_run,
+    which refreshes the graph's changed nodes (or captures it anew) and
+    launches it on the stream given at construction (else the current stream).
+    Synchronise the stream before reading x_out.  close() (or garbage
+    collection) releases the graph once the stream has finished its runs."""
+
+    def __init__(self, model: Model, slots: Sequence[Slot], rows_per_slot: Sequence[int], x_in, x, ws,
+                 x_out=None, logits=None, argmax=None, argmax_out=None, stream=None):
+        import torch
+        _need(x, torch.float32, "x")
+        if x_in.device.type != "cpu" or x_in.dtype != torch.float32 or not x_in.is_contiguous():
+            raise TypeError("x_in: expected a contiguous CPU float32 tensor")
+        if x_in.shape != x.shape or (x_out is not None and x_out.shape != x.shape):
+            raise ValueError("x_in, x and x_out must have the same shape")
+        self.slots = list(slots)
+        n = len(self.slots)
+        sc = (SlotC * max(1, n))()
+        for i, s in enumerate(self.slots):
+            sc[i] = SlotC(s.k.data_ptr(), s.v.data_ptr(), s.len, s.cap)
+        rows = (ctypes.c_int32 * max(1, n))(*rows_per_slot)
+        self._lens = (ctypes.c_int32 * max(1, n))()
+        self._keep = (model, x_in, x, ws, x_out, logits, argmax, argmax_out)
+        self._lib = load_library()
+        self._stream = _stream(stream)
+        h = ctypes.c_void_p()
+        _check(self._lib.luce_step_graph_create(ctypes.byref(model.c), sc, rows, n, x_in.data_ptr(), x.data_ptr(),
+                                                _ptr(x_out), _ptr(logits), _ptr(argmax), _ptr(argmax_out),
+                                                ws.data_ptr(), ws.numel(), ctypes.byref(h)))
+        self._h = h
+
+    def __call__(self):
+        lens = self._lens
+        for i, s in enumerate(self.slots):
+            lens[i] = s.len
+        _check(self._lib.luce_step_graph_run(self._h, lens, self._stream))
+
+    def stats(self) -> dict:
+        """Captures and node refreshes so far, and the graph's kernel nodes."""
+        c, u, k = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int32()
+        _check(self._lib.luce_step_graph_stats(self._h, ctypes.byref(c), ctypes.byref(u), ctypes.byref(k)))
+        return {"captures": c.value, "node_updates": u.value, "kernels": k.value}
+
+    def close(self):
+        if getattr(self, "_h", None) and self._h.value:
+            self._lib.luce_step_graph_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -10,6 +10,7 @@
 #include <algorithm>
 #include <atomic>
 #include <mutex>
+#include <new>
 #include <string>
 
 #include "../../include/luce.h"
@@ -19,7 +20,14 @@
 using namespace luce;
 
 static std::atomic<uint64_t> g_launches{0};
-void luce::count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+thread_local LaunchLog* luce::t_launch_log = nullptr;
+
+// A recorded launch is not a launch: the step graph counts its kernel nodes
+// when it launches the graph.
+void luce::count_launches(int n)
+{
+    if (!t_launch_log) g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed);
+}
 
 RopeFreq luce::rope_freq(double theta)
 {
@@ -513,17 +521,79 @@ struct StepSlot {
     const int32_t* table_host;
 };
 
+// A host<->device copy of the step: issued on the stream, or written to the
+// launch log while one is being recorded.
+static cudaError_t step_copy(void* dst, const void* src, size_t bytes, cudaMemcpyKind dir, cudaStream_t st)
+{
+    if (LaunchLog* log = t_launch_log) {
+        log->recs.emplace_back();
+        LaunchRec& r = log->recs.back();
+        r.copy = true;
+        r.func = nullptr;
+        r.grid = r.block = dim3(0, 0, 0);
+        r.smem = 0;
+        r.nargs = r.nbytes = 0;
+        r.dst = dst;
+        r.src = src;
+        r.bytes = bytes;
+        r.dir = dir;
+        return cudaSuccess;
+    }
+    return cudaMemcpyAsync(dst, src, bytes, dir, st);
+}
+
 // Host buffers of luce_decode_step_host (all nullable): the step's input rows,
-// and where its output rows and argmax are copied back.
+// and where its output rows and argmax are copied back.  The *_dev members
+// are their device addresses when the buffers are page-locked memory mapped
+// into the device's address space (resolve_io): the step's kernels then read
+// x_in and write x_out / argmax_out directly, over the host link, in place of
+// copy-engine transfers.
 struct HostIO {
     const float* x_in;
     float* x_out;
     int32_t* argmax_out;
+    const float* x_in_dev = nullptr;
+    float* x_out_dev = nullptr;
+    int32_t* argmax_out_dev = nullptr;
+    bool outputs_resolved = false;  // else the step looks the output views up after its launches
 };
 
-static int decode_step_impl(const luce_model* m, const StepSlot* slots, const int32_t* rows_per_slot, int n_seq,
-                            float* x, float* logits, int32_t* argmax, void* ws, size_t ws_bytes, void* stream,
-                            const char* who, const HostIO& io = HostIO{nullptr, nullptr, nullptr})
+// The device address of host buffer [p, p + bytes) when all of it is mapped
+// page-locked memory and that address is `align`-aligned, else nullptr.
+static void* device_view(const void* p, size_t bytes, size_t align)
+{
+    if (!p || bytes == 0) return nullptr;
+    cudaPointerAttributes a0, a1;
+    if (cudaPointerGetAttributes(&a0, p) != cudaSuccess ||
+        cudaPointerGetAttributes(&a1, (const char*)p + bytes - 1) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    if (a0.type != cudaMemoryTypeHost || a1.type != cudaMemoryTypeHost || !a0.devicePointer || !a1.devicePointer)
+        return nullptr;
+    if ((const char*)a1.devicePointer - (const char*)a0.devicePointer != (ptrdiff_t)(bytes - 1)) return nullptr;
+    if ((uintptr_t)a0.devicePointer % align != 0) return nullptr;
+    return a0.devicePointer;
+}
+
+static void resolve_input(HostIO* io, int T, int H)
+{
+    io->x_in_dev = (const float*)device_view(io->x_in, (size_t)T * H * sizeof(float), 4);
+}
+
+static void resolve_outputs(HostIO* io, int T, int H)
+{
+    io->x_out_dev = (float*)device_view(io->x_out, (size_t)T * H * sizeof(float), 16);
+    io->argmax_out_dev = (int32_t*)device_view(io->argmax_out, (size_t)T * sizeof(int32_t), 4);
+    io->outputs_resolved = true;
+}
+
+// The step's own argument checks (the slots are checked by the callers):
+// buffers, weights, row count and workspace size.  On success *L is the
+// workspace layout and *T the row count.
+static int check_step(const luce_model* m, const StepSlot* slots, const int32_t* rows_per_slot, int n_seq, float* x,
+                      float* logits, int32_t* argmax, void* ws, size_t ws_bytes, const char* who, const HostIO& io,
+                      luce_step_layout* L, int* T_out)
 {
     REQUIRE(x && ws, LUCE_EINVAL, "%s: null x/ws", who);
     REQUIRE(aligned(x, 16) && aligned(ws, 256), LUCE_EINVAL, "%s: x must be 16-byte and ws 256-byte aligned", who);
@@ -531,7 +601,6 @@ static int decode_step_impl(const luce_model* m, const StepSlot* slots, const in
             "%s: logits/argmax need vocab > 0 and the head weights", who);
     REQUIRE(!argmax || logits, LUCE_EINVAL, "%s: argmax needs the logits buffer", who);
     REQUIRE(!io.argmax_out || argmax, LUCE_EINVAL, "%s: argmax_out needs the argmax buffer", who);
-    const int H = m->hidden, Hq = m->n_q_heads, Hkv = m->n_kv_heads, D = m->head_dim, F = m->ffn;
     int T = 0, max_len = 1;
     for (int s = 0; s < n_seq; ++s) {
         T += rows_per_slot[s];
@@ -548,9 +617,21 @@ static int decode_step_impl(const luce_model* m, const StepSlot* slots, const in
     }
     REQUIRE(!logits || aligned(m->head_q, 32), LUCE_EINVAL, "%s: head weights must be 32-byte aligned", who);
 
+    layout_of(m, T, max_len, L);
+    REQUIRE(ws_bytes >= L->total, LUCE_ENOSPACE, "%s: workspace %zu bytes < %zu needed", who, ws_bytes, L->total);
+    *T_out = T;
+    return LUCE_OK;
+}
+
+static int decode_step_impl(const luce_model* m, const StepSlot* slots, const int32_t* rows_per_slot, int n_seq,
+                            float* x, float* logits, int32_t* argmax, void* ws, size_t ws_bytes, void* stream,
+                            const char* who, const HostIO& io = HostIO{nullptr, nullptr, nullptr})
+{
     luce_step_layout L;
-    layout_of(m, T, max_len, &L);
-    REQUIRE(ws_bytes >= L.total, LUCE_ENOSPACE, "%s: workspace %zu bytes < %zu needed", who, ws_bytes, L.total);
+    int T = 0;
+    const int rc = check_step(m, slots, rows_per_slot, n_seq, x, logits, argmax, ws, ws_bytes, who, io, &L, &T);
+    if (rc) return rc;
+    const int H = m->hidden, Hq = m->n_q_heads, Hkv = m->n_kv_heads, D = m->head_dim, F = m->ffn;
 
     char* wsb = (char*)ws;
     float* xn = (float*)(wsb + L.xn);
@@ -592,7 +673,11 @@ static int decode_step_impl(const luce_model* m, const StepSlot* slots, const in
         freq_theta = m->rope_theta;
     }
     cudaError_t e = cudaSuccess;
-    if (io.x_in && (e = cudaMemcpyAsync(x, io.x_in, (size_t)T * H * sizeof(float), cudaMemcpyHostToDevice, st)))
+    // input rows: read from mapped host memory by the first RMSNorm (which
+    // copies them into x), else copied in first
+    const bool in_mapped = io.x_in && io.x_in_dev;
+    if (io.x_in && !in_mapped &&
+        (e = step_copy(x, io.x_in, (size_t)T * H * sizeof(float), cudaMemcpyHostToDevice, st)))
         return cuda_status(e, who);
 
     const float scale = (float)(1.0 / sqrt((double)D));
@@ -642,7 +727,10 @@ static int decode_step_impl(const luce_model* m, const StepSlot* slots, const in
         }
         ar.total_chunks = c;
 
-        if ((e = launch_rmsnorm_quant(x, T, H, w.attn_norm, m->rms_eps, xn, xn_q, xn_d, false, st))) break;
+        const bool from_host = l == 0 && in_mapped;
+        if ((e = launch_rmsnorm_quant(from_host ? io.x_in_dev : x, T, H, w.attn_norm, m->rms_eps, xn, xn_q, xn_d,
+                                      false, st, from_host ? x : nullptr)))
+            break;
         if ((e = launch_qkv_rope(w.wqkv_q, (const __half*)w.wqkv_d, H, xn_q, xn_d, T, qkv, Hq, Hkv, pos, freq, q_rot,
                                  kv, st)))
             break;
@@ -671,10 +759,17 @@ static int decode_step_impl(const luce_model* m, const StepSlot* slots, const in
             return cuda_status(e, who);
         if (argmax && (e = launch_argmax(logits, T, m->vocab, argmax, st))) return cuda_status(e, who);
     }
-    if (io.x_out && (e = cudaMemcpyAsync(io.x_out, x, (size_t)T * H * sizeof(float), cudaMemcpyDeviceToHost, st)))
+    // results: stored into mapped host memory by one kernel, else copied back
+    HostIO out = io;
+    if (!out.outputs_resolved) resolve_outputs(&out, T, H);  // off the path to the first launch
+    float* xo = out.x_out ? out.x_out_dev : nullptr;
+    int32_t* ao = out.argmax_out ? out.argmax_out_dev : nullptr;
+    if ((xo || ao) && (e = launch_rows_to_host(x, (int64_t)T * H, xo, argmax, T, ao, st))) return cuda_status(e, who);
+    if (io.x_out && !xo &&
+        (e = step_copy(io.x_out, x, (size_t)T * H * sizeof(float), cudaMemcpyDeviceToHost, st)))
         return cuda_status(e, who);
-    if (io.argmax_out &&
-        (e = cudaMemcpyAsync(io.argmax_out, argmax, (size_t)T * sizeof(int32_t), cudaMemcpyDeviceToHost, st)))
+    if (io.argmax_out && !ao &&
+        (e = step_copy(io.argmax_out, argmax, (size_t)T * sizeof(int32_t), cudaMemcpyDeviceToHost, st)))
         return cuda_status(e, who);
     return ok();
 }
@@ -750,8 +845,274 @@ int luce_decode_step_host(const luce_model* m, const luce_slot* slots, const int
     StepSlot ss[LUCE_MAX_SEQ];
     const int rc = flat_slots(m, slots, rows_per_slot, n_seq, ss, who);
     if (rc) return rc;
-    return decode_step_impl(m, ss, rows_per_slot, n_seq, x, logits, argmax, ws, ws_bytes, stream, who,
-                            HostIO{x_in, x_out, argmax_out});
+    HostIO io{x_in, x_out, argmax_out};
+    int T = 0;
+    for (int s = 0; s < n_seq; ++s) T += rows_per_slot[s];
+    resolve_input(&io, T, m->hidden);
+    return decode_step_impl(m, ss, rows_per_slot, n_seq, x, logits, argmax, ws, ws_bytes, stream, who, io);
+}
+
+// ------------------------------------------------------------ step graph
+//
+// The step's launches and copies, recorded (not issued) by decode_step_impl,
+// become the nodes of one CUDA graph: built once by capturing the recorded
+// launches on a private stream, then, for every later step whose record has
+// the same sequence of nodes (the same kernel count and copies), refreshed
+// node by node - only the kernel nodes whose function, grid, block or
+// argument bytes changed (the positions, K/V destinations and attention rows
+// follow the slots' lengths) - and launched with one call.  A record with a
+// different sequence (an attention kind appearing or leaving) is captured
+// anew.  The graph's kernels are the very kernels, with the very arguments,
+// that luce_decode_step_host would launch, so the outputs are its bits.
+
+}  // extern "C"
+
+struct luce_step_graph {
+    const luce_model* m;
+    luce_slot slots[LUCE_MAX_SEQ];
+    int32_t rows[LUCE_MAX_SEQ];
+    int n_seq;
+    float* x;
+    float* logits;
+    int32_t* argmax;
+    void* ws;
+    size_t ws_bytes;
+    HostIO io;
+    bool io_resolved = false;    // io's device views are looked up at the first run
+    cudaStream_t cap = nullptr;  // private capture stream
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    std::vector<cudaGraphNode_t> nodes;  // graph nodes in launch order
+    LaunchLog live;                      // the record the executable graph holds
+    LaunchLog next;                      // this step's record
+    int kernels = 0;
+    int64_t captures = 0, node_updates = 0;
+};
+
+namespace {
+
+void release_graph(luce_step_graph* g)
+{
+    if (g->exec) cudaGraphExecDestroy(g->exec);
+    if (g->graph) cudaGraphDestroy(g->graph);
+    g->exec = nullptr;
+    g->graph = nullptr;
+    g->nodes.clear();
+}
+
+bool same_kernel(const LaunchRec& a, const LaunchRec& b)
+{
+    return a.func == b.func && a.grid.x == b.grid.x && a.grid.y == b.grid.y && a.grid.z == b.grid.z &&
+           a.block.x == b.block.x && a.block.y == b.block.y && a.block.z == b.block.z && a.smem == b.smem &&
+           a.nargs == b.nargs && a.nbytes == b.nbytes && memcmp(a.off, b.off, sizeof(uint16_t) * a.nargs) == 0 &&
+           memcmp(a.args, b.args, (size_t)a.nbytes) == 0;
+}
+
+// The same sequence of nodes: equal length, kernels where kernels were, and
+// the same copies.
+bool same_nodes(const LaunchLog& a, const LaunchLog& b)
+{
+    if (a.recs.size() != b.recs.size()) return false;
+    for (size_t i = 0; i < a.recs.size(); ++i) {
+        const LaunchRec &x = a.recs[i], &y = b.recs[i];
+        if (x.copy != y.copy) return false;
+        if (x.copy && (x.dst != y.dst || x.src != y.src || x.bytes != y.bytes || x.dir != y.dir)) return false;
+    }
+    return true;
+}
+
+void argv_of(LaunchRec& r, void** argv)
+{
+    for (int i = 0; i < r.nargs; ++i) argv[i] = r.args + r.off[i];
+}
+
+// Capture g->next into a new executable graph (the old one is released
+// first); the nodes are then listed by walking the chain from its root.
+cudaError_t capture(luce_step_graph* g)
+{
+    release_graph(g);
+    cudaError_t e = cudaSuccess;
+    if (!g->cap && (e = cudaStreamCreateWithFlags(&g->cap, cudaStreamNonBlocking))) return e;
+    if ((e = cudaStreamBeginCapture(g->cap, cudaStreamCaptureModeThreadLocal))) return e;
+    cudaError_t le = cudaSuccess;
+    for (LaunchRec& r : g->next.recs) {
+        if (r.copy) {
+            le = cudaMemcpyAsync(r.dst, r.src, r.bytes, r.dir, g->cap);
+        } else {
+            void* argv[LaunchRec::kMaxArgs];
+            argv_of(r, argv);
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = r.grid;
+            cfg.blockDim = r.block;
+            cfg.dynamicSmemBytes = r.smem;
+            cfg.stream = g->cap;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            le = cudaLaunchKernelExC(&cfg, r.func, argv);
+        }
+        if (le) break;
+    }
+    cudaGraph_t graph = nullptr;
+    e = cudaStreamEndCapture(g->cap, &graph);
+    if (le || e) {
+        if (graph) cudaGraphDestroy(graph);
+        return le ? le : e;
+    }
+    g->graph = graph;
+    size_t n = 1;
+    cudaGraphNode_t node = nullptr;
+    if ((e = cudaGraphGetRootNodes(graph, &node, &n))) return e;
+    while (n == 1 && node) {
+        g->nodes.push_back(node);
+        cudaGraphNode_t dep[2] = {nullptr, nullptr};
+        cudaGraphEdgeData ed[2];
+        n = 2;
+        if ((e = cudaGraphNodeGetDependentNodes(node, dep, ed, &n))) return e;
+        node = n == 1 ? dep[0] : nullptr;
+    }
+    if (n > 1 || g->nodes.size() != g->next.recs.size()) return cudaErrorInvalidValue;
+    for (size_t i = 0; i < g->nodes.size(); ++i) {
+        cudaGraphNodeType t;
+        if ((e = cudaGraphNodeGetType(g->nodes[i], &t))) return e;
+        if (t != (g->next.recs[i].copy ? cudaGraphNodeTypeMemcpy : cudaGraphNodeTypeKernel))
+            return cudaErrorInvalidValue;
+    }
+    if ((e = cudaGraphInstantiate(&g->exec, graph, 0))) return e;
+    g->kernels = 0;
+    for (const LaunchRec& r : g->next.recs) g->kernels += r.copy ? 0 : 1;
+    ++g->captures;
+    return cudaSuccess;
+}
+
+// Refresh the executable graph from g->next, node by node; false when a node
+// refused the new parameters (the caller then captures anew).
+bool refresh(luce_step_graph* g)
+{
+    for (size_t i = 0; i < g->next.recs.size(); ++i) {
+        LaunchRec& r = g->next.recs[i];
+        if (r.copy || same_kernel(r, g->live.recs[i])) continue;
+        void* argv[LaunchRec::kMaxArgs];
+        argv_of(r, argv);
+        cudaKernelNodeParams p = {};
+        p.func = const_cast<void*>(r.func);
+        p.gridDim = r.grid;
+        p.blockDim = r.block;
+        p.sharedMemBytes = (unsigned)r.smem;
+        p.kernelParams = argv;
+        p.extra = nullptr;
+        if (cudaGraphExecKernelNodeSetParams(g->exec, g->nodes[i], &p) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return false;
+        }
+        ++g->node_updates;
+    }
+    return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+int luce_step_graph_create(const luce_model* m, const luce_slot* slots, const int32_t* rows_per_slot, int n_seq,
+                           const float* x_in, float* x, float* x_out, float* logits, int32_t* argmax,
+                           int32_t* argmax_out, void* ws, size_t ws_bytes, luce_step_graph** out)
+{
+    const char* who = "step_graph_create";
+    REQUIRE(out, LUCE_EINVAL, "%s: null out", who);
+    *out = nullptr;
+    REQUIRE(x_in, LUCE_EINVAL, "%s: null x_in", who);
+    StepSlot ss[LUCE_MAX_SEQ];
+    int rc = flat_slots(m, slots, rows_per_slot, n_seq, ss, who);
+    if (rc) return rc;
+    luce_step_layout L;
+    int T = 0;
+    if ((rc = check_step(m, ss, rows_per_slot, n_seq, x, logits, argmax, ws, ws_bytes, who,
+                         HostIO{x_in, x_out, argmax_out}, &L, &T)))
+        return rc;
+    luce_step_graph* g = new (std::nothrow) luce_step_graph();
+    REQUIRE(g, LUCE_ENOSPACE, "%s: out of host memory", who);
+    g->m = m;
+    for (int s = 0; s < n_seq; ++s) {
+        g->slots[s] = slots[s];
+        g->rows[s] = rows_per_slot[s];
+    }
+    g->n_seq = n_seq;
+    g->x = x;
+    g->logits = logits;
+    g->argmax = argmax;
+    g->ws = ws;
+    g->ws_bytes = ws_bytes;
+    g->io = HostIO{x_in, x_out, argmax_out};
+    const size_t per_step = 4 + 12 * (size_t)m->n_layers;
+    g->live.recs.reserve(per_step);
+    g->next.recs.reserve(per_step);
+    *out = g;
+    return ok();
+}
+
+int luce_step_graph_run(luce_step_graph* g, const int32_t* lens, void* stream)
+{
+    const char* who = "step_graph_run";
+    REQUIRE(g && lens, LUCE_EINVAL, "%s: null graph/lens", who);
+    luce_slot sl[LUCE_MAX_SEQ];
+    for (int s = 0; s < g->n_seq; ++s) {
+        sl[s] = g->slots[s];
+        sl[s].len = lens[s];
+    }
+    StepSlot ss[LUCE_MAX_SEQ];
+    int rc = flat_slots(g->m, sl, g->rows, g->n_seq, ss, who);
+    if (rc) return rc;
+    if (!g->io_resolved) {
+        int T = 0;
+        for (int s = 0; s < g->n_seq; ++s) T += g->rows[s];
+        resolve_input(&g->io, T, g->m->hidden);
+        resolve_outputs(&g->io, T, g->m->hidden);
+        g->io_resolved = true;
+    }
+    REQUIRE((!g->io.x_in || g->io.x_in_dev) && (!g->io.x_out || g->io.x_out_dev) &&
+                (!g->io.argmax_out || g->io.argmax_out_dev),
+            LUCE_EUNSUPPORTED, "%s: the host buffers must be page-locked memory mapped into the device's space",
+            who);
+    g->next.recs.clear();
+    g->next.overflow = false;
+    t_launch_log = &g->next;
+    rc = decode_step_impl(g->m, ss, g->rows, g->n_seq, g->x, g->logits, g->argmax, g->ws, g->ws_bytes, stream, who,
+                          g->io);
+    t_launch_log = nullptr;
+    REQUIRE(!g->next.overflow, LUCE_EUNSUPPORTED, "%s: a launch has more arguments than a record holds", who);
+    if (rc) return rc;
+    cudaError_t e = cudaSuccess;
+    if (!g->exec || !same_nodes(g->live, g->next) || !refresh(g)) {
+        if ((e = capture(g))) {
+            release_graph(g);
+            return cuda_status(e, who);
+        }
+    }
+    std::swap(g->live, g->next);
+    if ((e = cudaGraphLaunch(g->exec, (cudaStream_t)stream))) return cuda_status(e, who);
+    count_launches(g->kernels);
+    return ok();
+}
+
+int luce_step_graph_stats(const luce_step_graph* g, int64_t* captures, int64_t* node_updates, int32_t* kernels)
+{
+    REQUIRE(g, LUCE_EINVAL, "step_graph_stats: null graph");
+    if (captures) *captures = g->captures;
+    if (node_updates) *node_updates = g->node_updates;
+    if (kernels) *kernels = g->kernels;
+    return ok();
+}
+
+int luce_step_graph_destroy(luce_step_graph* g)
+{
+    if (!g) return ok();
+    release_graph(g);
+    if (g->cap) cudaStreamDestroy(g->cap);
+    delete g;
+    return ok();
 }
 
 int luce_decode_step_paged(const luce_model* m, const luce_paged_slot* slots, const int32_t* rows_per_slot,

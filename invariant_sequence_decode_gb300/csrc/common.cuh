@@ -10,6 +10,9 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <string.h>
+
+#include <vector>
 
 #define LUCE_QK 32
 
@@ -26,10 +29,81 @@ namespace luce {
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// A launch written down instead of issued.  While a thread's t_launch_log is
+// set, launch_pdl_smem appends the kernel, its shape and a copy of its
+// arguments (each at its own alignment, the gaps zeroed, so two records of
+// equal launches compare equal byte for byte) to the log, and the host-device
+// copies of the decode step go there too; the step graph (api.cu) builds a
+// CUDA graph from such a log and refreshes its nodes from the next one.
+struct LaunchRec {
+    static constexpr int kMaxArgs = 24;
+    static constexpr int kArgBytes = 3072;
+    LaunchRec() {}  // fields are set by the recorder; the argument bytes are never zero-filled in bulk
+    bool copy;  // a cudaMemcpyAsync (dst, src, bytes, dir), not a kernel
+    const void* func;
+    dim3 grid, block;
+    size_t smem;
+    int nargs, nbytes;
+    uint16_t off[kMaxArgs];
+    void* dst;
+    const void* src;
+    size_t bytes;
+    cudaMemcpyKind dir;
+    alignas(64) unsigned char args[kArgBytes];
+};
+
+struct LaunchLog {
+    std::vector<LaunchRec> recs;
+    bool overflow = false;  // a launch had more arguments or bytes than a record holds
+};
+
+extern thread_local LaunchLog* t_launch_log;
+
+template <typename A>
+static inline bool rec_put(LaunchRec& r, int& off, const A& a)
+{
+    const int at = (off + (int)alignof(A) - 1) & ~((int)alignof(A) - 1);
+    if (r.nargs >= LaunchRec::kMaxArgs || at + (int)sizeof(A) > LaunchRec::kArgBytes) return false;
+    memset(r.args + off, 0, (size_t)(at - off));
+    memcpy(r.args + at, &a, sizeof(A));
+    r.off[r.nargs++] = (uint16_t)at;
+    off = at + (int)sizeof(A);
+    return true;
+}
+
+template <typename... KArgs>
+static inline cudaError_t rec_kernel(LaunchLog* log, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                     const KArgs&... args)
+{
+    log->recs.emplace_back();
+    LaunchRec& r = log->recs.back();
+    r.copy = false;
+    r.func = reinterpret_cast<const void*>(kernel);
+    r.grid = grid;
+    r.block = block;
+    r.smem = smem;
+    r.nargs = 0;
+    r.dst = nullptr;
+    r.src = nullptr;
+    r.bytes = 0;
+    r.dir = cudaMemcpyDefault;
+    int off = 0;
+    bool ok = true;
+    ((ok = ok && rec_put(r, off, args)), ...);
+    r.nbytes = off;
+    if (!ok) {
+        log->overflow = true;
+        return cudaErrorInvalidValue;
+    }
+    return cudaSuccess;
+}
+
 template <typename... KArgs, typename... Args>
 static inline cudaError_t launch_pdl_smem(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                                           cudaStream_t s, Args... args)
 {
+    if (LaunchLog* log = t_launch_log)
+        return rec_kernel<KArgs...>(log, kernel, grid, block, smem, static_cast<KArgs>(args)...);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;

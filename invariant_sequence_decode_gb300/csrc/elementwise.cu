@@ -55,7 +55,10 @@ cudaError_t launch_quantize(const float* x, int T, int K, int64_t ldx, int8_t* q
 // forms the row's sum in full, and then normalises and quantizes every second
 // block (from block k % 2) of its first chain, 8 (k / 2) + p, which spreads
 // the per-element divisions over several SMs with few registers per CTA.  gamma
-// is read before the wait on the previous kernel, x once.
+// is read before the wait on the previous kernel, x once.  xcopy (nullable):
+// each CTA also stores the raw x values of the blocks it normalises there, so
+// the CTAs of a row together copy the row (the decode step reads its input
+// rows straight from mapped host memory this way).
 constexpr int kNormSlices = 8;
 constexpr int kNormChains = 4 * kNormSlices;
 constexpr int kNormCtasPerRow = 8;
@@ -65,7 +68,7 @@ static_assert(kNormChains * 2 == kNormCtasPerRow * (kNormThreads / 32), "half a 
 template <int MAXK, bool HALF>  // MAXK: blocks per chain held in registers (0: loop over x)
 __global__ void __launch_bounds__(kNormThreads)
 rmsnorm_quant_kernel(const float* __restrict__ x, int H, const float* __restrict__ gamma, float eps,
-                     float* __restrict__ xn, int8_t* __restrict__ q, void* d)
+                     float* __restrict__ xn, int8_t* __restrict__ q, void* d, float* __restrict__ xcopy)
 {
     constexpr int NJ = kNormChains / (kNormThreads / 32);  // chains per warp
     constexpr int KR = MAXK > 0 ? MAXK : 1;
@@ -138,7 +141,7 @@ rmsnorm_quant_kernel(const float* __restrict__ x, int H, const float* __restrict
         // every owned block's quantization computed branch-free (the shuffles
         // and divisions of the blocks interleave), the stores predicated
         constexpr int KH = (KR + 1) / 2;
-        float vn[KH];
+        float vn[KH], raw[KH];
         Q8Lane qz[KH];
 #pragma unroll
         for (int h = 0; h < KH; ++h) {
@@ -147,6 +150,7 @@ rmsnorm_quant_kernel(const float* __restrict__ x, int H, const float* __restrict
             const int m1 = 2 * h + 1 < KR ? 2 * h + 1 : dummy;
             const float e = half ? (2 * h + 1 < KR ? xv[0][m1] : 0.0f) : xv[0][2 * h];
             const float g = half ? (2 * h + 1 < KR ? gv[m1] : 0.0f) : gv[2 * h];
+            raw[h] = e;
             vn[h] = __fmul_rn(__fmul_rn(e, r), g);
         }
 #pragma unroll
@@ -156,6 +160,7 @@ rmsnorm_quant_kernel(const float* __restrict__ x, int H, const float* __restrict
             const int m = 2 * h + half, b = first(vo) + 4 * m;
             if (m < KR && b < end(vo)) {
                 const int i = b * 32 + lane;
+                if (xcopy) xcopy[(size_t)t * H + i] = raw[h];
                 xn[(size_t)t * H + i] = vn[h];
                 q[(size_t)t * H + i] = (int8_t)qz[h].code;
                 if (lane == 0) q8_store_scale<HALF>(d, (size_t)t * nb + b, qz[h].s);
@@ -164,7 +169,9 @@ rmsnorm_quant_kernel(const float* __restrict__ x, int H, const float* __restrict
     } else {
         for (int b = first(vo) + 4 * half; b < end(vo); b += 8) {
             const int i = b * 32 + lane;
-            const float vn = __fmul_rn(__fmul_rn(xr[i], r), gamma[i]);
+            const float e = xr[i];
+            if (xcopy) xcopy[(size_t)t * H + i] = e;
+            const float vn = __fmul_rn(__fmul_rn(e, r), gamma[i]);
             xn[(size_t)t * H + i] = vn;
             const int code = q8_quantize_store<HALF>(vn, d, (size_t)t * nb + b, lane == 0);
             q[(size_t)t * H + i] = (int8_t)code;
@@ -174,21 +181,49 @@ rmsnorm_quant_kernel(const float* __restrict__ x, int H, const float* __restrict
 
 template <bool HALF>
 static cudaError_t launch_rmsnorm_quant_t(const float* x, int T, int H, const float* gamma, float eps, float* xn,
-                                         int8_t* q, void* d, cudaStream_t s)
+                                         int8_t* q, void* d, float* xcopy, cudaStream_t s)
 {
     const int bpc = ((H >> 5) + kNormSlices - 1) / kNormSlices;
     const int per_chain = (bpc + 3) / 4;
     const dim3 grid(kNormCtasPerRow, T), block(kNormThreads);
-    if (per_chain <= 8) return launch_pdl(rmsnorm_quant_kernel<8, HALF>, grid, block, s, x, H, gamma, eps, xn, q, d);
-    if (per_chain <= 16) return launch_pdl(rmsnorm_quant_kernel<16, HALF>, grid, block, s, x, H, gamma, eps, xn, q, d);
-    return launch_pdl(rmsnorm_quant_kernel<0, HALF>, grid, block, s, x, H, gamma, eps, xn, q, d);
+    if (per_chain <= 8)
+        return launch_pdl(rmsnorm_quant_kernel<8, HALF>, grid, block, s, x, H, gamma, eps, xn, q, d, xcopy);
+    if (per_chain <= 16)
+        return launch_pdl(rmsnorm_quant_kernel<16, HALF>, grid, block, s, x, H, gamma, eps, xn, q, d, xcopy);
+    return launch_pdl(rmsnorm_quant_kernel<0, HALF>, grid, block, s, x, H, gamma, eps, xn, q, d, xcopy);
 }
 
 cudaError_t launch_rmsnorm_quant(const float* x, int T, int H, const float* gamma, float eps, float* xn, int8_t* q,
-                                 void* d, bool half_scale, cudaStream_t s)
+                                 void* d, bool half_scale, cudaStream_t s, float* xcopy)
 {
-    const cudaError_t e = half_scale ? launch_rmsnorm_quant_t<true>(x, T, H, gamma, eps, xn, q, d, s)
-                                     : launch_rmsnorm_quant_t<false>(x, T, H, gamma, eps, xn, q, d, s);
+    const cudaError_t e = half_scale ? launch_rmsnorm_quant_t<true>(x, T, H, gamma, eps, xn, q, d, xcopy, s)
+                                     : launch_rmsnorm_quant_t<false>(x, T, H, gamma, eps, xn, q, d, xcopy, s);
+    count_launches(1);
+    return e;
+}
+
+// The step's results to the host through mapped (page-locked, device-visible)
+// memory: x [n] floats to x_out and am [T] to am_out (either nullable), with
+// plain stores that cross the host link inside the kernel.
+__global__ void __launch_bounds__(256)
+rows_to_host_kernel(const float4* __restrict__ x, int n4, float4* __restrict__ x_out, const int32_t* __restrict__ am,
+                    int T, int32_t* __restrict__ am_out)
+{
+    pdl_trigger();
+    pdl_wait();
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (x_out && i < n4) x_out[i] = x[i];
+    if (am_out && i < T) am_out[i] = am[i];
+}
+
+cudaError_t launch_rows_to_host(const float* x, int64_t n, float* x_out, const int32_t* am, int T, int32_t* am_out,
+                                cudaStream_t s)
+{
+    const int n4 = (int)(n / 4);
+    const int work = n4 > T ? n4 : T;
+    const cudaError_t e = launch_pdl(rows_to_host_kernel, dim3((unsigned)((work + 255) / 256)), dim3(256), s,
+                                     reinterpret_cast<const float4*>(x), n4, reinterpret_cast<float4*>(x_out), am, T,
+                                     am_out);
     count_launches(1);
     return e;
 }

@@ -137,8 +137,14 @@ cudaError_t launch_attention(const float* q, int64_t ldq, const AttnRows& rows, 
                              float scale, float* part, float* out, int64_t ldo,
                              int8_t* out_q, float* out_d, cudaStream_t s);
 
+// xcopy (nullable): the CTAs also copy the rows of x there (x may then be a
+// mapped host pointer).
 cudaError_t launch_rmsnorm_quant(const float* x, int T, int H, const float* gamma, float eps, float* xn, int8_t* q,
-                                 void* d, bool half_scale, cudaStream_t s);
+                                 void* d, bool half_scale, cudaStream_t s, float* xcopy = nullptr);
+// x [n] (n a multiple of 4, 16-byte aligned) to x_out and am [T] to am_out,
+// both mapped host memory (either nullable).
+cudaError_t launch_rows_to_host(const float* x, int64_t n, float* x_out, const int32_t* am, int T, int32_t* am_out,
+                                cudaStream_t s);
 
 cudaError_t launch_swiglu_quant(const float* gu, int T, int F, float* h, int8_t* q, void* d, bool half_scale,
                                 cudaStream_t s);

@@ -186,6 +186,41 @@ def test_decode_step_host_refusals(lib):
     assert host(ctypes.byref(m), s, rows([1, 1]), 2, xin, P, None, None, None, out, P, big, None) == luce.LUCE_EINVAL
 
 
+def test_step_graph_create_validates_and_makes_no_cuda_call(lib):
+    """luce_step_graph_create checks what luce_decode_step_host checks and
+    touches no device; run refuses bad lengths before any CUDA call; destroy
+    of a never-run object (and of NULL) needs no device either."""
+    m, _keep = fake_model()
+    big = 1 << 40
+    create = lib.luce_step_graph_create
+    s = slots([(3, 64), (3, 64)])
+    xin = (ctypes.c_float * 16)()
+    h = ctypes.c_void_p()
+    assert create(ctypes.byref(m), s, rows([1, 1]), 2, None, P, None, None, None, None, P, big,
+                  ctypes.byref(h)) == luce.LUCE_EINVAL and not h.value
+    assert create(ctypes.byref(m), s, rows([1, 5]), 2, xin, P, None, None, None, None, P, big,
+                  ctypes.byref(h)) == luce.LUCE_EINVAL
+    assert create(ctypes.byref(m), s, rows([1, 1]), 2, xin, P, None, None, None, None, P, 1024,
+                  ctypes.byref(h)) == luce.LUCE_ENOSPACE
+    assert create(ctypes.byref(m), s, rows([1, 1]), 2, xin, P, None, P, None, None, P, big,
+                  ctypes.byref(h)) == luce.LUCE_EINVAL  # logits without a head
+    assert create(ctypes.byref(m), s, rows([1, 1]), 2, xin, P, None, None, None, None, P, big, None) == luce.LUCE_EINVAL
+    assert create(ctypes.byref(m), s, rows([1, 1]), 2, xin, P, None, None, None, None, P, big,
+                  ctypes.byref(h)) == luce.LUCE_OK and h.value
+    c, u, k = ctypes.c_int64(-1), ctypes.c_int64(-1), ctypes.c_int32(-1)
+    assert lib.luce_step_graph_stats(h, ctypes.byref(c), ctypes.byref(u), ctypes.byref(k)) == luce.LUCE_OK
+    assert (c.value, u.value, k.value) == (0, 0, 0)
+    run = lib.luce_step_graph_run
+    assert run(h, None, None) == luce.LUCE_EINVAL
+    assert run(h, (ctypes.c_int32 * 2)(3, 64), None) == luce.LUCE_EINVAL  # len + rows > cap
+    assert "exceeds cap" in status_msg(lib)
+    assert run(h, (ctypes.c_int32 * 2)(-1, 3), None) == luce.LUCE_EINVAL
+    assert lib.luce_step_graph_stats(h, ctypes.byref(c), None, None) == luce.LUCE_OK and c.value == 0
+    assert lib.luce_step_graph_destroy(h) == luce.LUCE_OK
+    assert lib.luce_step_graph_destroy(None) == luce.LUCE_OK
+    assert lib.luce_step_graph_stats(None, None, None, None) == luce.LUCE_EINVAL
+
+
 def test_step_layout_is_monotone_and_part_is_last(lib):
     m, _keep = fake_model()
     lay = luce.StepLayoutC()
