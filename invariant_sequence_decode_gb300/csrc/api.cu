@@ -740,10 +740,17 @@ static int decode_step_impl(const luce_model* m, const StepSlot* slots, const in
         if ((e = launch_matvec(w.wo_q, (const __half*)w.wo_d, H, Hq * D, attn_q, attn_d, T, x1, H, x, H, st)))
             break;
         if ((e = launch_rmsnorm_quant(x1, T, H, w.ffn_norm, m->rms_eps, xn2, xn2_q, xn2_d, false, st))) break;
-        if ((e = launch_matvec(w.wgu_q, (const __half*)w.wgu_d, 2 * F, H, xn2_q, xn2_d, T, gu, 2 * F, nullptr, 0,
-                               st)))
-            break;
-        if ((e = launch_swiglu_quant(gu, T, F, hh, h_q, h_d, false, st))) break;
+        // gate||up with SwiGLU and its codes in one launch where the fused ring
+        // takes the shape, else the projection and then the SwiGLU kernel
+        e = launch_gateup_swiglu_tma(w.wgu_q, (const __half*)w.wgu_d, F, H, xn2_q, xn2_d, T, gu, hh, h_q, h_d, st);
+        if (e == cudaErrorNotSupported) {
+            (void)cudaGetLastError();
+            if ((e = launch_matvec(w.wgu_q, (const __half*)w.wgu_d, 2 * F, H, xn2_q, xn2_d, T, gu, 2 * F, nullptr, 0,
+                                   st)))
+                break;
+            e = launch_swiglu_quant(gu, T, F, hh, h_q, h_d, false, st);
+        }
+        if (e) break;
         if ((e = launch_matvec(w.wdown_q, (const __half*)w.wdown_d, H, F, h_q, h_d, T, x, H, x1, H, st))) break;
     }
     if (e != cudaSuccess) return cuda_status(e, who);

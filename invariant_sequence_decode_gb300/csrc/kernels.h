@@ -88,6 +88,14 @@ cudaError_t launch_matvec_path(int path, const int8_t* wq, const __half* wd, int
 // The fused q|k|v + RoPE + K/V-append projection on the TMA ring (1..8 rows
 // in one launch, 13..16 in two); cudaErrorNotSupported, with nothing
 // launched, otherwise.
+// The step's gate||up projection (W = [gate; up], 2F x K) with SwiGLU and
+// its q8_0 codes (fp32 scales) in the epilogue: gu [T][2F] as the plain
+// projection, h [T][F], hq [T][F], hd [T][F/32] as swiglu_quant_kernel.
+// cudaErrorNotSupported when the fused ring does not take the shape (the
+// caller then runs the two launches).
+cudaError_t launch_gateup_swiglu_tma(const int8_t* wq, const __half* wd, int F, int K, const int8_t* aq,
+                                     const float* ad, int T, float* gu, float* h, int8_t* hq, float* hd,
+                                     cudaStream_t s);
 cudaError_t launch_qkv_rope_tma(const int8_t* wq, const __half* wd, int K, const int8_t* aq, const float* ad, int T,
                                 float* qkv, int Hq, int Hkv, const RowPos& pos, const RopeFreq& f, float* q_rot,
                                 const KvRows& kv, cudaStream_t s);

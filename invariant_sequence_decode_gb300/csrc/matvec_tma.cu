@@ -385,6 +385,89 @@ q8_qkv_rope_tma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_cons
     }
 }
 
+// The decode step's gate||up projection (gate rows [0, F), up rows [F, 2F)
+// of W) with SwiGLU and its q8_0 quantization in the epilogue, 1..4
+// activation rows: the same chains.  A unit is the 32 features f0 .. f0 + 31
+// (f0 = 32u) and its four groups hold gate rows f0 + 8i .. f0 + 8i + 7
+// (quads 0, 1) and the up rows F + the same features (quads 2, 3), i = 0..3,
+// so the CTA that finishes a feature holds its gate and its up value: it
+// stores both to gu as the plain projection would, h = silu(g) * u, and once
+// the unit's 32 features are in, warp t quantizes token t's block of h -
+// exactly swiglu_quant_kernel's arithmetic.  Persistent: CTA b owns units
+// [b*U/grid, (b+1)*U/grid) of the U = F/32; mdp has an 8-row scale box.
+template <int T, int S, bool BIAS>
+__global__ void __launch_bounds__(kRingThreads)
+q8_gateup_swiglu_tma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mdp,
+                            const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mad, int F,
+                            int K, float* __restrict__ gu, float* __restrict__ h, int8_t* __restrict__ hq,
+                            float* __restrict__ hd)
+{
+    constexpr int G = 4;
+    using L = RingLayout<T, G, S>;
+    extern __shared__ uint8_t smem_raw[];
+    const RingSmem<T, G, S> R(smem_raw);
+    __shared__ float hb[T][32];  // the unit's h values, token by token
+    pdl_trigger();
+    const int nb = K >> 5, nj = (nb + 31) >> 5;
+    const int U = F >> 5;
+    const int u0 = (int)((int64_t)blockIdx.x * U / gridDim.x);
+    const int u1 = (int)((int64_t)(blockIdx.x + 1) * U / gridDim.x);
+    const int ngrp = 4 * (u1 - u0);
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+    if (tid == 0) R.init();
+    __syncthreads();
+
+    if (w == 4) {
+        if (lane != 0) return;
+        ring_produce<T, G, S>(
+            R, ngrp * nj, nj, &ma, &mad,
+            [&](int it, uint8_t* slot, uint64_t* bar) {
+                const int j = it % nj, gi = it / nj;
+                const int f = 32 * (u0 + gi / 4) + 8 * (gi % 4);
+                tma_load_3d(slot, &mw, 0, 4 * j, f, bar);
+                tma_load_3d(slot + 4096, &mw, 0, 4 * j, f + 4, bar);
+                tma_load_3d(slot + 2 * 4096, &mw, 0, 4 * j, F + f, bar);
+                tma_load_3d(slot + 3 * 4096, &mw, 0, 4 * j, F + f + 4, bar);
+                tma_load_2d(slot + L::W, &mdp, 32 * j, f, bar);
+                tma_load_2d(slot + L::W + 8 * 64, &mdp, 32 * j, F + f, bar);
+            },
+            [&](int) { return G * 4096 + L::D; });
+        return;
+    }
+
+    pdl_wait();  // gu, h and the codes may be touched by earlier kernels
+    const int r = lane >> 3, c = (lane & 7) + 8 * w;
+    bool ok = true;
+    int it = 0;
+    for (int gi = 0; gi < ngrp; ++gi) {
+        float acc[G][T];
+        ring_chains<T, G, S, BIAS>(R, it, nj, nb, r, c, lane, acc, ok);
+        // two chain buffers, so one barrier per group separates writers and readers
+        float* pp = R.part + (L::PB == 2 ? (gi & 1) * (L::ROWS * T * 33) : 0);
+        if (L::PB == 1 && gi > 0) asm volatile("bar.sync 1, 128;" ::: "memory");  // last group's readers are done
+        store_chains<T, G>(pp, r, c, acc);
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        const int fu = 32 * (u0 + gi / 4), i = gi % 4;
+        if (tid < 8 * T && ok) {  // feature fu + 8i + p of token t: local rows p (gate) and 8 + p (up)
+            const int p = tid / T, t = tid - (tid / T) * T;
+            const float g = q8_butterfly(pp + (p * T + t) * 33);
+            const float u = q8_butterfly(pp + ((8 + p) * T + t) * 33);
+            gu[(size_t)t * 2 * F + fu + 8 * i + p] = g;
+            gu[(size_t)t * 2 * F + F + fu + 8 * i + p] = u;
+            hb[t][8 * i + p] = silu_mul(g, u);
+        }
+        if (i == 3) {  // the unit's 32 features are in: warp t quantizes token t's block
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (w < T && ok) {
+                const float v = hb[w][lane];
+                h[(size_t)w * F + fu + lane] = v;
+                const int code = q8_quantize_store<false>(v, hd, (size_t)w * U + (fu >> 5), lane == 0);
+                hq[(size_t)w * F + fu + lane] = (int8_t)code;
+            }
+        }
+    }
+}
+
 namespace {
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
@@ -630,6 +713,51 @@ cudaError_t launch_qkv_rope_tma(const int8_t* wq, const __half* wd, int K, const
     if (e != cudaSuccess) return e;
     return qkv_ring_rows(wq, wd, K, aq + (size_t)8 * K, ad + (size_t)8 * (K / 32), T - 8, qkv + (size_t)8 * N, Hq, Hkv,
                          pos_hi, f, q_rot + (size_t)8 * Hq * kHeadDim, kv_hi, s);
+}
+
+namespace {
+
+constexpr int kGateUpSlots = 4;  // two CTAs per SM at most, so one more slot than the plain ring
+
+template <int T, bool BIAS>
+cudaError_t launch_gateup_t(const CUtensorMap& mw, const CUtensorMap& mdp, const CUtensorMap& ma,
+                            const CUtensorMap& mad, int F, int K, float* gu, float* h, int8_t* hq, float* hd,
+                            int grid, cudaStream_t s)
+{
+    using L = RingLayout<T, 4, kGateUpSlots>;
+    static std::atomic<bool> done[kMaxDevices];
+    cudaError_t e = set_smem_once(q8_gateup_swiglu_tma_kernel<T, kGateUpSlots, BIAS>, L::SMEM, done);
+    if (e == cudaSuccess)
+        e = launch_pdl_smem(q8_gateup_swiglu_tma_kernel<T, kGateUpSlots, BIAS>, dim3(grid), dim3(kRingThreads),
+                            L::SMEM, s, mw, mdp, ma, mad, F, K, gu, h, hq, hd);
+    count_launches(1);
+    return e;
+}
+
+}  // namespace
+
+// The fused gate||up + SwiGLU + q8_0 launch for 1..4 rows: four slots, the
+// units spread so that every CTA gets the same number (a grid of U/k CTAs, k
+// the smallest count that keeps three CTAs per SM or fewer).  Not taken (the
+// caller then launches the projection and the SwiGLU kernel) for other row
+// counts, shapes the ring does not take or F not a multiple of 32.
+cudaError_t launch_gateup_swiglu_tma(const int8_t* wq, const __half* wd, int F, int K, const int8_t* aq,
+                                     const float* ad, int T, float* gu, float* h, int8_t* hq, float* hd,
+                                     cudaStream_t s)
+{
+    const int sms = sm_count();
+    if (sms <= 0 || T < 1 || T > 4 || F % 32 != 0 || F < 32) return cudaErrorNotSupported;
+    CUtensorMap mw, mdp, ma, mad;
+    if (!ring_maps(wq, wd, 2 * F, K, aq, ad, T, 8, &mw, &mdp, &ma, &mad)) return cudaErrorNotSupported;
+    const int U = F / 32;
+    const int k = (U + kRingCtasPerSm * sms - 1) / (kRingCtasPerSm * sms);
+    const int grid = (U + k - 1) / k;
+    switch (T) {
+        case 1: return launch_gateup_t<1, true>(mw, mdp, ma, mad, F, K, gu, h, hq, hd, grid, s);
+        case 2: return launch_gateup_t<2, false>(mw, mdp, ma, mad, F, K, gu, h, hq, hd, grid, s);
+        case 3: return launch_gateup_t<3, false>(mw, mdp, ma, mad, F, K, gu, h, hq, hd, grid, s);
+        default: return launch_gateup_t<4, false>(mw, mdp, ma, mad, F, K, gu, h, hq, hd, grid, s);
+    }
 }
 
 cudaError_t launch_wait_expiry(uint64_t limit_ns, cudaStream_t s)
