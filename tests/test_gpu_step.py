@@ -296,3 +296,27 @@ def test_27b_layer_batched_equals_solo():
     for k in (1, 2, 3):
         sub = case.run(list(range(k)))
         assert same_bits(sub["x"], b["x"][:k])
+
+
+@pytest.mark.parametrize("dims,n_seq,rows", [(wl.LAYER27B, 4, 1), (wl.LAYER27B, 1, 1), (wl.TINY_LAYER, 3, 1),
+                                             (wl.TINY_LAYER, 2, 2), (wl.TINY_LAYER, 2, 3)])
+def test_fused_gate_up_swiglu_equals_the_two_launches_bitwise(dims, n_seq, rows):
+    """At 1-4 rows the step computes gate||up, SwiGLU and its q8_0 codes in one
+    launch; its gu, h and codes equal the standalone projection followed by the
+    standalone SwiGLU quantizer on the same activations, bit for bit (at 5-8
+    rows the step runs those two launches itself)."""
+    cap = 2051 if dims is wl.LAYER27B else 160
+    case = Case(5, dims, 1, [cap - rows] * n_seq, [rows] * n_seq, cap=cap)
+    out = case.run()
+    T, H, F = out["T"], dims.hidden, dims.ffn
+    lay = case.model.layout(T, case.cap)
+    ws = out["ws"]
+    L = case.layers_h[0]
+    aq = cuda(ws_view(ws, lay["xn2_q"], (T, H), np.int8))
+    ad = cuda(ws_view(ws, lay["xn2_d"], (T, H // 32), np.float32))
+    gu = luce.luce_q8_matvec_batch(cuda(L.wgu_q), cuda(L.wgu_d), aq, ad)
+    h, hq, hd = luce.luce_swiglu_q8(gu)
+    assert same_bits(ws_view(ws, lay["gu"], (T, 2 * F), np.float32), host(gu))
+    assert same_bits(ws_view(ws, lay["h"], (T, F), np.float32), host(h))
+    assert np.array_equal(ws_view(ws, lay["h_q"], (T, F), np.int8), host(hq))
+    assert same_bits(ws_view(ws, lay["h_d"], (T, F // 32), np.float32), host(hd))
