@@ -54,6 +54,10 @@ constexpr int kRingCtasPerSmWide = 3;  // 5..8 rows (larger activation boxes)
 constexpr int kRingSlotsWide = 3;
 constexpr int kRingSlotsNarrow = 3;    // 1..4 rows
 constexpr int kRingThreads = 160;  // 4 consumer warps + 1 producer warp
+// Consumer warps of the fused gate||up kernel at T rows (two CTAs per SM):
+// 8 at one row, where more warps hide more latency, 4 from two rows on, where
+// each lane's 4 rows give the dp4a chains more independent work (measured).
+__host__ __device__ constexpr int gateup_warps(int T) { return T == 1 ? 8 : 4; }
 
 // Shape of a ring: T activation rows, G rows per lane (a group is G quads,
 // 4G rows), S slots.
@@ -135,11 +139,11 @@ struct RingSmem {
         full = reinterpret_cast<uint64_t*>(slots + S * L::STAGE + L::PART);
         empty = full + S;
     }
-    __device__ void init() const
+    __device__ void init(int consumer_warps = 4) const
     {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 4);
+            mbar_init(&empty[s], consumer_warps);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -179,17 +183,19 @@ __device__ __forceinline__ void ring_produce(const RingSmem<T, G, S>& R, int tot
 
 // A consumer lane's chains for one group: stages it .. it + nj - 1 (it
 // advances), lane (r, kb) of warp w, chain c = kb + 8w, rows r + 4g of the
-// group.  acc[g][t] = chain c of row r + 4g against token t.  ok turns false
-// when a wait expires; from then on the lane waits for nothing more and the
-// caller writes nothing.
-template <int T, int G, int S, bool BIAS>
+// group, g < GL (GL = G: all the group's rows; fewer when several warps share
+// the chains, r then carrying the row offset of this warp's share).
+// acc[g][t] = chain c of row r + 4g against token t.  ok turns false when a
+// wait expires; from then on the lane waits for nothing more and the caller
+// writes nothing.
+template <int T, int G, int S, bool BIAS, int GL = G>
 __device__ __forceinline__ void ring_chains(const RingSmem<T, G, S>& R, int& it, int nj, int nb, int r, int c, int lane,
-                                            float (&acc)[G][T], bool& ok)
+                                            float (&acc)[GL][T], bool& ok)
 {
     using L = RingLayout<T, G, S>;
     const int h0 = ((lane & 7) >> 2) & 1;  // which 16-byte half first: a phase's 8 lanes hit 8 distinct bank quads
 #pragma unroll
-    for (int g = 0; g < G; ++g)
+    for (int g = 0; g < GL; ++g)
 #pragma unroll
         for (int t = 0; t < T; ++t) acc[g][t] = 0.0f;
     for (int j = 0; j < nj; ++j, ++it) {
@@ -198,11 +204,11 @@ __device__ __forceinline__ void ring_chains(const RingSmem<T, G, S>& R, int& it,
         if (!ok) continue;
         const uint8_t* slot = R.slots + s * L::STAGE;
         const bool has = 32 * j + c < nb;
-        uint4 wx[G], wy[G], ax[T], ay[T];
-        float sw[G], sa[T];
+        uint4 wx[GL], wy[GL], ax[T], ay[T];
+        float sw[GL], sa[T];
         if (has) {
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
+            for (int g = 0; g < GL; ++g) {
                 const uint8_t* p = slot + (r + 4 * g) * 1024 + c * 32;
                 wx[g] = lds128(p + 16 * h0);
                 wy[g] = lds128(p + 16 * (h0 ^ 1));
@@ -222,7 +228,7 @@ __device__ __forceinline__ void ring_chains(const RingSmem<T, G, S>& R, int& it,
 #pragma unroll
             for (int t = 0; t < T; ++t)
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
+                for (int g = 0; g < GL; ++g) {
                     const float sd = block_dot_halves<BIAS>(wx[g], wy[g], ax[t], ay[t]);
                     acc[g][t] = __fmaf_rn(__fmul_rn(sw[g], sa[t]), sd, acc[g][t]);
                 }
@@ -395,8 +401,11 @@ q8_qkv_rope_tma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_cons
 // the unit's 32 features are in, warp t quantizes token t's block of h -
 // exactly swiglu_quant_kernel's arithmetic.  Persistent: CTA b owns units
 // [b*U/grid, (b+1)*U/grid) of the U = F/32; mdp has an 8-row scale box.
+// Shared memory allows two CTAs per SM; at one row a CTA has 8 consumer
+// warps (the gate and the up rows of a group in two sets of 4, each lane 2
+// rows), else 4 (each lane 4 rows: 2 gate, 2 up).
 template <int T, int S, bool BIAS>
-__global__ void __launch_bounds__(kRingThreads)
+__global__ void __launch_bounds__(32 * (gateup_warps(T) + 1), 2)
 q8_gateup_swiglu_tma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap mdp,
                             const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mad, int F,
                             int K, float* __restrict__ gu, float* __restrict__ h, int8_t* __restrict__ hq,
@@ -413,11 +422,12 @@ q8_gateup_swiglu_tma_kernel(const __grid_constant__ CUtensorMap mw, const __grid
     const int u0 = (int)((int64_t)blockIdx.x * U / gridDim.x);
     const int u1 = (int)((int64_t)(blockIdx.x + 1) * U / gridDim.x);
     const int ngrp = 4 * (u1 - u0);
+    constexpr int CW = gateup_warps(T), GL = 16 / CW;  // consumer warps, rows per lane
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-    if (tid == 0) R.init();
+    if (tid == 0) R.init(CW);
     __syncthreads();
 
-    if (w == 4) {
+    if (w == CW) {
         if (lane != 0) return;
         ring_produce<T, G, S>(
             R, ngrp * nj, nj, &ma, &mad,
@@ -436,17 +446,20 @@ q8_gateup_swiglu_tma_kernel(const __grid_constant__ CUtensorMap mw, const __grid
     }
 
     pdl_wait();  // gu, h and the codes may be touched by earlier kernels
-    const int r = lane >> 3, c = (lane & 7) + 8 * w;
+    // with 8 consumer warps, warps 0-3 take the gate rows 0-7 of a group and
+    // warps 4-7 the up rows 8-15; lane (r, kb) of warp w runs chain
+    // c = kb + 8 (w % 4) of rows r + 8 (w / 4) + 4g, g < GL
+    const int r = (lane >> 3) + 8 * (w >> 2), c = (lane & 7) + 8 * (w & 3);
     bool ok = true;
     int it = 0;
     for (int gi = 0; gi < ngrp; ++gi) {
-        float acc[G][T];
-        ring_chains<T, G, S, BIAS>(R, it, nj, nb, r, c, lane, acc, ok);
+        float acc[GL][T];
+        ring_chains<T, G, S, BIAS, GL>(R, it, nj, nb, r, c, lane, acc, ok);
         // two chain buffers, so one barrier per group separates writers and readers
         float* pp = R.part + (L::PB == 2 ? (gi & 1) * (L::ROWS * T * 33) : 0);
-        if (L::PB == 1 && gi > 0) asm volatile("bar.sync 1, 128;" ::: "memory");  // last group's readers are done
-        store_chains<T, G>(pp, r, c, acc);
-        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (L::PB == 1 && gi > 0) asm volatile("bar.sync 1, %0;" ::"n"(32 * CW) : "memory");  // readers are done
+        store_chains<T, GL>(pp, r, c, acc);
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * CW) : "memory");
         const int fu = 32 * (u0 + gi / 4), i = gi % 4;
         if (tid < 8 * T && ok) {  // feature fu + 8i + p of token t: local rows p (gate) and 8 + p (up)
             const int p = tid / T, t = tid - (tid / T) * T;
@@ -457,7 +470,7 @@ q8_gateup_swiglu_tma_kernel(const __grid_constant__ CUtensorMap mw, const __grid
             hb[t][8 * i + p] = silu_mul(g, u);
         }
         if (i == 3) {  // the unit's 32 features are in: warp t quantizes token t's block
-            asm volatile("bar.sync 1, 128;" ::: "memory");
+            asm volatile("bar.sync 1, %0;" ::"n"(32 * CW) : "memory");
             if (w < T && ok) {
                 const float v = hb[w][lane];
                 h[(size_t)w * F + fu + lane] = v;
@@ -728,7 +741,8 @@ cudaError_t launch_gateup_t(const CUtensorMap& mw, const CUtensorMap& mdp, const
     static std::atomic<bool> done[kMaxDevices];
     cudaError_t e = set_smem_once(q8_gateup_swiglu_tma_kernel<T, kGateUpSlots, BIAS>, L::SMEM, done);
     if (e == cudaSuccess)
-        e = launch_pdl_smem(q8_gateup_swiglu_tma_kernel<T, kGateUpSlots, BIAS>, dim3(grid), dim3(kRingThreads),
+        e = launch_pdl_smem(q8_gateup_swiglu_tma_kernel<T, kGateUpSlots, BIAS>, dim3(grid),
+                            dim3(32 * (gateup_warps(T) + 1)),
                             L::SMEM, s, mw, mdp, ma, mad, F, K, gu, h, hq, hd);
     count_launches(1);
     return e;
