@@ -119,6 +119,13 @@ cudaError_t launch_qkv_rope(const int8_t* wq, const __half* wd, int K, const int
 
 // RoPE of the q and k heads and the K/V append from a q|k|v projection in
 // qkv [T][(Hq + 2 Hkv) 128] (the epilogue of launch_qkv_rope as its own launch).
+// The step's q|k|v projection on the tensor-core ring with RoPE and the K/V
+// append in its epilogue (1..16 rows; the same bits as launch_matvec_mma +
+// launch_qkv_rope_kv).  cudaErrorNotSupported when the ring does not take
+// the shapes.
+cudaError_t launch_qkv_rope_mma(const int8_t* wq, const __half* wd, int K, const int8_t* aq, const float* ad, int T,
+                                float* qkv, int Hq, int Hkv, const RowPos& pos, const RopeFreq& f, float* q_rot,
+                                const KvRows& kv, cudaStream_t s);
 cudaError_t launch_qkv_rope_kv(const float* qkv, int T, int Hq, int Hkv, const RowPos& pos, const RopeFreq& f,
                                float* q_rot, const KvRows& kv, cudaStream_t s);
 

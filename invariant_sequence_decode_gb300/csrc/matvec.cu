@@ -288,15 +288,19 @@ cudaError_t launch_qkv_rope(const int8_t* wq, const __half* wd, int K, const int
                             float* qkv, int Hq, int Hkv, const RowPos& pos, const RopeFreq& f, float* q_rot,
                             const KvRows& kv, cudaStream_t s)
 {
-    // From kMmaQkvMinRows rows: the tensor-core matvec, then RoPE and the
-    // K/V append as a launch of their own (the same rotation and rounding).
+    // From kMmaQkvMinRows rows: the tensor-core ring with RoPE and the K/V
+    // append in its epilogue, or (shapes it does not take) the tensor-core
+    // matvec and then RoPE and the append as a launch of their own (the same
+    // rotation and rounding either way).
     // Otherwise 1..8 and 13..16 rows on the TMA ring when the shapes allow
     // (matvec_tma.cu), else the plain kernel's launch shapes, except G = 4
     // where the plain kernel takes G = 3 (T = 3, 12): the rotation pairs
     // P = 2G must tile 64
     if (T >= kMmaQkvMinRows) {
+        cudaError_t e = launch_qkv_rope_mma(wq, wd, K, aq, ad, T, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
+        if (e != cudaErrorNotSupported) return e;
         const int N = (Hq + 2 * Hkv) * kHeadDim;
-        const cudaError_t e = launch_matvec_mma(wq, wd, N, K, aq, ad, T, qkv, N, nullptr, 0, s);
+        e = launch_matvec_mma(wq, wd, N, K, aq, ad, T, qkv, N, nullptr, 0, s);
         if (e != cudaErrorNotSupported) {
             if (e != cudaSuccess) return e;
             return launch_qkv_rope_kv(qkv, T, Hq, Hkv, pos, f, q_rot, kv, s);

@@ -179,7 +179,13 @@ struct MmaSmem {
 // `total` goes to slot it % S; the group's first tile is t0 + TL (it / nj) and
 // it has min(TL, t1 - that) tiles.  The first S stages' weights go before the
 // wait on the previous kernel, which the activations need.
-template <int NT, int TL, int S, int CW, int H>
+// PAIRED (the q|k|v projection with RoPE): tile v holds rows 8a .. 8a + 7
+// and 64 + 8a .. 64 + 8a + 7 of head v / 8 (a = v % 8), two 8-row boxes each
+// (mw and md with 8-row boxes), so rows r and r + 8 of a tile are the
+// rotation pair (8a + r, 8a + r + 64) and meet in one thread's fragment.
+__device__ __forceinline__ int paired_row(int v, int half) { return (v >> 3) * kHeadDim + 8 * (v & 7) + 64 * half; }
+
+template <int NT, int TL, int S, int CW, int H, bool PAIRED = false>
 __device__ __forceinline__ void mma_produce(const MmaSmem<NT, TL, S, CW, H>& R, int total, int nj, int t0, int t1,
                                             const CUtensorMap* mw, const CUtensorMap* md, const CUtensorMap* ma,
                                             const CUtensorMap* mad)
@@ -189,8 +195,18 @@ __device__ __forceinline__ void mma_produce(const MmaSmem<NT, TL, S, CW, H>& R, 
     auto load_w = [&](int it) {
         const int s = it % S, j = it % nj, tile0 = t0 + TL * (it / nj), nt = tiles(it);
         uint8_t* slot = R.slots + s * L::STAGE;
-        for (int i = 0; i < nt; ++i) tma_load_3d(slot + i * kTileBytes, mw, 0, kTileRows * (tile0 + i), 8 * j, &R.full[s]);
-        tma_load_2d(slot + L::W + L::A, md, 32 * j, kTileRows * tile0, &R.full[s]);
+        if (PAIRED) {
+            for (int i = 0; i < nt; ++i)
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int row = paired_row(tile0 + i, hf);
+                    tma_load_3d(slot + i * kTileBytes + hf * (kTileBytes / 2), mw, 0, row, 8 * j, &R.full[s]);
+                    tma_load_2d(slot + L::W + L::A + (16 * i + 8 * hf) * 64, md, 32 * j, row, &R.full[s]);
+                }
+        } else {
+            for (int i = 0; i < nt; ++i)
+                tma_load_3d(slot + i * kTileBytes, mw, 0, kTileRows * (tile0 + i), 8 * j, &R.full[s]);
+            tma_load_2d(slot + L::W + L::A, md, 32 * j, kTileRows * tile0, &R.full[s]);
+        }
     };
     auto load_a = [&](int it) {
         const int s = it % S, j = it % nj;
@@ -198,7 +214,9 @@ __device__ __forceinline__ void mma_produce(const MmaSmem<NT, TL, S, CW, H>& R, 
         tma_load_3d(slot + L::W, ma, 0, 0, 8 * j, &R.full[s]);
         tma_load_2d(slot + L::W + L::A + L::WD, mad, 32 * j, 0, &R.full[s]);
     };
-    auto bytes = [&](int it) { return (uint32_t)(tiles(it) * kTileBytes + L::A + L::WD + L::AD); };
+    auto bytes = [&](int it) {
+        return (uint32_t)(tiles(it) * kTileBytes + L::A + (PAIRED ? tiles(it) * kTileRows * 64 : L::WD) + L::AD);
+    };
     const int pre = min(S, total);
     for (int it = 0; it < pre; ++it) {
         mbar_expect_tx(&R.full[it], bytes(it));
@@ -221,7 +239,7 @@ __device__ __forceinline__ void mma_produce(const MmaSmem<NT, TL, S, CW, H>& R, 
 // token tile n, element e of the m16n8 fragment (rows gr, gr + 8; tokens
 // 2tq, 2tq + 1).  ok turns false when a wait expires; from then on the warp
 // waits for nothing more.
-template <int NT, int TL, int S, int CW, int H>
+template <int NT, int TL, int S, int CW, int H, bool PAIRED = false>
 __device__ __forceinline__ void mma_chains(const MmaSmem<NT, TL, S, CW, H>& R, int& it, int nj, int nb, int nt, int w,
                                            int lane, float (&acc)[32 / (CW / H)][TL][NT / H][4], bool& ok)
 {
@@ -288,7 +306,11 @@ __device__ __forceinline__ void mma_chains(const MmaSmem<NT, TL, S, CW, H>& R, i
                 for (int i = 0; i < TL; ++i) {
                     if (i < nt) {
                         uint32_t r[4], a[2][4];
-                        ldsm_x4(s_w + i * kTileBytes + swz(z * 16 + rr + 8 * (mi & 1), ch + (mi >> 1)), r);
+                        if (PAIRED)  // rows 0-7 and 8-15 of the tile are two 8-row boxes
+                            ldsm_x4(s_w + i * kTileBytes + (mi & 1) * (kTileBytes / 2) + swz(z * 8 + rr, ch + (mi >> 1)),
+                                    r);
+                        else
+                            ldsm_x4(s_w + i * kTileBytes + swz(z * 16 + rr + 8 * (mi & 1), ch + (mi >> 1)), r);
                         i8x4_to_h2_biased(r[0], a[0][0], a[0][2]);  // row gr, bytes 4tq..4tq+3 of the first half
                         i8x4_to_h2_biased(r[1], a[0][1], a[0][3]);  // row gr + 8
                         i8x4_to_h2_biased(r[2], a[1][0], a[1][2]);  // the second half
@@ -448,6 +470,87 @@ q8_matvec_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_consta
     }
 }
 
+// The decode step's q|k|v projection at wide verify batches with the RoPE
+// rotation and the K/V append in the epilogue ("antirez/ds4 pull 604",
+// Commit walkthrough): the tiles are PAIRED (mma_produce), so the thread that
+// finishes row 8a + p of a head also finishes row 8a + p + 64, and it stores
+// both to qkv, rotates them (q and k heads) by the token's position and
+// writes q_rot, or rounds them to binary16 at the token's K/V destination -
+// the rotation and conversion of qkv_rope_kv_kernel, so the same bits.
+// mw: W as [K/128][N][128] with an 8-row box; md: scales with an 8-row box.
+template <int NT, int TL, int S, int CW, int H>
+__global__ void __launch_bounds__(32 * (CW + 1), 1)
+q8_qkv_rope_mma_kernel(const __grid_constant__ CUtensorMap mw, const __grid_constant__ CUtensorMap md,
+                       const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mad, int K, int T,
+                       float* __restrict__ qkv, int Hq, int Hkv, const __grid_constant__ RowPos pos,
+                       const __grid_constant__ RopeFreq f, float* __restrict__ q_rot, const __grid_constant__ KvRows kv)
+{
+    using L = MmaRing<NT, TL, S, CW, H>;
+    extern __shared__ uint8_t smem_raw[];
+    const MmaSmem<NT, TL, S, CW, H> R(smem_raw);
+    pdl_trigger();
+    const int N = (Hq + 2 * Hkv) * kHeadDim;
+    const int nb = K >> 5, nj = (nb + 31) >> 5;
+    const int ntl = N / kTileRows;
+    const int t0 = (int)((int64_t)blockIdx.x * ntl / gridDim.x);
+    const int t1 = (int)((int64_t)(blockIdx.x + 1) * ntl / gridDim.x);
+    const int ngrp = (t1 - t0 + TL - 1) / TL;
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&R.full[s], 1);
+            mbar_init(&R.empty[s], CW);
+        }
+        *R.failed = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    if (w == CW) {
+        if (lane == 0) mma_produce<NT, TL, S, CW, H, true>(R, ngrp * nj, nj, t0, t1, &mw, &md, &ma, &mad);
+        return;
+    }
+
+    pdl_wait();  // the K/V caches and outputs may be touched by earlier kernels
+    bool ok = true;
+    int it = 0;
+    const int ldq = N;
+    for (int gi = 0; gi < ngrp; ++gi) {
+        const int tile0 = t0 + TL * gi, nt = min(TL, t1 - tile0);
+        float acc[L::CP][TL][L::NTL][4];
+        mma_chains<NT, TL, S, CW, H, true>(R, it, nj, nb, nt, w, lane, acc, ok);
+        mma_reduce<NT, TL, CW, H>(R.red, w, lane, gi > 0, acc);
+        if (*R.failed) continue;
+        // (tile i, pair p, token tok): rows p and 8 + p of tile i
+        for (int idx = tid; idx < nt * 8 * L::TOK; idx += 32 * CW) {
+            const int i = idx / (8 * L::TOK), rem = idx - i * 8 * L::TOK;
+            const int p = rem / L::TOK, tok = rem - p * L::TOK;
+            if (tok >= T) continue;
+            const int v = tile0 + i, h = v >> 3, d = 8 * (v & 7) + p;  // the pair (d, d + 64) of head h
+            float x0 = mma_finish<L::WH>(R.red, (16 * i + p) * L::TOK + tok, L::ROWS * L::TOK);
+            float x1 = mma_finish<L::WH>(R.red, (16 * i + 8 + p) * L::TOK + tok, L::ROWS * L::TOK);
+            float* yr = qkv + (size_t)tok * ldq + (size_t)h * kHeadDim;
+            yr[d] = x0;
+            yr[d + kHeadDim / 2] = x1;
+            const bool rot = h < Hq + Hkv;
+            if (rot) {
+                const float2 cs = rope_cs(pos.pos[tok], f.inv[d]);
+                rope_rotate(x0, x1, cs.x, cs.y);
+            }
+            if (h < Hq) {
+                float* dst = q_rot + ((size_t)tok * Hq + h) * kHeadDim;
+                dst[d] = x0;
+                dst[d + kHeadDim / 2] = x1;
+            } else {
+                const KvRow kr = kv.row[tok];
+                __half* dst = rot ? kr.k + (h - Hq) * kr.head_stride : kr.v + (h - Hq - Hkv) * kr.head_stride;
+                dst[d] = __float2half_rn(x0);
+                dst[d + kHeadDim / 2] = __float2half_rn(x1);
+            }
+        }
+    }
+}
+
 namespace {
 
 template <int NT, int TL, int S, int CW, int H>
@@ -470,7 +573,8 @@ cudaError_t launch_mma_t(const CUtensorMap& mw, const CUtensorMap& md, const CUt
 // The four maps of a launch; false when the shapes or alignments do not allow
 // one (K a multiple of 256, 16-byte aligned operands, a driver that encodes it).
 bool mma_maps(const int8_t* wq, const __half* wd, int N, int K, const int8_t* aq, const float* ad, int T, int tok_box,
-              int scale_rows, CUtensorMap* mw, CUtensorMap* md, CUtensorMap* ma, CUtensorMap* mad)
+              int scale_rows, CUtensorMap* mw, CUtensorMap* md, CUtensorMap* ma, CUtensorMap* mad,
+              int w_rows = kTileRows)
 {
     auto al16 = [](const void* p) { return ((uintptr_t)p & 15) == 0; };
     if (T < 1 || T > 16 || K % 256 != 0 || !al16(wq) || !al16(wd) || !al16(aq) || !al16(ad)) return false;
@@ -478,7 +582,7 @@ bool mma_maps(const int8_t* wq, const __half* wd, int N, int K, const int8_t* aq
     // x = byte of a 128-byte line of K, y = row, z = line: rows of one line
     // land 128 bytes apart, which the swizzle spreads over all banks
     const cuuint64_t wdim[3] = {128, (cuuint64_t)N, lines}, wstr[2] = {(cuuint64_t)K, 128};
-    const cuuint32_t wbox[3] = {128, kTileRows, 8};
+    const cuuint32_t wbox[3] = {128, (cuuint32_t)w_rows, 8};
     const cuuint64_t ddim[2] = {nb, (cuuint64_t)N}, dstr[1] = {nb * 2};
     const cuuint32_t dbox[2] = {32, (cuuint32_t)scale_rows};
     const cuuint64_t adim[3] = {128, (cuuint64_t)T, lines}, astr[2] = {(cuuint64_t)K, 128};
@@ -523,6 +627,43 @@ cudaError_t launch_matvec_mma(const int8_t* wq, const __half* wd, int N, int K, 
                                                                       sms, s);
     return launch_mma_t<2, kMmaTiles, kMmaSlots2, kMmaWarps2, kMmaHalves2>(mw, md, ma, mad, N, K, T, y, ldy, resid,
                                                                            ldr, sms, s);
+}
+
+namespace {
+
+template <int NT, int TL, int S, int CW, int H>
+cudaError_t launch_qkv_mma_t(const CUtensorMap& mw, const CUtensorMap& md, const CUtensorMap& ma,
+                             const CUtensorMap& mad, int K, int T, float* qkv, int Hq, int Hkv, const RowPos& pos,
+                             const RopeFreq& f, float* q_rot, const KvRows& kv, int ctas, cudaStream_t s)
+{
+    using L = MmaRing<NT, TL, S, CW, H>;
+    static std::atomic<bool> done[kMaxDevices];
+    const cudaError_t attr = set_smem_once(q8_qkv_rope_mma_kernel<NT, TL, S, CW, H>, L::SMEM, done);
+    if (attr != cudaSuccess) return attr;
+    const int ntl = (Hq + 2 * Hkv) * kHeadDim / kTileRows;
+    const cudaError_t e =
+        launch_pdl_smem(q8_qkv_rope_mma_kernel<NT, TL, S, CW, H>, dim3(min(ctas, ntl)), dim3(L::THREADS), L::SMEM, s,
+                        mw, md, ma, mad, K, T, qkv, Hq, Hkv, pos, f, q_rot, kv);
+    count_launches(1);
+    return e;
+}
+
+}  // namespace
+
+cudaError_t launch_qkv_rope_mma(const int8_t* wq, const __half* wd, int K, const int8_t* aq, const float* ad, int T,
+                                float* qkv, int Hq, int Hkv, const RowPos& pos, const RopeFreq& f, float* q_rot,
+                                const KvRows& kv, cudaStream_t s)
+{
+    const int sms = sm_count();
+    if (sms <= 0 || T < 1 || T > 16) return cudaErrorNotSupported;
+    const int N = (Hq + 2 * Hkv) * kHeadDim;
+    CUtensorMap mw, md, ma, mad;
+    if (!mma_maps(wq, wd, N, K, aq, ad, T, T <= 8 ? 8 : 16, 8, &mw, &md, &ma, &mad, 8)) return cudaErrorNotSupported;
+    if (T <= 8)
+        return launch_qkv_mma_t<1, kMmaTiles, kMmaSlots1, kMmaWarps1, 1>(mw, md, ma, mad, K, T, qkv, Hq, Hkv, pos, f,
+                                                                          q_rot, kv, sms, s);
+    return launch_qkv_mma_t<2, kMmaTiles, kMmaSlots2, kMmaWarps2, kMmaHalves2>(mw, md, ma, mad, K, T, qkv, Hq, Hkv,
+                                                                               pos, f, q_rot, kv, sms, s);
 }
 
 cudaError_t read_mma_wait_timeouts(uint32_t* count, bool reset)
