@@ -176,6 +176,10 @@ static cudaError_t launch_matvec_register(const int8_t* wq, const __half* wd, in
 // projection (which the dp4a ring serves with RoPE fused at 1..8 rows).
 constexpr int kMmaMinRows = 5;
 constexpr int kMmaQkvMinRows = QKV_MMA_MIN;
+// Rows from which the step's q|k|v runs on the tensor-core ring with RoPE and
+// the K/V append fused (measured: one-layer step at 4 slots x 2 rows 103.4 ->
+// 99.3 us, 2 x 3 rows 101.4 -> 99.3 us against the fused dp4a ring).
+constexpr int kMmaQkvFusedMinRows = 5;
 
 cudaError_t launch_matvec_path(int path, const int8_t* wq, const __half* wd, int N, int K, const int8_t* aq,
                                const float* ad, int T, float* y, int64_t ldy, const float* resid, int64_t ldr,
@@ -288,19 +292,21 @@ cudaError_t launch_qkv_rope(const int8_t* wq, const __half* wd, int K, const int
                             float* qkv, int Hq, int Hkv, const RowPos& pos, const RopeFreq& f, float* q_rot,
                             const KvRows& kv, cudaStream_t s)
 {
-    // From kMmaQkvMinRows rows: the tensor-core ring with RoPE and the K/V
-    // append in its epilogue, or (shapes it does not take) the tensor-core
-    // matvec and then RoPE and the append as a launch of their own (the same
-    // rotation and rounding either way).
+    // From kMmaQkvFusedMinRows rows: the tensor-core ring with RoPE and the
+    // K/V append in its epilogue; for shapes it does not take, from
+    // kMmaQkvMinRows rows the tensor-core matvec and then RoPE and the append
+    // as a launch of their own (the same rotation and rounding either way).
     // Otherwise 1..8 and 13..16 rows on the TMA ring when the shapes allow
     // (matvec_tma.cu), else the plain kernel's launch shapes, except G = 4
     // where the plain kernel takes G = 3 (T = 3, 12): the rotation pairs
     // P = 2G must tile 64
-    if (T >= kMmaQkvMinRows) {
-        cudaError_t e = launch_qkv_rope_mma(wq, wd, K, aq, ad, T, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
+    if (T >= kMmaQkvFusedMinRows) {
+        const cudaError_t e = launch_qkv_rope_mma(wq, wd, K, aq, ad, T, qkv, Hq, Hkv, pos, f, q_rot, kv, s);
         if (e != cudaErrorNotSupported) return e;
+    }
+    if (T >= kMmaQkvMinRows) {
         const int N = (Hq + 2 * Hkv) * kHeadDim;
-        e = launch_matvec_mma(wq, wd, N, K, aq, ad, T, qkv, N, nullptr, 0, s);
+        const cudaError_t e = launch_matvec_mma(wq, wd, N, K, aq, ad, T, qkv, N, nullptr, 0, s);
         if (e != cudaErrorNotSupported) {
             if (e != cudaSuccess) return e;
             return launch_qkv_rope_kv(qkv, T, Hq, Hkv, pos, f, q_rot, kv, s);
