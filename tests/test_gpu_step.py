@@ -320,3 +320,36 @@ def test_fused_gate_up_swiglu_equals_the_two_launches_bitwise(dims, n_seq, rows)
     assert same_bits(ws_view(ws, lay["h"], (T, F), np.float32), host(h))
     assert np.array_equal(ws_view(ws, lay["h_q"], (T, F), np.int8), host(hq))
     assert same_bits(ws_view(ws, lay["h_d"], (T, F // 32), np.float32), host(hd))
+
+
+@pytest.mark.parametrize("dims,n_seq,rows", [(wl.LAYER27B, 4, 2), (wl.LAYER27B, 4, 4), (wl.TINY_LAYER, 2, 3),
+                                             (wl.TINY_LAYER, 4, 4)])
+def test_wide_qkv_rope_epilogue_equals_the_separate_kernels_bitwise(dims, n_seq, rows):
+    """From 5 rows the step's q|k|v runs on the tensor-core ring with RoPE and
+    the K/V append in its epilogue; its qkv, q_rot and cache rows equal the
+    standalone projection, then the standalone RoPE, then binary16 rounding,
+    bit for bit."""
+    cap = 2051 if dims is wl.LAYER27B else 160
+    case = Case(7, dims, 1, [cap - rows] * n_seq, [rows] * n_seq, cap=cap)
+    out = case.run()
+    T, H, Hq, Hkv, D = out["T"], dims.hidden, dims.n_q_heads, dims.n_kv_heads, dims.head_dim
+    lay = case.model.layout(T, case.cap)
+    ws = out["ws"]
+    L = case.layers_h[0]
+    aq = cuda(ws_view(ws, lay["xn_q"], (T, H), np.int8))
+    ad = cuda(ws_view(ws, lay["xn_d"], (T, H // 32), np.float32))
+    qkv = luce.luce_q8_matvec_batch(cuda(L.wqkv_q), cuda(L.wqkv_d), aq, ad)
+    assert same_bits(ws_view(ws, lay["qkv"], (T, (Hq + 2 * Hkv) * D), np.float32), host(qkv))
+    heads = qkv.view(T, Hq + 2 * Hkv, D)
+    qk = heads[:, :Hq + Hkv].contiguous()
+    pos = torch.tensor([cap - rows + j for _ in range(n_seq) for j in range(rows)], dtype=torch.int32, device="cuda")
+    luce.luce_rope_posvec(qk, pos, dims.rope_theta)
+    assert same_bits(ws_view(ws, lay["q_rot"], (T, Hq, D), np.float32), host(qk[:, :Hq]))
+    k_ref = host(qk[:, Hq:]).astype(np.float16)
+    v_ref = host(heads[:, Hq + Hkv:]).astype(np.float16)
+    for t in range(T):
+        s, j = divmod(t, rows)
+        p = cap - rows + j
+        sl = out["slots"][s]
+        assert same_bits(host(sl.k[0, :, p, :]), k_ref[t]), t
+        assert same_bits(host(sl.v[0, :, p, :]), v_ref[t]), t
