@@ -707,8 +707,27 @@ attn_merge_kernel(AttnRows rows, int Hq, const float* __restrict__ part, float* 
 #pragma unroll
     for (int u = 0; u < kPre; ++u) ov[u] = u < nch ? __ldcg(bh + u * cstride + d) : 0.0f;
     if (d < 32) {
+        // every chunk's (m, l) up to 128 chunks requested at once (one L2 round
+        // trip), then the rest; the maximum is order-free
+        constexpr int kStatPre = 4;
+        float mp[kStatPre], lp[kStatPre];
+#pragma unroll
+        for (int i = 0; i < kStatPre; ++i) {
+            const int cc = lane + 32 * i;
+            mp[i] = cc < nch ? __ldcg(bh + cc * cstride + 128) : -INFINITY;
+            lp[i] = cc < nch ? __ldcg(bh + cc * cstride + 129) : 0.0f;
+        }
         float M = -INFINITY;
-        for (int cc = lane; cc < nch; cc += 32) {
+#pragma unroll
+        for (int i = 0; i < kStatPre; ++i) {
+            const int cc = lane + 32 * i;
+            if (cc < nch) {
+                wts[cc] = mp[i];
+                lsum[cc] = lp[i];
+                M = fmaxf(M, mp[i]);
+            }
+        }
+        for (int cc = lane + 32 * kStatPre; cc < nch; cc += 32) {
             const float m = __ldcg(bh + cc * cstride + 128);
             wts[cc] = m;
             lsum[cc] = __ldcg(bh + cc * cstride + 129);
@@ -730,6 +749,13 @@ attn_merge_kernel(AttnRows rows, int Hq, const float* __restrict__ part, float* 
     for (int u = 0; u < kPre; ++u)
         if (u < nch) O = __fmaf_rn(ov[u], wts[u], O);
     int cc = kPre;
+    for (; cc + 32 <= nch; cc += 32) {
+        float ob[32];
+#pragma unroll
+        for (int u = 0; u < 32; ++u) ob[u] = __ldcg(bh + (cc + u) * cstride + d);
+#pragma unroll
+        for (int u = 0; u < 32; ++u) O = __fmaf_rn(ob[u], wts[cc + u], O);
+    }
     for (; cc + 16 <= nch; cc += 16) {
         float ob[16];
 #pragma unroll
