@@ -165,10 +165,18 @@ class Layer27B:
         self.ws = self.model.workspace(n_seq_max, self.cap)
         from invariant_sequence_decode_gb300.kernel_bench import L2Flush
         self.flush_l2 = L2Flush(torch)
+        self._steps = {}
 
     def step(self, n_seq: int, x=None):
-        self.luce.luce_decode_step(self.model, self.slots[:n_seq], [1] * n_seq,
-                                   self.x[:n_seq] if x is None else x, self.ws)
+        """One step of n_seq slots x 1 row: the prepared C call (DeviceStep)
+        for the workload's own rows, so the host stays well ahead of the GPU."""
+        if x is not None:
+            self.luce.luce_decode_step(self.model, self.slots[:n_seq], [1] * n_seq, x, self.ws)
+            return
+        if n_seq not in self._steps:
+            self._steps[n_seq] = self.luce.DeviceStep(self.model, self.slots[:n_seq], [1] * n_seq,
+                                                      self.x[:n_seq], self.ws)
+        self._steps[n_seq]()
 
 
 def time_steps(torch, fn, flush, k: int) -> list:

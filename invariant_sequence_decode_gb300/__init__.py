@@ -514,6 +514,35 @@ def luce_decode_step_host(model: Model, slots: Sequence[Slot], rows_per_slot: Se
     return x_out
 
 
+class DeviceStep:
+    """luce_decode_step with its arguments marshalled once, for repeated steps
+    over the same slots and buffers (x on the device): each call copies the
+    slots' current ``len`` into the prepared slot array and makes the C call
+    (nothing else is re-checked).  The stream is the one given, or the current
+    stream at construction."""
+
+    def __init__(self, model: Model, slots: Sequence[Slot], rows_per_slot: Sequence[int], x, ws, logits=None,
+                 argmax=None, stream=None):
+        import torch
+        _need(x, torch.float32, "x")
+        self.slots = list(slots)
+        n = len(self.slots)
+        self._sc = (SlotC * max(1, n))()
+        for i, s in enumerate(self.slots):
+            self._sc[i] = SlotC(s.k.data_ptr(), s.v.data_ptr(), s.len, s.cap)
+        self._rows = (ctypes.c_int32 * max(1, n))(*rows_per_slot)
+        self._keep = (model, x, ws, logits, argmax)
+        self._fn = load_library().luce_decode_step
+        self._args = (ctypes.byref(model.c), self._sc, self._rows, n, x.data_ptr(), _ptr(logits), _ptr(argmax),
+                      ws.data_ptr(), ws.numel(), _stream(stream))
+
+    def __call__(self):
+        sc = self._sc
+        for i, s in enumerate(self.slots):
+            sc[i].len = s.len
+        _check(self._fn(*self._args))
+
+
 class HostStep:
     """luce_decode_step_host with its arguments marshalled once, for repeated
     steps over the same slots and buffers: each call copies the slots' current

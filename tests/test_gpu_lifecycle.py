@@ -188,3 +188,28 @@ def test_host_buffer_step_equals_device_step_bitwise(model):
     h2, _, a2 = step(model, [(k4, v4, L + 3)], [xr], [3])
     torch.cuda.synchronize()
     assert np.array_equal(bits(x_out.numpy()), bits(h2)) and np.array_equal(am_out.numpy(), a2)
+
+
+def test_prepared_device_step_equals_the_plain_call_bitwise(model):
+    """DeviceStep (luce_decode_step with its arguments marshalled once) gives
+    the plain call's bits, and follows the slot's len from call to call."""
+    L = 37
+    xr = rows(11, 3)
+    k1, v1 = cache(15, L)
+    h1, l1, a1 = step(model, [(k1, v1, L)], [xr], [3])
+    h2, l2, a2 = step(model, [(k1, v1, L + 3)], [xr], [3])
+    k2, v2 = cache(15, L)
+    x = cuda(xr)
+    logits = torch.empty((3, VOCAB), dtype=torch.float32, device="cuda")
+    am = torch.empty(3, dtype=torch.int32, device="cuda")
+    sl = luce.Slot(k2, v2, L)
+    ds = luce.DeviceStep(model, [sl], [3], x, model.workspace(3, CAP), logits=logits, argmax=am)
+    ds()
+    assert np.array_equal(bits(host(x)), bits(h1)) and np.array_equal(bits(host(logits)), bits(l1))
+    assert np.array_equal(host(am), a1)
+    x.copy_(cuda(xr))
+    sl.len = L + 3
+    ds()
+    assert np.array_equal(bits(host(x)), bits(h2)) and np.array_equal(host(am), a2)
+    assert np.array_equal(host(k1).view(np.uint16), host(k2).view(np.uint16))
+    assert np.array_equal(host(v1).view(np.uint16), host(v2).view(np.uint16))
