@@ -14,9 +14,9 @@ The lifecycle and paged tests elsewhere compare the GPU with other GPU runs
     host and attended by the oracle (2e-3 absolute), and a paged step checked
     stage by stage against the oracle over the gathered caches.
   * Composed steps at 8 and 12 rows (4 slots x 2 and x 3 rows), where every
-    projection runs on the tensor-core matvec and, at 12 rows, the q|k|v
-    projection is followed by its own RoPE/K-V launch: stage by stage
-    against the oracle, on the small stack and on the 27B-shaped layer.
+    projection runs on the tensor-core matvec and the q|k|v projection
+    applies RoPE and appends K/V in its epilogue: stage by stage against the
+    oracle, on the small stack and on the 27B-shaped layer.
 """
 import math
 import os
@@ -250,6 +250,7 @@ def test_wide_step_small_stack_stages_match_the_oracle(rows_per_slot):
 @pytest.mark.parametrize("rows_per_slot", [2, 3])
 def test_wide_step_27b_layer_stages_match_the_oracle(rows_per_slot):
     """8 and 12 rows through the 27B-shaped layer (every projection on the
-    tensor-core matvec; the 12-row q|k|v projection then its RoPE/K-V launch)."""
+    tensor-core matvec, the q|k|v projection with RoPE and the K/V append in
+    its epilogue)."""
     case = Case(1, wl.LAYER27B, 1, [2050 - rows_per_slot] * 4, [rows_per_slot] * 4, cap=2050)
     staged_layer_check(case, case.run())
