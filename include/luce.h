@@ -82,10 +82,12 @@ uint64_t luce_launch_count(void);
  * partial outputs).
  *
  * A non-zero count means the device context is suspect, not that some
- * outputs were merely skipped: the CTA whose wait expired stops writing and
- * may exit while tensor copies it issued are still in flight, and such a
- * copy can land in shared memory that later belongs to another CTA.  Treat
- * every result computed since the last zero reading as untrusted and
+ * outputs were merely skipped: the CTA whose wait expired stops writing;
+ * before it exits it waits once more, again for about one second, for the
+ * tensor copies it issued (and an attention CTA for its MMAs, before it
+ * frees their tensor memory), and if that wait expires too (counted again)
+ * a late copy can land in shared memory that later belongs to another CTA.
+ * Treat every result computed since the last zero reading as untrusted and
  * recreate the context.  The decode step entry points return LUCE_OK
  * without looking at this counter (reading it synchronises the device):
  * callers that need the guarantee poll it after their steps.

@@ -676,6 +676,9 @@ attn_slot_kernel(const float* __restrict__ q, int64_t ldq, AttnRows rows, AttnGr
             for (int h = 0; h < GQ; ++h) pout[(size_t)h * kPartStride + d] = o[ri][h];
         }
     }
+    // after an expired wait the MMAs may still be writing the accumulator:
+    // wait once more (bounded) before its tensor memory is freed
+    if (!ok && tid == 0) mbar_wait(&mbar, 0, &g_attn_wait_timeouts);
     tc_fence_before();
     __syncthreads();  // every read of the accumulator is done
     if (warp == 0)

@@ -48,7 +48,8 @@
 //
 // Every wait is bounded (about one second, ring.cuh); an expired wait adds one
 // to this file's device counter (read by luce_wait_timeouts) and the CTA
-// writes no further outputs.
+// writes no further outputs.  The producer drains its last stages' copies
+// (ring_drain, bounded) before it returns.
 #include <string.h>
 
 #include <atomic>
@@ -254,13 +255,15 @@ __device__ __forceinline__ void mma_produce(const MmaSmem<NT, TL, S, CW, H>& R, 
     }
     pdl_wait();
     for (int it = 0; it < pre; ++it) load_a(it);
-    for (int it = pre; it < total; ++it) {
-        const int s = it % S;
+    int issued = pre;
+    for (; issued < total; ++issued) {
+        const int it = issued, s = it % S;
         if (!mbar_wait(&R.empty[s], ((it / S) - 1) & 1, &g_mma_wait_timeouts)) break;
         mbar_expect_tx(&R.full[s], bytes(it));
         load_w(it);
         load_a(it);
     }
+    ring_drain<S>(R.full, issued, &g_mma_wait_timeouts);
 }
 
 // A consumer warp's chains for one group: stages it .. it + nj - 1 (it

@@ -33,7 +33,9 @@
 //
 // Every wait is bounded (about one second on the global timer, 2^26 polls);
 // a wait that expires adds one to a device counter (luce_wait_timeouts) and
-// the CTA stops consuming, leaving its remaining outputs unwritten.
+// the CTA stops consuming, leaving its remaining outputs unwritten; the
+// producer drains its last stages' copies (ring_drain, bounded) before it
+// returns.
 #include <string.h>
 
 #include <atomic>
@@ -172,13 +174,15 @@ __device__ __forceinline__ void ring_produce(const RingSmem<T, G, S>& R, int tot
     }
     pdl_wait();
     for (int it = 0; it < pre; ++it) load_acts(it);
-    for (int it = pre; it < total; ++it) {
-        const int s = it % S;
+    int issued = pre;
+    for (; issued < total; ++issued) {
+        const int it = issued, s = it % S;
         if (!mbar_wait(&R.empty[s], ((it / S) - 1) & 1, &g_wait_timeouts)) break;
         mbar_expect_tx(&R.full[s], (uint32_t)(weight_bytes(it) + L::A + L::AD));
         load_weights(it, R.slots + s * L::STAGE, &R.full[s]);
         load_acts(it);
     }
+    ring_drain<S>(R.full, issued, &g_wait_timeouts);
 }
 
 // A consumer lane's chains for one group: stages it .. it + nj - 1 (it

@@ -71,6 +71,29 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, unsigned
     return true;
 }
 
+// Before a ring's producer thread returns: wait for the copies of the last
+// stages it issued (stage it went to slot it % S, phase parity (it / S) & 1;
+// no later phase of those slots follows), for kWaitLimitNs in all, so that
+// no tensor copy is still landing in this CTA's shared memory once the CTA
+// may exit - also after a consumer's or the producer's own wait expired.  On
+// a healthy run the consumers wait for the same phases, so this waits for
+// nothing they do not; it polls with a short sleep in between, leaving the
+// issue slots to the consumer warps.  An expiry here is counted like any
+// other.
+template <int S>
+__device__ __forceinline__ void ring_drain(uint64_t* full, int issued, unsigned int* counter)
+{
+    const uint64_t t0 = global_ns();
+    for (int it = issued > S ? issued - S : 0; it < issued; ++it)
+        for (uint32_t polls = 0; !mbar_try(&full[it % S], (it / S) & 1); ++polls) {
+            if (global_ns() - t0 > kWaitLimitNs || polls >= (1u << 22)) {
+                atomicAdd(counter, 1u);
+                return;
+            }
+            __nanosleep(128);
+        }
+}
+
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, int x, int y, int z, uint64_t* bar)
 {
     asm volatile(
